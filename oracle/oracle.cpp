@@ -1,0 +1,247 @@
+// Grouped matrix multiplication oracle: TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, fp64 CPU statement of what the grouped matmul computes.  It is
+// used by the tests, by __graft_entry__.smoke() and by the CPU-baseline leg of
+// bench.py to check and time the CUDA library; nothing in the product path may
+// link or call it.  It shares no code, header, table or helper with the CUDA
+// library.
+//
+// Sources (page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230",
+// files tpu_inference/kernels/megablox/gmm.py and common.py):
+//   * gmm docstring: row block of group i of lhs [m,k] times the group's rhs;
+//     rhs is [num_groups, n, k] and the contraction is over the last dim of both
+//     operands (the dot_general in the kernel body contracts dim 1 with dim 1).
+//   * make_group_metadata: group offsets are the exclusive cumulative sum of
+//     group_sizes (CSR-style row offsets).
+//   * kernel body (_accum): fp32 accumulation; on the last k tile of quant block
+//     b the block's partial sum is multiplied by rhs_scale[g, b, 0, n]; the bias
+//     rhs_bias[g, 0, n] is added once (with the first block).
+//   * rhs index is group_id - group_offset (rhs_transform_indices), and rows
+//     outside the groups [group_offset, group_offset + num_local_groups) are
+//     zero (_zero_uninitialized_memory).
+// Readings where the pages are silent (all of them listed in the design notes):
+//   * rows at or beyond sum(group_sizes) are zero;
+//   * negative group sizes count as 0 and offsets are capped at m;
+//   * transpose_rhs = 1 means rhs is [G, n, k] (the pages' layout), 0 means
+//     rhs is [G, k, n];
+//   * tgmm(lhs, dout)[g, k, n] = sum over the rows r of group g of
+//     lhs[r, k] * dout[r, n]; an empty group gives a zero block (the
+//     visit_empty_groups note in make_group_metadata).
+//
+// Every result is exact-product, fp64-sum.  Alongside the value `ref` the
+// oracle returns `mag`, the same sum taken over absolute values, which the
+// tolerance |gpu - ref| <= 1e-3 * mag + 2^-8 * |ref| is stated in.
+//
+// Pins: tests/test_oracle_pins.py checks this file against hand-worked values,
+// brute-force dense per-group products, the format definition of e4m3fn, and
+// the invariants of the method (zero tail rows, empty groups, NT == NN on the
+// transposed weight, tgmm == per-group lhs_g^T dout_g, group_offset slicing).
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+enum { DT_BF16 = 0, DT_F32 = 1, DT_E4M3 = 2 };
+
+// bfloat16: the top 16 bits of an IEEE binary32.
+double decode_bf16(uint16_t bits) {
+  uint32_t u = uint32_t(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return double(f);
+}
+
+double decode_f32(uint32_t bits) {
+  float f;
+  std::memcpy(&f, &bits, sizeof f);
+  return double(f);
+}
+
+// float8_e4m3fn (the dtype named in common.py's supported list): 1 sign bit,
+// 4 exponent bits with bias 7, 3 mantissa bits, no infinities; exponent 15
+// with mantissa 7 is NaN.  Exponent 0 encodes subnormals m/8 * 2^-6.
+double decode_e4m3fn(uint8_t code) {
+  const int s = code >> 7;
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = (e == 0) ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+double load(const void* base, int dtype, int64_t idx) {
+  switch (dtype) {
+    case DT_BF16: return decode_bf16(static_cast<const uint16_t*>(base)[idx]);
+    case DT_F32: return decode_f32(static_cast<const uint32_t*>(base)[idx]);
+    case DT_E4M3: return decode_e4m3fn(static_cast<const uint8_t*>(base)[idx]);
+  }
+  return std::nan("");
+}
+
+bool valid_dtype(int d) { return d == DT_BF16 || d == DT_F32 || d == DT_E4M3; }
+
+int resolve_threads(int threads) {
+  if (threads > 0) return threads;
+  unsigned hc = std::thread::hardware_concurrency();
+  return hc ? int(hc) : 1;
+}
+
+// Runs body(i) for i in [0, count) on `threads` workers (dynamic hand-out).
+template <class F>
+void parallel_for(int64_t count, int threads, F body) {
+  threads = std::max(1, std::min<int>(threads, int(std::min<int64_t>(count, 1 << 20))));
+  if (threads <= 1) {
+    for (int64_t i = 0; i < count; ++i) body(i);
+    return;
+  }
+  std::atomic<int64_t> next{0};
+  std::vector<std::thread> pool;
+  for (int t = 0; t < threads; ++t)
+    pool.emplace_back([&] {
+      for (int64_t i = next++; i < count; i = next++) body(i);
+    });
+  for (auto& th : pool) th.join();
+}
+
+// offs[0] = 0, offs[g+1] = offs[g] + max(group_sizes[g], 0), capped at m.
+void group_offsets(const int32_t* sizes, int32_t groups, int64_t m, std::vector<int64_t>& offs) {
+  offs.assign(size_t(groups) + 1, 0);
+  for (int32_t g = 0; g < groups; ++g) {
+    int64_t s = sizes[g] > 0 ? sizes[g] : 0;
+    offs[g + 1] = std::min<int64_t>(offs[g] + s, m);
+  }
+}
+
+// The group that owns row r, or -1 when r lies at or past the last offset.
+int32_t owning_group(const std::vector<int64_t>& offs, int64_t r) {
+  const int32_t groups = int32_t(offs.size()) - 1;
+  for (int32_t g = 0; g < groups; ++g)
+    if (offs[g] <= r && r < offs[g + 1]) return g;
+  return -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_default_threads(void) { return resolve_threads(0); }
+
+void oracle_group_offsets(const int32_t* group_sizes, int32_t num_groups, int64_t m, int64_t* offs_out) {
+  std::vector<int64_t> offs;
+  group_offsets(group_sizes, num_groups, m, offs);
+  std::copy(offs.begin(), offs.end(), offs_out);
+}
+
+// Forward grouped matmul.
+//   lhs        [m, k]                          (lhs_dtype)
+//   rhs        [L, n, k] if transpose_rhs else [L, k, n]   (rhs_dtype), L = num_local_groups
+//   group_sizes[num_total_groups] int32; local groups are
+//              [group_offset, group_offset + L) and use rhs[g - group_offset]
+//   rhs_scale  NULL or [L, num_blocks, 1, n] f32; block b covers
+//              k in [b*k/num_blocks, (b+1)*k/num_blocks)
+//   rhs_bias   NULL or [L, 1, n] (bias_dtype)
+//   rows       NULL: compute every row 0..m-1; else the listed row indices
+//   ref, mag   [num_rows, n] fp64 outputs (num_rows = m when rows is NULL)
+// Returns 0, or -1 on an argument it cannot interpret.
+int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+               int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+               int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_blocks,
+               const void* rhs_bias, int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref,
+               double* mag, int threads) {
+  if (!valid_dtype(lhs_dtype) || !valid_dtype(rhs_dtype)) return -1;
+  if (rhs_bias && !valid_dtype(bias_dtype)) return -1;
+  if (m < 0 || k < 0 || n < 0 || num_local_groups < 0 || num_total_groups < 0) return -1;
+  if (group_offset < 0 || group_offset + num_local_groups > num_total_groups) return -1;
+  const int32_t nb = rhs_scale ? num_blocks : 1;
+  if (nb <= 0 || (k % nb) != 0) return -1;
+  const int64_t block = nb ? k / nb : k;
+
+  std::vector<int64_t> offs;
+  group_offsets(group_sizes, num_total_groups, m, offs);
+  const int64_t count = rows ? num_rows : m;
+
+  parallel_for(count, resolve_threads(threads), [&](int64_t i) {
+    const int64_t r = rows ? rows[i] : i;
+    double* ref_row = ref + i * n;
+    double* mag_row = mag + i * n;
+    const int32_t g = (r >= 0 && r < m) ? owning_group(offs, r) : -1;
+    if (g < group_offset || g >= group_offset + num_local_groups) {
+      for (int64_t c = 0; c < n; ++c) ref_row[c] = mag_row[c] = 0.0;
+      return;
+    }
+    const int64_t gl = g - group_offset;  // index into the local rhs slice
+    std::vector<double> a(static_cast<size_t>(k));
+    for (int64_t kk = 0; kk < k; ++kk) a[kk] = load(lhs, lhs_dtype, r * k + kk);
+    for (int64_t c = 0; c < n; ++c) {
+      double acc = 0.0, acc_abs = 0.0;
+      for (int32_t b = 0; b < nb; ++b) {
+        double part = 0.0, part_abs = 0.0;
+        for (int64_t kk = b * block; kk < (b + 1) * block; ++kk) {
+          const int64_t widx = transpose_rhs ? (gl * n + c) * k + kk : (gl * k + kk) * n + c;
+          const double w = load(rhs, rhs_dtype, widx);
+          part += a[kk] * w;
+          part_abs += std::fabs(a[kk] * w);
+        }
+        const double s = rhs_scale ? double(rhs_scale[(gl * nb + b) * n + c]) : 1.0;
+        acc += s * part;
+        acc_abs += std::fabs(s) * part_abs;
+      }
+      if (rhs_bias) {
+        const double bias = load(rhs_bias, bias_dtype, gl * n + c);
+        acc += bias;
+        acc_abs += std::fabs(bias);
+      }
+      ref_row[c] = acc;
+      mag_row[c] = acc_abs;
+    }
+  });
+  return 0;
+}
+
+// Backward weight gradient: out[g, kk, c] = sum_{r in group g} lhs[r, kk] * dout[r, c].
+//   lhs  [m, k], dout [m, n]; out blocks [num_groups, k, n] (every group,
+//   empty ones all-zero).
+//   k_rows NULL: every kk in 0..k-1; else the listed kk (the same list for
+//   every group); ref, mag are [num_groups, num_k_rows, n].
+int oracle_tgmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* dout, int dout_dtype,
+                int64_t n, const int32_t* group_sizes, int32_t num_groups, const int64_t* k_rows,
+                int64_t num_k_rows, double* ref, double* mag, int threads) {
+  if (!valid_dtype(lhs_dtype) || !valid_dtype(dout_dtype)) return -1;
+  if (m < 0 || k < 0 || n < 0 || num_groups < 0) return -1;
+  std::vector<int64_t> offs;
+  group_offsets(group_sizes, num_groups, m, offs);
+  const int64_t kc = k_rows ? num_k_rows : k;
+
+  parallel_for(int64_t(num_groups) * kc, resolve_threads(threads), [&](int64_t job) {
+    const int64_t g = job / kc;
+    const int64_t j = job % kc;
+    const int64_t kk = k_rows ? k_rows[j] : j;
+    double* ref_row = ref + (g * kc + j) * n;
+    double* mag_row = mag + (g * kc + j) * n;
+    for (int64_t c = 0; c < n; ++c) ref_row[c] = mag_row[c] = 0.0;
+    for (int64_t r = offs[g]; r < offs[g + 1]; ++r) {
+      const double a = load(lhs, lhs_dtype, r * k + kk);
+      for (int64_t c = 0; c < n; ++c) {
+        const double p = a * load(dout, dout_dtype, r * n + c);
+        ref_row[c] += p;
+        mag_row[c] += std::fabs(p);
+      }
+    }
+  });
+  return 0;
+}
+
+// Decodes `count` stored values of `dtype` into fp64 (used by the format pins).
+int oracle_decode(const void* src, int dtype, int64_t count, double* dst) {
+  if (!valid_dtype(dtype)) return -1;
+  for (int64_t i = 0; i < count; ++i) dst[i] = load(src, dtype, i);
+  return 0;
+}
+
+}  // extern "C"

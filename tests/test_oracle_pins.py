@@ -1,0 +1,329 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is checked against things that do not come from itself: hand-worked
+values (tests/golden/hand_worked.json), the e4m3fn and bf16 format definitions
+(and torch's independent decoders), brute-force dense per-group products written
+separately here, and the invariants of the grouped matmul:
+  I0 brute force over every composition of m rows into G groups (zeros included)
+  I1 rows at or past sum(group_sizes) are zero
+  I2 an empty group contributes nothing
+  I3 NT on W equals NN on an explicitly transposed W, bit for bit
+  I4 tgmm equals the per-group lhs_g^T dout_g; summed over groups it is lhs^T dout
+  I5 group_offset selects the expert slice; shards add up to the full result
+  I6 integer-valued inputs give exact results
+  I7 special cases: one group is a dense matmul, unit scale is no scale,
+     power-of-two scales are exact, and mag is the result on |inputs|.
+Definitions: page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230",
+tpu_inference/kernels/megablox/gmm.py (gmm docstring, _accum, make_group_metadata,
+rhs_transform_indices, _zero_uninitialized_memory) and common.py (dtype list).
+"""
+
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def bf16_bits(x) -> np.ndarray:
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.uint16).numpy()
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(bits.copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rand_bf16(rng, shape, scale=1.0):
+    return bf16_bits(rng.standard_normal(shape) * scale)
+
+
+# ------------------------------------------------------------------ golden
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden()["gmm"], ids=lambda c: c["name"])
+def test_hand_worked_gmm(case):
+    lhs = bf16_bits(case["lhs"])
+    if "rhs_e4m3_codes" in case:
+        rhs = np.asarray(case["rhs_e4m3_codes"], dtype=np.uint8)
+    else:
+        rhs = bf16_bits(case["rhs"])
+    scale = None if "rhs_scale" not in case else np.asarray(case["rhs_scale"], np.float32)
+    bias = None if "rhs_bias" not in case else bf16_bits(case["rhs_bias"])
+    ref, mag = oracle.gmm(lhs, rhs, np.asarray(case["group_sizes"]), transpose_rhs=case["transpose_rhs"],
+                          group_offset=case["group_offset"], rhs_scale=scale, rhs_bias=bias)
+    np.testing.assert_array_equal(ref, np.asarray(case["ref"], np.float64))
+    np.testing.assert_array_equal(mag, np.asarray(case["mag"], np.float64))
+
+
+@pytest.mark.parametrize("case", _golden()["tgmm"], ids=lambda c: c["name"])
+def test_hand_worked_tgmm(case):
+    ref, mag = oracle.tgmm(bf16_bits(case["lhs"]), bf16_bits(case["dout"]), np.asarray(case["group_sizes"]))
+    np.testing.assert_array_equal(ref, np.asarray(case["ref"], np.float64))
+    np.testing.assert_array_equal(mag, np.asarray(case["mag"], np.float64))
+
+
+# ------------------------------------------------------------------ formats
+def test_e4m3fn_all_codes_match_format_definition_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode(codes)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(got)
+    assert set(np.flatnonzero(nan)) == {0x7F, 0xFF}, "e4m3fn has exactly two NaN codes"
+    np.testing.assert_array_equal(got[~nan], lib[~nan])
+    assert np.isnan(lib[nan]).all()
+    # values fixed by the format: bias 7, 3 mantissa bits, subnormals at 2^-6 * m/8
+    assert got[0x38] == 1.0 and got[0x40] == 2.0 and got[0xB8] == -1.0
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+    assert got[0x01] == 2.0 ** -9 and got[0x07] == 7 * 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert got[0x00] == 0.0 and np.signbit(got[0x80])
+
+
+def test_bf16_all_codes_match_torch():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode(codes)
+    lib = bf16_values(codes)
+    nan = np.isnan(lib)
+    assert (np.isnan(got) == nan).all()
+    np.testing.assert_array_equal(got[~nan], lib[~nan])
+
+
+# ------------------------------------------------------------------ brute force (I0)
+def brute_force_gmm(lhs_v, w_v, sizes, transpose_rhs, group_offset=0, scale=None, bias_v=None):
+    """Dense per-group products, written independently of the oracle: gather the group's
+    rows into a matrix and multiply by the group's weight with numpy (fp64)."""
+    m, k = lhs_v.shape
+    L = w_v.shape[0]
+    n = w_v.shape[1] if transpose_rhs else w_v.shape[2]
+    out = np.zeros((m, n))
+    start = 0
+    for g, s in enumerate(sizes):
+        s = max(int(s), 0)
+        stop = min(start + s, m)
+        if group_offset <= g < group_offset + L and stop > start:
+            wg = w_v[g - group_offset]
+            wg_nk = wg if transpose_rhs else wg.T  # [n, k]
+            rows = lhs_v[start:stop]
+            if scale is None:
+                res = rows @ wg_nk.T
+            else:
+                nb = scale.shape[1]
+                bs = k // nb
+                res = np.zeros((stop - start, n))
+                for b in range(nb):
+                    res += (rows[:, b * bs:(b + 1) * bs] @ wg_nk[:, b * bs:(b + 1) * bs].T) * scale[g - group_offset, b, 0]
+            if bias_v is not None:
+                res = res + bias_v[g - group_offset, 0]
+            out[start:stop] = res
+        start = stop
+    return out
+
+
+def compositions(total, parts):
+    for cuts in itertools.combinations_with_replacement(range(total + 1), parts - 1):
+        edges = (0,) + cuts + (total,)
+        yield [edges[i + 1] - edges[i] for i in range(parts)]
+
+
+@pytest.mark.parametrize("transpose_rhs", [True, False])
+def test_brute_force_every_composition(transpose_rhs):
+    rng = np.random.default_rng(7)
+    m, k, n, G = 6, 24, 5, 3
+    lhs = rand_bf16(rng, (m, k))
+    w = rand_bf16(rng, (G, n, k) if transpose_rhs else (G, k, n), 0.25)
+    lhs_v, w_v = bf16_values(lhs), bf16_values(w)
+    count = 0
+    for total in range(m + 1):  # sums below m leave tail rows (I1)
+        for sizes in compositions(total, G):
+            ref, mag = oracle.gmm(lhs, w, np.array(sizes), transpose_rhs=transpose_rhs)
+            np.testing.assert_allclose(ref, brute_force_gmm(lhs_v, w_v, sizes, transpose_rhs), rtol=1e-12, atol=1e-12)
+            count += 1
+    assert count == sum(len(list(compositions(t, G))) for t in range(m + 1))
+
+
+def test_brute_force_with_torch_matmul_as_library_routine():
+    rng = np.random.default_rng(8)
+    m, k, n, G = 40, 64, 24, 4
+    sizes = [9, 0, 20, 8]  # sum 37 < m
+    lhs = rand_bf16(rng, (m, k))
+    w = rand_bf16(rng, (G, n, k), 0.1)
+    ref, _ = oracle.gmm(lhs, w, np.array(sizes))
+    lt = torch.from_numpy(bf16_values(lhs))
+    wt = torch.from_numpy(bf16_values(w))
+    start = 0
+    for g, s in enumerate(sizes):
+        if s:
+            exp = torch.matmul(lt[start:start + s], wt[g].T).numpy()
+            np.testing.assert_allclose(ref[start:start + s], exp, rtol=1e-12, atol=1e-12)
+        start += s
+    assert (ref[start:] == 0).all()
+
+
+def test_scale_and_bias_against_brute_force():
+    rng = np.random.default_rng(9)
+    m, k, n, G, nb = 20, 64, 12, 3, 4
+    sizes = [7, 0, 11]
+    lhs = rand_bf16(rng, (m, k))
+    w = rand_bf16(rng, (G, n, k), 0.3)
+    scale = rng.uniform(-2, 2, (G, nb, 1, n)).astype(np.float32)
+    bias = rand_bf16(rng, (G, 1, n))
+    ref, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_scale=scale, rhs_bias=bias)
+    exp = brute_force_gmm(bf16_values(lhs), bf16_values(w), sizes, True, scale=scale.astype(np.float64),
+                          bias_v=bf16_values(bias))
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_weights_with_scale_against_brute_force():
+    rng = np.random.default_rng(10)
+    m, k, n, G, nb = 16, 256, 8, 2, 2
+    sizes = [5, 9]
+    lhs = rand_bf16(rng, (m, k))
+    codes = torch.from_numpy(np.clip(rng.standard_normal((G, n, k)) * 40, -448, 448).astype(np.float32))
+    w = codes.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    w_v = torch.from_numpy(w.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    scale = rng.uniform(0.5, 2, (G, nb, 1, n)).astype(np.float32) / 448
+    ref, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_scale=scale)
+    exp = brute_force_gmm(bf16_values(lhs), w_v, sizes, True, scale=scale.astype(np.float64))
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------ invariants
+def _case(seed=11, m=48, k=32, n=16, G=5, sizes=(10, 0, 13, 7, 12)):
+    rng = np.random.default_rng(seed)
+    return (rand_bf16(rng, (m, k)), rand_bf16(rng, (G, n, k), 0.2), np.array(sizes, np.int32), rng)
+
+
+def test_I1_rows_past_sum_are_zero():
+    lhs, w, sizes, _ = _case(sizes=(3, 0, 9, 1, 2))
+    ref, mag = oracle.gmm(lhs, w, sizes)
+    assert (ref[15:] == 0).all() and (mag[15:] == 0).all()
+    assert (np.abs(ref[:15]).sum(axis=1) > 0).all()
+
+
+def test_I2_inserting_an_empty_group_changes_nothing():
+    lhs, w, sizes, rng = _case()
+    ref, _ = oracle.gmm(lhs, w, sizes)
+    for pos in range(len(sizes) + 1):
+        junk = rand_bf16(rng, (1,) + w.shape[1:], 5.0)
+        ref2, _ = oracle.gmm(lhs, np.concatenate([w[:pos], junk, w[pos:]]), np.insert(sizes, pos, 0))
+        np.testing.assert_array_equal(ref, ref2)
+
+
+def test_I3_nt_equals_nn_on_transposed_weight_bitwise():
+    lhs, w, sizes, _ = _case()
+    a, am = oracle.gmm(lhs, w, sizes, transpose_rhs=True)
+    b, bm = oracle.gmm(lhs, np.ascontiguousarray(np.swapaxes(w, 1, 2)), sizes, transpose_rhs=False)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(am, bm)
+
+
+def test_I4_tgmm_is_per_group_product_and_sums_to_dense():
+    rng = np.random.default_rng(12)
+    m, k, n = 30, 12, 10
+    sizes = np.array([4, 0, 17, 9], np.int32)  # sum == m
+    lhs, dout = rand_bf16(rng, (m, k)), rand_bf16(rng, (m, n))
+    ref, _ = oracle.tgmm(lhs, dout, sizes)
+    lv, dv = bf16_values(lhs), bf16_values(dout)
+    start = 0
+    for g, s in enumerate(sizes):
+        np.testing.assert_allclose(ref[g], lv[start:start + s].T @ dv[start:start + s], rtol=1e-12, atol=1e-12)
+        start += s
+    assert (ref[1] == 0).all()
+    np.testing.assert_allclose(ref.sum(axis=0), lv.T @ dv, rtol=1e-12, atol=1e-12)
+
+
+def test_I5_group_offset_selects_slice_and_shards_sum_to_full():
+    lhs, w, sizes, _ = _case()
+    full, _ = oracle.gmm(lhs, w, sizes)
+    offs = oracle.group_offsets(sizes, lhs.shape[0])
+    acc = np.zeros_like(full)
+    for go, L in [(0, 2), (2, 1), (3, 2)]:
+        part, _ = oracle.gmm(lhs, w[go:go + L], sizes, group_offset=go)
+        lo, hi = offs[go], offs[go + L]
+        np.testing.assert_array_equal(part[lo:hi], full[lo:hi])
+        assert (part[:lo] == 0).all() and (part[hi:] == 0).all()
+        acc += part
+    np.testing.assert_array_equal(acc, full)
+
+
+def test_I6_integer_inputs_exact_and_each_row_uses_its_expert():
+    rng = np.random.default_rng(13)
+    m, k, n, G = 37, 256, 9, 4
+    sizes = np.array([11, 0, 20, 6], np.int32)
+    lhs_i = rng.integers(-8, 9, (m, k))
+    base = rng.integers(-8, 9, (n, k))
+    w_i = np.stack([(g + 1) * base for g in range(G)])
+    ref, _ = oracle.gmm(bf16_bits(lhs_i), bf16_bits(w_i), sizes)
+    start = 0
+    for g, s in enumerate(sizes):
+        for r in range(start, start + s):
+            exact = [int(np.dot(lhs_i[r].astype(object), w_i[g, c].astype(object))) for c in range(n)]
+            assert ref[r].tolist() == [float(v) for v in exact]
+        start += s
+    assert (ref[start:] == 0).all()
+
+
+def test_I7_one_group_is_dense_and_unit_scale_is_no_scale():
+    rng = np.random.default_rng(14)
+    m, k, n = 19, 64, 7
+    lhs, w = rand_bf16(rng, (m, k)), rand_bf16(rng, (1, n, k))
+    ref, _ = oracle.gmm(lhs, w, np.array([m]))
+    np.testing.assert_allclose(ref, bf16_values(lhs) @ bf16_values(w)[0].T, rtol=1e-12, atol=1e-12)
+    ones = np.ones((1, 4, 1, n), np.float32)
+    ref1, _ = oracle.gmm(lhs, w, np.array([m]), rhs_scale=ones)
+    np.testing.assert_allclose(ref1, ref, rtol=1e-14, atol=1e-14)
+    pow2 = np.full((1, 4, 1, n), 0.25, np.float32)
+    ref4, _ = oracle.gmm(lhs, w, np.array([m]), rhs_scale=pow2)
+    np.testing.assert_array_equal(ref4, ref1 * 0.25)
+
+
+def test_I7_mag_is_result_on_absolute_inputs():
+    rng = np.random.default_rng(15)
+    m, k, n, G, nb = 25, 64, 11, 3, 2
+    sizes = np.array([8, 9, 8], np.int32)
+    lhs, w = rand_bf16(rng, (m, k)), rand_bf16(rng, (G, n, k))
+    scale = rng.uniform(-1, 1, (G, nb, 1, n)).astype(np.float32)
+    bias = rand_bf16(rng, (G, 1, n))
+    _, mag = oracle.gmm(lhs, w, sizes, rhs_scale=scale, rhs_bias=bias)
+    absb = lambda b: bf16_bits(np.abs(bf16_values(b)))
+    ref_abs, _ = oracle.gmm(absb(lhs), absb(w), sizes, rhs_scale=np.abs(scale), rhs_bias=absb(bias))
+    np.testing.assert_allclose(mag, ref_abs, rtol=1e-12, atol=0)
+
+
+def test_sampled_rows_and_k_rows_match_full_runs():
+    lhs, w, sizes, rng = _case()
+    full, fmag = oracle.gmm(lhs, w, sizes)
+    rows = np.array([0, 5, 9, 10, 22, 23, 40, 47])
+    part, pmag = oracle.gmm(lhs, w, sizes, rows=rows)
+    np.testing.assert_array_equal(part, full[rows])
+    np.testing.assert_array_equal(pmag, fmag[rows])
+    dout = rand_bf16(rng, (lhs.shape[0], 6))
+    t_full, _ = oracle.tgmm(lhs, dout, sizes)
+    kr = np.array([1, 7, 31])
+    t_part, _ = oracle.tgmm(lhs, dout, sizes, k_rows=kr)
+    np.testing.assert_array_equal(t_part, t_full[:, kr])
+
+
+def test_negative_sizes_count_as_zero_and_offsets_cap_at_m():
+    offs = oracle.group_offsets(np.array([3, -2, 5, 100], np.int32), 10)
+    assert offs.tolist() == [0, 3, 3, 8, 10]
+    lhs, w, _, _ = _case(G=4, sizes=(0, 0, 0, 0))
+    ref_neg, _ = oracle.gmm(lhs, w, np.array([5, -7, 30, 40], np.int32))
+    ref_pos, _ = oracle.gmm(lhs, w, np.array([5, 0, 30, 13], np.int32))
+    np.testing.assert_array_equal(ref_neg, ref_pos)
+
+
+def test_rejects_bad_arguments():
+    lhs, w, sizes, _ = _case()
+    with pytest.raises(ValueError):
+        oracle.gmm(lhs, w, sizes, group_offset=3)  # 3 + 5 local groups > 5 total
+    with pytest.raises(ValueError):
+        oracle.gmm(lhs, w, sizes, rhs_scale=np.ones((5, 3, 1, 16), np.float32))  # k=32 not divisible by 3
