@@ -1,0 +1,138 @@
+/*
+ * libgmm: grouped matrix multiplication for GB300 (sm_103a).
+ *
+ * The rows of lhs [m, k] are split into consecutive groups by an int32
+ * group_sizes vector; each group is multiplied by its own expert weight from
+ * a 3-D rhs.  Definitions follow the page "tpu-inference 0.12.0.dev20251213
+ * -> 0.13.2.dev20251230", file tpu_inference/kernels/megablox/gmm.py (the gmm
+ * signature and docstring, _validate_args, _accum, make_group_metadata,
+ * rhs_transform_indices and _zero_uninitialized_memory), and the page
+ * "Megablox: transposed-RHS gmm_v2 kernel for the backward dlhs" (Context
+ * section: dlhs = dout @ W^T read from the untransposed [groups, n, k]
+ * weight; drhs per group).
+ *
+ * Conventions shared by every call:
+ *  - Every tensor argument is a DEVICE pointer to a dense row-major array
+ *    owned by the caller.  The library never allocates, frees or
+ *    synchronises inside gmm() / tgmm(); work is enqueued on `stream` (a
+ *    cudaStream_t; NULL is the legacy default stream) and runs
+ *    asynchronously.
+ *  - Host-checkable argument errors return a status below before anything is
+ *    launched; outputs are then untouched.
+ *  - Errors that only the device can see (bad group_sizes, an internal wait
+ *    that timed out) set sticky flags in the workspace; the call still
+ *    completes, treating negative sizes as 0 and cutting the groups at row m.
+ *    Read them with gmm_read_device_errors().
+ *  - The workspace is caller-owned device memory of at least
+ *    gmm_workspace_bytes() bytes, 256-byte aligned, zero-filled once before
+ *    its first use.  Calls that share a workspace must be stream-ordered.
+ *  - Requires the current device to be compute capability 10.3 (GB300).
+ */
+#ifndef LIBGMM_H_
+#define LIBGMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types (stored layout). */
+enum {
+  GMM_DTYPE_BF16 = 0, /* bfloat16 */
+  GMM_DTYPE_F32 = 1,  /* IEEE binary32 */
+  GMM_DTYPE_E4M3 = 2  /* float8_e4m3fn: bias 7, no infinities, 0x7F/0xFF NaN */
+};
+
+/* Status codes returned by every entry point. */
+enum {
+  GMM_OK = 0,
+  GMM_ERR_NULL = 1,         /* a required pointer is NULL */
+  GMM_ERR_DTYPE = 2,        /* dtype combination not supported */
+  GMM_ERR_SHAPE = 3,        /* inconsistent or unsupported sizes */
+  GMM_ERR_ALIGN = 4,        /* a pointer is not 16-byte aligned or a row pitch is not a multiple of 16 bytes */
+  GMM_ERR_GROUP_OFFSET = 5, /* group_offset outside [0, num_total_groups - num_local_groups] */
+  GMM_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or smaller than gmm_workspace_bytes() */
+  GMM_ERR_ARCH = 7,         /* current device is not compute capability 10.3 */
+  GMM_ERR_CUDA = 8          /* a CUDA runtime or driver call failed; see gmm_last_cuda_error() */
+};
+
+/* Sticky device-side error flags kept in the workspace. */
+#define GMM_DEVERR_NEGATIVE_GROUP_SIZE 0x1u /* some group_sizes[g] < 0 (counted as 0) */
+#define GMM_DEVERR_GROUP_SIZES_EXCEED_M 0x2u /* sum(group_sizes) > m (groups cut at row m) */
+#define GMM_DEVERR_TIMEOUT 0x4u              /* an internal pipeline wait gave up; output is undefined */
+
+/* Largest num_total_groups (gmm) or num_groups (tgmm) accepted. */
+#define GMM_MAX_GROUPS 1024
+
+/* Size in bytes of the workspace every call needs (a small constant). */
+size_t gmm_workspace_bytes(void);
+
+/*
+ * Forward grouped matmul (page "tpu-inference ...", gmm.py: gmm).
+ *
+ *   For every local group g in [group_offset, group_offset + num_local_groups)
+ *   and every row r of that group (rows offs[g] <= r < offs[g+1], offs the
+ *   exclusive prefix sum of group_sizes):
+ *     out[r, c] = sum_b  s[g', b, c] * sum_{kk in block b} lhs[r, kk] * W(g', c, kk)
+ *                 + bias[g', c]                                  (g' = g - group_offset)
+ *   with fp32 accumulation and one rounding to out_dtype.  Every other row of
+ *   out (rows of non-local groups, rows at or past sum(group_sizes)) is set to 0:
+ *   out is fully overwritten.
+ *
+ *   lhs          [m, k], lhs_dtype must be GMM_DTYPE_BF16.
+ *   rhs          transpose_rhs != 0: [num_local_groups, n, k] (the pages' layout,
+ *                W(g, c, kk) = rhs[g, c, kk]); transpose_rhs == 0: [num_local_groups, k, n].
+ *                rhs_dtype GMM_DTYPE_BF16, or GMM_DTYPE_E4M3 (transpose_rhs != 0 only).
+ *   group_sizes  device int32 [num_total_groups], 1 <= num_total_groups <= GMM_MAX_GROUPS.
+ *   group_offset first local group; 0 <= group_offset <= num_total_groups - num_local_groups.
+ *   rhs_scale    NULL (s = 1, one block) or device f32 [num_local_groups, num_quant_blocks, 1, n];
+ *                block b covers kk in [b*k/nb, (b+1)*k/nb); k % num_quant_blocks == 0.
+ *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
+ *   out          [m, n] of out_dtype (BF16 or F32).
+ *   Sizes: m >= 0, k >= 8, n >= 8, k % 8 == 0, n % 8 == 0 (16-byte rows); lhs, rhs,
+ *   out and bias 16-byte aligned.  Row counts and offsets must fit in int32.
+ *   Returns GMM_OK or an error status above.
+ */
+int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+        int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+        int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+        const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
+        size_t workspace_bytes, void* stream);
+
+/*
+ * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS
+ * gmm_v2 kernel ...", Context section; gmm.py make_group_metadata docstring on
+ * visiting empty groups so that their output is zeroed).
+ *
+ *   out[g, kk, c] = sum_{r in group g} lhs[r, kk] * dout[r, c]   for every g,
+ *   fp32 accumulation, one rounding to out_dtype; empty groups give zero blocks.
+ *
+ *   lhs    [m, k] BF16;  dout [m, n] BF16;  out [num_groups, k, n] F32 or BF16.
+ *   group_sizes device int32 [num_groups], 1 <= num_groups <= GMM_MAX_GROUPS.
+ *   Sizes: m >= 0, k % 8 == 0, n % 8 == 0, k, n >= 8; pointers 16-byte aligned.
+ *   For an NT weight [G, n, k] the matching gradient is tgmm(dout, x): pass the
+ *   forward output gradient as `lhs` and the forward input as `dout`.
+ */
+int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
+         const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
+         size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the sticky device error flags
+ * (GMM_DEVERR_*) of `workspace` into *flags.  Returns GMM_OK or GMM_ERR_CUDA.
+ */
+int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags);
+
+/* Static English text for a status code. */
+const char* gmm_status_string(int status);
+
+/* The cudaError_t behind the last GMM_ERR_CUDA returned on this thread (0 if none). */
+int gmm_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBGMM_H_ */

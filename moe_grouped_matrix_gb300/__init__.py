@@ -1,0 +1,174 @@
+"""Grouped matrix multiplication (gmm / NT gmm / tgmm) for GB300, behind the C ABI of libgmm.
+
+This module only marshals arguments: every step of the computation runs in
+the CUDA kernels of ``libgmm.so`` (sources in ``csrc/``, ABI in
+``include/libgmm.h``).  PyTorch supplies device memory and streams.  If the
+library is not built, importing the ops raises: there is no fallback.
+
+    gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True,
+        group_offset=0, out=None, out_dtype=torch.bfloat16)
+    tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32)
+
+Definitions: page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230",
+tpu_inference/kernels/megablox/gmm.py (gmm), and page "Megablox:
+transposed-RHS gmm_v2 kernel for the backward dlhs" (NT dlhs, drhs).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["gmm", "tgmm", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
+           "DEVERR_NEGATIVE_GROUP_SIZE", "DEVERR_GROUP_SIZES_EXCEED_M", "DEVERR_TIMEOUT"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
+
+DTYPE_BF16, DTYPE_F32, DTYPE_E4M3 = 0, 1, 2
+DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+
+_TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3}
+
+_lock = threading.Lock()
+_lib = None
+_workspaces: dict[int, torch.Tensor] = {}
+
+# Every function the header declares, with its ctypes signature.
+_P, _I, _I32, _I64, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
+                                  ctypes.POINTER(ctypes.c_uint32))
+SIGNATURES = {
+    "gmm_workspace_bytes": ([], _SZ),
+    "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
+    "tgmm": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _P, _I, _P, _SZ, _P], _I),
+    "gmm_read_device_errors": ([_P, _P, _U32P], _I),
+    "gmm_status_string": ([_I], ctypes.c_char_p),
+    "gmm_last_cuda_error": ([], _I),
+}
+
+
+class GmmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        lib = load_library()
+        msg = lib.gmm_status_string(status).decode()
+        extra = f" (CUDA error {lib.gmm_last_cuda_error()})" if status == 8 else ""
+        super().__init__(f"{fn}: status {status}: {msg}{extra}")
+        self.status = status
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads libgmm.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with `python -m moe_grouped_matrix_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def workspace_for(device: torch.device) -> torch.Tensor:
+    """A zero-filled per-device workspace of gmm_workspace_bytes() bytes (cached)."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    ws = _workspaces.get(idx)
+    if ws is None:
+        nbytes = int(load_library().gmm_workspace_bytes())
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=torch.device("cuda", idx))
+        _workspaces[idx] = ws
+    return ws
+
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return _TORCH_TO_CODE[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _stream(device, stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
+        out_dtype=torch.bfloat16, workspace=None, stream=None):
+    """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
+    for each row r of local group g; all other rows of out are zero."""
+    lib = load_library()
+    _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
+    if group_sizes.dtype != torch.int32:
+        raise TypeError("group_sizes must be int32")
+    m, k = lhs.shape
+    n = rhs.shape[1] if transpose_rhs else rhs.shape[2]
+    kr = rhs.shape[2] if transpose_rhs else rhs.shape[1]
+    if kr != k:
+        raise ValueError(f"lhs has k={k} but rhs has k={kr}")
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
+    _dev(out, "out")
+    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    nb = 0
+    if rhs_scale is not None:
+        _dev(rhs_scale, "rhs_scale")
+        nb = rhs_scale.shape[1]
+    if rhs_bias is not None:
+        _dev(rhs_bias, "rhs_bias")
+    rc = lib.gmm(lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n,
+                 int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
+                 None if rhs_scale is None else rhs_scale.data_ptr(), nb,
+                 None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
+                 out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+    if rc != 0:
+        raise GmmError("gmm", rc)
+    return out
+
+
+def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=None, stream=None):
+    """out[g] = lhs_g^T @ dout_g for every group g (zero blocks for empty groups)."""
+    lib = load_library()
+    _dev(lhs, "lhs"), _dev(dout, "dout"), _dev(group_sizes, "group_sizes")
+    if group_sizes.dtype != torch.int32:
+        raise TypeError("group_sizes must be int32")
+    m, k = lhs.shape
+    if dout.shape[0] != m:
+        raise ValueError("lhs and dout must have the same number of rows")
+    n = dout.shape[1]
+    G = group_sizes.shape[0]
+    if out is None:
+        out = torch.empty((G, k, n), dtype=out_dtype, device=lhs.device)
+    _dev(out, "out")
+    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    rc = lib.tgmm(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(), G,
+                  out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+    if rc != 0:
+        raise GmmError("tgmm", rc)
+    return out
+
+
+def read_device_errors(device=None, workspace=None, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the sticky device error flags."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = workspace if workspace is not None else workspace_for(dev)
+    flags = ctypes.c_uint32(0)
+    rc = lib.gmm_read_device_errors(ws.data_ptr(), _stream(dev, stream), ctypes.byref(flags))
+    if rc != 0:
+        raise GmmError("gmm_read_device_errors", rc)
+    return int(flags.value)

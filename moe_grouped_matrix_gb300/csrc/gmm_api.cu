@@ -1,0 +1,251 @@
+// C ABI of libgmm: host-side validation, TMA tensor-map encoding and kernel
+// launch.  Argument rules follow the page "tpu-inference 0.12.0.dev20251213 ->
+// 0.13.2.dev20251230", gmm.py (_validate_args: lhs 2-D, rhs 3-D with matching
+// k, int32 group_sizes, rhs_scale [G, nb, 1, n], rhs_bias [G, 1, n]; gmm:
+// k // num_quant_blocks block width) plus the alignment rules of TMA.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/libgmm.h"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = 256;
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(int code) {
+  t_last_cuda_error = code;
+  return GMM_ERR_CUDA;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0, major = 0, minor = 0;
+  cudaError_t status = cudaSuccess;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::once_flag g_device_once[kMaxDevices];
+
+// Current device's SM count; GMM_ERR_ARCH unless it is compute capability 10.3.
+int current_device(DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return GMM_ERR_ARCH;
+  std::call_once(g_device_once[dev], [dev] {
+    DeviceInfo d;
+    d.status = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.status == cudaSuccess) d.status = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (d.status == cudaSuccess) d.status = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_devices[dev] = d;
+  });
+  *info = g_devices[dev];
+  if (info->status != cudaSuccess) return cuda_fail(info->status);
+  if (info->major != 10 || info->minor != 3) return GMM_ERR_ARCH;
+  return GMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tiled tensor map over a row-major array; dims are innermost first.
+int make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, int rank, const void* base,
+             const uint64_t* dims, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  uint64_t pitch = uint64_t(elem_bytes);
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = pitch;
+    pitch *= dims[i];
+  }
+  CUresult r = fn(map, dt, cuuint32_t(rank), const_cast<void*>(base), gdim, gstride, bdim, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(int(r));
+  return GMM_OK;
+}
+
+bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gmm_workspace_bytes(void) { return kWorkspaceBytes; }
+
+const char* gmm_status_string(int status) {
+  switch (status) {
+    case GMM_OK: return "ok";
+    case GMM_ERR_NULL: return "a required pointer is NULL";
+    case GMM_ERR_DTYPE: return "unsupported dtype combination";
+    case GMM_ERR_SHAPE: return "inconsistent or unsupported sizes";
+    case GMM_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case GMM_ERR_GROUP_OFFSET: return "group_offset out of range";
+    case GMM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GMM_ERR_ARCH: return "current device is not compute capability 10.3";
+    case GMM_ERR_CUDA: return "CUDA call failed";
+  }
+  return "unknown status";
+}
+
+int gmm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags) {
+  if (workspace == nullptr || flags == nullptr) return GMM_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(workspace, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GMM_OK;
+}
+
+int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+        int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+        int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+        const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+        void* stream) {
+  if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
+  if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  if (rhs_dtype != GMM_DTYPE_BF16 && rhs_dtype != GMM_DTYPE_E4M3) return GMM_ERR_DTYPE;
+  if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
+  if (rhs_bias != nullptr && bias_dtype != GMM_DTYPE_BF16 && bias_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
+  if (rhs_dtype == GMM_DTYPE_E4M3 && !transpose_rhs) return GMM_ERR_DTYPE;
+  if (!fits_i32(m) || !fits_i32(k) || !fits_i32(n) || k < 8 || n < 8 || k % 8 != 0 || n % 8 != 0)
+    return GMM_ERR_SHAPE;
+  if (num_total_groups < 1 || num_total_groups > GMM_MAX_GROUPS || num_local_groups < 1 ||
+      num_local_groups > num_total_groups)
+    return GMM_ERR_SHAPE;
+  if (group_offset < 0 || group_offset > num_total_groups - num_local_groups) return GMM_ERR_GROUP_OFFSET;
+  const bool scaled_path = rhs_dtype == GMM_DTYPE_E4M3 || rhs_scale != nullptr;
+  if (rhs_scale != nullptr) {
+    if (num_quant_blocks < 1 || k % num_quant_blocks != 0) return GMM_ERR_SHAPE;
+  }
+  if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || (rhs_bias && !aligned16(rhs_bias)) ||
+      (rhs_scale && !aligned16(rhs_scale)))
+    return GMM_ERR_ALIGN;
+  if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (int st = current_device(&dev)) return st;
+  if (m == 0) return GMM_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* err = static_cast<uint32_t*>(workspace);
+
+  if (scaled_path) return GMM_ERR_DTYPE;
+
+  gmmk::GemmLaunch L{};
+  {
+    const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
+    const uint32_t box[2] = {64, 128};
+    if (int st = make_map(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  if (transpose_rhs) {
+    const uint64_t dims[3] = {uint64_t(k), uint64_t(n), uint64_t(num_local_groups)};
+    const uint32_t box[3] = {64, 256, 1};
+    if (int st = make_map(&L.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, rhs, dims, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  } else {
+    const uint64_t dims[3] = {uint64_t(n), uint64_t(k), uint64_t(num_local_groups)};
+    const uint32_t box[3] = {64, 64, 1};
+    if (int st = make_map(&L.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, rhs, dims, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  L.group_sizes = group_sizes;
+  L.num_total_groups = num_total_groups;
+  L.group_offset = group_offset;
+  L.num_local_groups = num_local_groups;
+  L.m = int32_t(m);
+  L.n = int32_t(n);
+  L.k = int32_t(k);
+  L.out = out;
+  L.bias = rhs_bias;
+  L.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
+  L.err = err;
+  L.raster = 8;
+  // Work items = m-tiles x n-tiles must fit in int32.
+  const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
+  if (m_tiles_max * ((n + 255) / 256) > INT32_MAX) return GMM_ERR_SHAPE;
+  cudaError_t e = gmmk::launch_gemm_bf16(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GMM_OK;
+}
+
+int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
+         const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
+         size_t workspace_bytes, void* stream) {
+  if (lhs == nullptr || dout == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
+  if (lhs_dtype != GMM_DTYPE_BF16 || dout_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
+  if (!fits_i32(m) || !fits_i32(k) || !fits_i32(n) || k < 8 || n < 8 || k % 8 != 0 || n % 8 != 0)
+    return GMM_ERR_SHAPE;
+  if (num_groups < 1 || num_groups > GMM_MAX_GROUPS) return GMM_ERR_SHAPE;
+  if (!aligned16(lhs) || !aligned16(dout) || !aligned16(out)) return GMM_ERR_ALIGN;
+  if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
+  const int64_t items = int64_t(num_groups) * ((k + 127) / 128) * ((n + 255) / 256);
+  if (items > INT32_MAX) return GMM_ERR_SHAPE;
+  DeviceInfo dev;
+  if (int st = current_device(&dev)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  gmmk::TgmmLaunch L{};
+  // With m == 0 every group is empty and no copy is issued; the maps still
+  // need a non-zero extent.
+  const uint64_t rows = m > 0 ? uint64_t(m) : 1;
+  {
+    const uint64_t dims[2] = {uint64_t(k), rows};
+    const uint32_t box[2] = {64, 64};
+    if (int st = make_map(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  {
+    const uint64_t dims[2] = {uint64_t(n), rows};
+    const uint32_t box[2] = {64, 64};
+    if (int st = make_map(&L.tm_dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dout, dims, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  L.group_sizes = group_sizes;
+  L.num_groups = num_groups;
+  L.m = int32_t(m);
+  L.n = int32_t(n);
+  L.k = int32_t(k);
+  L.out = out;
+  L.err = static_cast<uint32_t*>(workspace);
+  cudaError_t e = gmmk::launch_tgmm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Host-side interface between the C ABI (gmm_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace gmmk {
+
+// Forward grouped matmul with bf16 operands (NT or NN weight layout).
+struct GemmLaunch {
+  CUtensorMap tm_lhs;  // lhs [m, k], box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_rhs;  // NT: [L, n, k] box {64, 256, 1};  NN: [L, k, n] box {64, 64, 1}
+  const int32_t* group_sizes;
+  int32_t num_total_groups, group_offset, num_local_groups;
+  int32_t m, n, k;
+  void* out;
+  const void* bias;  // NULL or [L, 1, n]
+  int32_t bias_f32;  // bias dtype: 1 = f32, 0 = bf16
+  uint32_t* err;
+  int32_t raster;  // n-tiles per L2 super-column
+};
+
+cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
+
+// tgmm: out[g] = lhs_g^T dout_g (bf16 operands, fp32 accumulate).
+struct TgmmLaunch {
+  CUtensorMap tm_lhs;   // lhs  [m, k], box {64, 64}
+  CUtensorMap tm_dout;  // dout [m, n], box {64, 64}
+  const int32_t* group_sizes;
+  int32_t num_groups;
+  int32_t m, n, k;
+  void* out;  // [G, k, n]
+  uint32_t* err;
+};
+
+cudaError_t launch_tgmm(const TgmmLaunch& p, bool out_f32, int grid, cudaStream_t stream);
+
+// Block-scaled grouped matmul for small groups (decode): rhs e4m3 or bf16
+// [L, n, k], per-(group, k-block, n) fp32 scale, optional bias.
+struct ScaledLaunch {
+  CUtensorMap tm_lhs;  // lhs [m, k] bf16, box {64, 16}
+  CUtensorMap tm_rhs;  // rhs [L, n, k]: e4m3 box {128, 128, 1} / bf16 box {64, 128, 1}
+  const int32_t* group_sizes;
+  int32_t num_total_groups, group_offset, num_local_groups;
+  int32_t m, n, k;
+  const float* scale;  // NULL or [L, nb, 1, n]
+  int32_t num_blocks;
+  const void* bias;
+  int32_t bias_f32;
+  void* out;
+  uint32_t* err;
+};
+
+cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
+
+}  // namespace gmmk

@@ -1,0 +1,302 @@
+// Backward weight gradient per group: out[g] = lhs_g^T @ dout_g.
+//
+// For every group g (page "Megablox: transposed-RHS gmm_v2 kernel for the
+// backward dlhs", Context: the drhs of the grouped matmul; page
+// "tpu-inference ...", gmm.py make_group_metadata: empty groups are still
+// visited so that their output is zeroed):
+//   out[g, kk, c] = sum_{r in group g} lhs[r, kk] * dout[r, c].
+// The contraction runs over the group's rows.  Both operands are read in
+// place from their row-major [rows, features] layout as MN-major tcgen05
+// operands (A = lhs_g^T: 128 lhs columns x 64 rows; B = dout_g: 256 dout
+// columns x 64 rows).  The last row chunk of a group may run into the next
+// group's rows; the MMA warp zeroes those rows in shared memory (both
+// operands) before issuing, so no other group's data enters the sum.
+//
+// Same CTA shape as the forward kernel: warp 0 TMA, warp 1 TMEM + MMA,
+// warps 2-5 epilogue (fp32 or bf16 stores of 128 x 256 output tiles; empty
+// groups' tiles are written as zeros without touching TMEM).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "worklist.cuh"
+
+namespace gmmk {
+namespace {
+
+constexpr int BM = 128;  // output rows (lhs columns)
+constexpr int BN = 256;  // output columns (dout columns)
+constexpr int BR = 64;   // contraction rows per stage
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 1024;
+constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64-feature x 64-row box
+constexpr uint32_t A_BYTES = (BM / 64) * BOX_BYTES;
+constexpr uint32_t B_BYTES = (BN / 64) * BOX_BYTES;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = STAGES * A_BYTES;
+constexpr uint32_t OFF_CTRL = STAGES * STAGE_BYTES;
+constexpr uint32_t OFF_FULL = OFF_CTRL;
+constexpr uint32_t OFF_EMPTY = OFF_FULL + 8 * STAGES;
+constexpr uint32_t OFF_ACCF = OFF_EMPTY + 8 * STAGES;
+constexpr uint32_t OFF_ACCE = OFF_ACCF + 16;
+constexpr uint32_t OFF_DONE = OFF_ACCE + 16;
+constexpr uint32_t OFF_TMEM = OFF_DONE + 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
+constexpr uint32_t OFF_OFFS = OFF_CTRL + 256;
+constexpr uint32_t SMEM_USED = OFF_OFFS + 4 * (kMaxGroups + 4);
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct Params {
+  const int32_t* group_sizes;
+  int32_t num_groups;
+  int32_t m, n, k;
+  void* out;
+  uint32_t* err;
+};
+
+template <bool kOutF32>
+__device__ __forceinline__ void store_chunk(const Params& p, int64_t out_row, int32_t col0, const float (&f)[32]) {
+  if constexpr (kOutF32) {
+    float* o = static_cast<float*>(p.out) + out_row * p.n + col0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (col0 + 4 * q < p.n)
+        st_global_v4(o + 4 * q, __float_as_uint(f[4 * q]), __float_as_uint(f[4 * q + 1]),
+                     __float_as_uint(f[4 * q + 2]), __float_as_uint(f[4 * q + 3]));
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + out_row * p.n + col0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (col0 + 8 * q < p.n)
+        st_global_v4(o + 8 * q, pack_bf16x2(f[8 * q], f[8 * q + 1]), pack_bf16x2(f[8 * q + 2], f[8 * q + 3]),
+                     pack_bf16x2(f[8 * q + 4], f[8 * q + 5]), pack_bf16x2(f[8 * q + 6], f[8 * q + 7]));
+  }
+}
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kThreads, 1)
+    tgmm_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_dout,
+                const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
+  int32_t* offs = reinterpret_cast<int32_t*>(smem + OFF_OFFS);
+  auto full_bar = [&](uint32_t s) { return sbase + OFF_FULL + 8 * s; };
+  auto empty_bar = [&](uint32_t s) { return sbase + OFF_EMPTY + 8 * s; };
+  auto accf_bar = [&](uint32_t b) { return sbase + OFF_ACCF + 8 * b; };
+  auto acce_bar = [&](uint32_t b) { return sbase + OFF_ACCE + 8 * b; };
+  const uint32_t done_bar = sbase + OFF_DONE;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch(&tm_lhs);
+    tma_prefetch(&tm_dout);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + OFF_TMEM, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) build_group_offsets(p.group_sizes, p.num_groups, p.m, offs, p.err);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM);
+
+  const int32_t k_tiles = (p.k + BM - 1) / BM;
+  const int32_t n_tiles = (p.n + BN - 1) / BN;
+  const int32_t per_group = k_tiles * n_tiles;
+  const int32_t total = p.num_groups * per_group;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, pend_mask = 0;
+      uint32_t pend_par[STAGES];
+      bool ok = true;
+      for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const int32_t g = w / per_group;
+        const int32_t r = w - g * per_group;
+        const int32_t kt = r / n_tiles, nt = r - kt * n_tiles;
+        const int32_t row_begin = offs[g], rows = offs[g + 1] - offs[g];
+        for (int32_t c = 0; c * BR < rows; ++c) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a_dst = sbase + OFF_A + stage * A_BYTES;
+          const uint32_t b_dst = sbase + OFF_B + stage * B_BYTES;
+          const int32_t row = row_begin + c * BR;
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * BOX_BYTES, &tm_lhs, fb, kt * BM + 64 * j, row);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * BOX_BYTES, &tm_dout, fb, nt * BN + 64 * j, row);
+          pend_par[stage] = phase;
+          pend_mask |= 1u << stage;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (pend_mask >> s & 1u) drain_bar(full_bar(s), pend_par[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdesc = idesc_bf16(BM, BN, true, true);
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const int32_t g = w / per_group;
+      const int32_t rows = offs[g + 1] - offs[g];
+      if (rows == 0) continue;  // the epilogue writes zeros; no accumulator is used
+      if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int32_t c = 0; c * BR < rows; ++c) {
+        if (!wait_bar(full_bar(stage), phase, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sbase + OFF_A + stage * A_BYTES;
+        const uint32_t b0 = sbase + OFF_B + stage * B_BYTES;
+        const int32_t valid = min(BR, rows - c * BR);
+        if (valid < BR) {
+          // Rows [valid, round_up(valid, 16)) belong to the next group (or lie
+          // past m): zero them in all six boxes.  A row is 128 contiguous bytes
+          // (the swizzle permutes 16-byte chunks within the row only).
+          const int32_t zrows = ((valid + 15) & ~15) - valid;
+          const int32_t units = zrows * 6 * 8;
+          for (int32_t u = lane; u < units; u += 32) {
+            const int32_t box = u / (zrows * 8);
+            const int32_t rem = u - box * zrows * 8;
+            const int32_t zr = valid + rem / 8, chunk = rem % 8;
+            const uint32_t base = box < 2 ? a0 + box * BOX_BYTES : b0 + (box - 2) * BOX_BYTES;
+            st_shared_v4(base + zr * 128 + chunk * 16, 0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const int32_t ksteps = (valid + 15) / 16;
+          for (int32_t kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = sw128_desc(a0 + kk * 2048, BOX_BYTES, 1024);
+            const uint64_t bd = sw128_desc(b0 + kk * 2048, BOX_BYTES, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, kIdesc, (c | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(accf_bar(acc));
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) {
+      mma_commit(done_bar);
+      drain_bar(done_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int32_t w = blockIdx.x; w < total; w += gridDim.x) {
+      const int32_t g = w / per_group;
+      const int32_t r = w - g * per_group;
+      const int32_t kt = r / n_tiles, nt = r - kt * n_tiles;
+      const int32_t rows = offs[g + 1] - offs[g];
+      const int32_t krow = kt * BM + row_in_tile;
+      const int64_t out_row = int64_t(g) * p.k + krow;
+      if (rows == 0) {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0.f;
+        if (krow < p.k)
+          for (int c = 0; c < BN / 32; ++c)
+            if (nt * BN + c * 32 < p.n) store_chunk<kOutF32>(p, out_row, nt * BN + c * 32, z);
+        continue;
+      }
+      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (uint32_t(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32cols(tbase + c * 32, v);
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(acce_bar(acc));
+        }
+        const int32_t col0 = nt * BN + c * 32;
+        if (krow < p.k && col0 < p.n) {
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          store_chunk<kOutF32>(p, out_row, col0, f);
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <bool kOutF32>
+cudaError_t launch_impl(const TgmmLaunch& L, int grid, cudaStream_t stream) {
+  auto kern = tgmm_kernel<kOutF32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  Params p{L.group_sizes, L.num_groups, L.m, L.n, L.k, L.out, L.err};
+  kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tgmm(const TgmmLaunch& p, bool out_f32, int grid, cudaStream_t stream) {
+  return out_f32 ? launch_impl<true>(p, grid, stream) : launch_impl<false>(p, grid, stream);
+}
+
+}  // namespace gmmk

@@ -1,0 +1,43 @@
+"""Shared helpers for the GPU parity tests: run the oracle on the same stored bytes
+the CUDA library read, and apply the acceptance bound
+    |gpu - ref| <= 1e-3 * mag + 2^-8 * |ref|   (element-wise; NaN never accepted)
+where ref is the oracle's exact-product fp64 sum and mag the same sum over
+absolute values.  The bound covers fp32 accumulation of up to ~4096 products
+(relative error well under 1e-3 of mag) plus one bf16 rounding of the result
+(at most 2^-9 of |result| for round-to-nearest-even)."""
+
+import numpy as np
+import torch
+
+import oracle
+from moe_grouped_matrix_gb300.workloads import stored_bits
+
+REL_MAG = 1e-3
+REL_REF = 2.0 ** -8
+
+
+def bits(t):
+    return stored_bits(t)
+
+
+def check_close(gpu: torch.Tensor, ref: np.ndarray, mag: np.ndarray, what: str):
+    g = gpu.detach().cpu().to(torch.float64).numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    bound = REL_MAG * mag + REL_REF * np.abs(ref)
+    err = np.abs(g - ref)
+    bad = ~(err <= bound)  # NaN in g fails here
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        details = ", ".join(f"{tuple(i)}: gpu={g[tuple(i)]!r} ref={ref[tuple(i)]!r} mag={mag[tuple(i)]!r}" for i in idx)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside the bound; {details}")
+
+
+def oracle_gmm(lhs, rhs, group_sizes_np, *, transpose_rhs=True, group_offset=0, rhs_scale=None, rhs_bias=None,
+               rows=None):
+    return oracle.gmm(bits(lhs), bits(rhs), group_sizes_np, transpose_rhs=transpose_rhs, group_offset=group_offset,
+                      rhs_scale=None if rhs_scale is None else bits(rhs_scale),
+                      rhs_bias=None if rhs_bias is None else bits(rhs_bias), rows=rows)
+
+
+def oracle_tgmm(lhs, dout, group_sizes_np, k_rows=None):
+    return oracle.tgmm(bits(lhs), bits(dout), group_sizes_np, k_rows=k_rows)

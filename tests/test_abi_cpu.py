@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads and exports every symbol include/libgmm.h declares,
+and rejects bad host-side arguments before touching the device (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_grouped_matrix_gb300 as G
+from moe_grouped_matrix_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "libgmm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return G.load_library()
+
+
+def test_header_declares_the_expected_calls():
+    assert declared_functions() == sorted(
+        ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in G.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert lib.gmm_status_string(0) == b"ok"
+    for code in range(1, 9):
+        assert lib.gmm_status_string(code) != b"unknown status"
+    assert lib.gmm_workspace_bytes() >= 4
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+
+
+def call_gmm(lib, **over):
+    a = dict(lhs=FAKE, lhs_dtype=0, m=256, k=128, rhs=FAKE, rhs_dtype=0, L=4, n=256, trhs=1, gs=FAKE, G=4, go=0,
+             scale=None, nb=0, bias=None, bias_dtype=0, out=FAKE, out_dtype=0, ws=FAKE, ws_bytes=256, stream=None)
+    a.update(over)
+    return lib.gmm(a["lhs"], a["lhs_dtype"], a["m"], a["k"], a["rhs"], a["rhs_dtype"], a["L"], a["n"], a["trhs"],
+                   a["gs"], a["G"], a["go"], a["scale"], a["nb"], a["bias"], a["bias_dtype"], a["out"],
+                   a["out_dtype"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(lhs=None), 1), (dict(gs=None), 1), (dict(out=None), 1),
+    (dict(lhs_dtype=1), 2), (dict(rhs_dtype=1), 2), (dict(out_dtype=2), 2), (dict(rhs_dtype=2, trhs=0), 2),
+    (dict(bias=FAKE, bias_dtype=2), 2),
+    (dict(k=100), 3), (dict(n=12), 3), (dict(m=-1), 3), (dict(L=5), 3), (dict(G=0), 3), (dict(G=2000, L=4), 3),
+    (dict(scale=FAKE, nb=3), 3),
+    (dict(G=8, L=4, go=5), 5), (dict(G=8, L=4, go=-1), 5),
+    (dict(lhs=ctypes.c_void_p((1 << 20) + 8)), 4), (dict(out=ctypes.c_void_p((1 << 20) + 4)), 4),
+    (dict(ws=None), 6), (dict(ws_bytes=8), 6),
+])
+def test_gmm_host_validation(lib, over, status):
+    assert call_gmm(lib, **over) == status
+
+
+def test_tgmm_host_validation(lib):
+    t = lambda **o: lib.tgmm(o.get("lhs", FAKE), o.get("ld", 0), o.get("dout", FAKE), o.get("dd", 0), o.get("m", 64),
+                             o.get("k", 128), o.get("n", 256), o.get("gs", FAKE), o.get("G", 4), o.get("out", FAKE),
+                             o.get("od", 1), o.get("ws", FAKE), o.get("wb", 256), None)
+    assert t(lhs=None) == 1
+    assert t(ld=2) == 2
+    assert t(od=2) == 2
+    assert t(k=12) == 3
+    assert t(G=0) == 3
+    assert t(out=ctypes.c_void_p((1 << 20) + 2)) == 4
+    assert t(wb=0) == 6
