@@ -1,0 +1,442 @@
+"""Benchmark of the grouped matmul on GB300 (one JSON line on stdout).
+
+Headline workload: the Mixtral-like MoE up-projection forward (8192 tokens,
+top-2 of 8 experts -> 16384 rows; lhs [16384, 4096] bf16; rhs [8, 28672, 4096]
+bf16 in the NT layout; bf16 out).  A step is one gmm call over that batch.
+Metric: useful TFLOP/s = 2 * sum_g m_g * n * k / time.  Inputs (2.0 GB) are
+larger than the 126 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gmm,reference}] [--no-suite]
+
+Under torchrun every rank runs its own replica of the step (independent
+batches: weak scaling, no collective on the data path); rank 0 prints the line.
+--impl reference times the CPU oracle on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped-GEMM useful TFLOP/s and % of GB300 dense peak (HBM GB/s for decode)"
+UNIT = "TFLOP/s"
+WORKLOAD = ("mixtral_up: gmm NT, lhs [16384,4096] bf16, rhs [8,28672,4096] bf16, "
+            "group_sizes from softmax top-2 of 8 (seeded N(0,1) logits), bf16 out")
+PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_nt_mixtral_up.md")
+KERNEL_SRC = os.path.join(ROOT, "moe_grouped_matrix_gb300", "csrc", "gemm_bf16.cu")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM bytes per launch recorded by the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not h or not t or h.group(1) != kernel_hash():
+        return None
+    return float(t.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- cpu baseline
+def oracle_sample(lhs_cpu, rhs_cpu, group_sizes, rows_per_group, seed=123):
+    import oracle
+    from moe_grouped_matrix_gb300.workloads import sample_rows, stored_bits
+
+    offs = oracle.group_offsets(group_sizes, lhs_cpu.shape[0])
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = []
+    for g in range(offs.size - 1):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi > lo:
+            rows.append(np.sort(rng.choice(hi - lo, size=min(rows_per_group, hi - lo), replace=False) + lo))
+    rows = np.concatenate(rows).astype(np.int64)
+    lb, rb = stored_bits(lhs_cpu), stored_bits(rhs_cpu)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.gmm(lb, rb, group_sizes, transpose_rhs=True, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    k = lhs_cpu.shape[1]
+    n = rhs_cpu.shape[1]
+    flops = 2.0 * rows.size * n * k
+    return dict(value=flops / dt / 1e12, seconds=dt, rows=int(rows.size), threads=threads)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    import torch
+    import moe_grouped_matrix_gb300 as G
+    from moe_grouped_matrix_gb300 import build as B
+    from moe_grouped_matrix_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    B.build()
+    G.load_library()
+    peaks = load_peaks()
+
+    d = W.mixtral_up(dev)
+    sizes = d["group_sizes"]
+    m, k = d["lhs"].shape
+    n = d["rhs"].shape[1]
+    flops = 2.0 * float(sizes.sum()) * n * k
+    gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    step = lambda: G.gmm(d["lhs"], d["rhs"], gs, transpose_rhs=True, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s, e in ev:
+        s.record(stream)
+        step()
+        e.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop() if clocks else None
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [s.elapsed_time(e) for s, e in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if G.read_device_errors() != 0:
+        raise RuntimeError("device error flags set during the benchmark")
+
+    ms_per_step = total_ms / args.steps
+    value = flops * world * args.steps / (total_ms / 1e3) / 1e12
+    kernel_ms = float(np.mean(per_launch))
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+
+    # end to end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if True:
+        h_lhs = d["lhs"].cpu().pin_memory()
+        h_rhs = d["rhs"].cpu().pin_memory()
+        h_gs = torch.from_numpy(sizes.copy()).pin_memory()
+        h_out = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+        d_lhs = torch.empty_like(d["lhs"])
+        d_rhs = torch.empty_like(d["rhs"])
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            d_lhs.copy_(h_lhs, non_blocking=True)
+            d_rhs.copy_(h_rhs, non_blocking=True)
+            gs.copy_(h_gs, non_blocking=True)
+            G.gmm(d_lhs, d_rhs, gs, transpose_rhs=True, out=out)
+            h_out.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = h_lhs.numel() * 2 + h_rhs.numel() * 2 + h_gs.numel() * 4
+        d2h = h_out.numel() * 2
+        e2e = {"value": flops * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+        del h_lhs, h_rhs, h_out, d_lhs, d_rhs
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(d["lhs"][: m].cpu(), d["rhs"].cpu(), sizes, rows_per_group=args.cpu_rows)
+        cpu = {"value": cb["value"], "unit": UNIT, "cores": cb["threads"], "kind": "oracle",
+               "sample": f"{cb['rows']} rows ({args.cpu_rows} per group) of the workload, every column, "
+                         f"fp64; {cb['seconds']:.1f} s"}
+
+    suite = None
+    if rank == 0 and world == 1 and not args.no_suite:
+        del d, out
+        torch.cuda.empty_cache()
+        suite = run_suite(dev, peaks)
+
+    traffic = profile_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": int(m), "k": int(k), "n": int(n), "groups": int(sizes.size),
+                   "group_sizes": sizes.tolist(), "l2": "inputs larger than L2 (2.0 GB per step)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst", "kernel": "gemm_bf16_kernel<NT, bf16 out>",
+                     "kernel_ms": kernel_ms, "flops_per_launch": flops},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if suite is not None:
+        line["suite"] = suite
+    return line
+
+
+def _time_call(torch, fn, iters=20, warm=3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def run_suite(dev, peaks):
+    """Every other workload once: time, useful TFLOP/s, algorithmic GB/s and the fraction
+    of the relevant roofline max(F / P_bf16, B / BW) / t."""
+    import torch
+    import moe_grouped_matrix_gb300 as G
+    from moe_grouped_matrix_gb300 import workloads as W
+
+    res = {}
+
+    def record(name, ms, flops, bytes_):
+        t = ms / 1e3
+        floor = max(flops / (peaks["bf16"] * 1e12), bytes_ / (peaks["hbm"] * 1e9))
+        res[name] = {"ms": ms, "tflops": flops / t / 1e12, "gbs": bytes_ / t / 1e9,
+                     "bound": "tensor" if flops / (peaks["bf16"] * 1e12) > bytes_ / (peaks["hbm"] * 1e9) else "hbm",
+                     "roofline_frac": floor / t, "frac_of_bf16_peak": flops / t / 1e12 / peaks["bf16"]}
+
+    mo = W.moe128(dev)
+    sizes = mo["group_sizes"]
+    gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    rows = float(sizes.sum())
+    live = int((sizes > 0).sum())
+    for name, lhs, w, trhs, n, k in [
+        ("moe128_wi_nt", mo["lhs"], mo["wi"], True, 2048, 2048),
+        ("moe128_wo_nt_k1024", mo["lhs_wo"], mo["wo"], True, 2048, 1024),
+        ("moe128_wo_nn_n1024", mo["lhs"], mo["wo"], False, 1024, 2048),
+        ("moe128_dlhs_nt", mo["dout"], mo["wi"], True, 2048, 2048),
+    ]:
+        o = torch.empty((lhs.shape[0], n), dtype=torch.bfloat16, device=dev)
+        ms = _time_call(torch, lambda: G.gmm(lhs, w, gs, transpose_rhs=trhs, out=o))
+        bytes_ = rows * k * 2 + live * n * k * 2 + lhs.shape[0] * n * 2
+        record(name, ms, 2 * rows * n * k, bytes_)
+        del o
+    dw = torch.empty((128, 2048, 2048), dtype=torch.float32, device=dev)
+    ms = _time_call(torch, lambda: G.tgmm(mo["lhs"], mo["dout"], gs, out=dw))
+    record("moe128_tgmm_f32", ms, 2 * rows * 2048 * 2048, rows * 2048 * 2 * 2 + dw.numel() * 4)
+    del mo, dw
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------- ncu cases
+def _ncu_gemm_small(torch, G, W, dev):
+    # the headline kernel on a quarter of the workload's n (0.8 GB on the device, > L2)
+    d = W.mixtral_up(dev)
+    lhs, rhs = d["lhs"], d["rhs"][:, :7168].contiguous()
+    gs = torch.tensor(d["group_sizes"], dtype=torch.int32, device=dev)
+    out = torch.empty((lhs.shape[0], 7168), dtype=torch.bfloat16, device=dev)
+    del d
+    return lambda: G.gmm(lhs, rhs, gs, transpose_rhs=True, out=out)
+
+
+def _ncu_tgmm(torch, G, W, dev):
+    mo = W.moe128(dev, which=("lhs", "dout"))
+    gs = torch.tensor(mo["group_sizes"], dtype=torch.int32, device=dev)
+    dw = torch.empty((128, 2048, 2048), dtype=torch.float32, device=dev)
+    return lambda: G.tgmm(mo["lhs"], mo["dout"], gs, out=dw)
+
+
+NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm}
+
+
+def run_ncu_case(name):
+    import torch
+    import moe_grouped_matrix_gb300 as G
+    from moe_grouped_matrix_gb300 import build as B
+    from moe_grouped_matrix_gb300 import workloads as W
+
+    B.build()
+    dev = torch.device("cuda", 0)
+    fn = NCU_CASES[name](torch, G, W, dev)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    if G.read_device_errors() != 0:
+        raise RuntimeError("device error flags set")
+    print(f"ncu case {name}: 3 launches ok")
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload each step."""
+    import torch
+    from moe_grouped_matrix_gb300 import workloads as W
+
+    d = W.mixtral_up("cpu")
+    sizes = d["group_sizes"]
+    m, k = d["lhs"].shape
+    n = d["rhs"].shape[1]
+    for _ in range(args.warmup):
+        oracle_sample(d["lhs"], d["rhs"], sizes, rows_per_group=1)
+    times, vals, info = [], [], None
+    for s in range(args.steps):
+        info = oracle_sample(d["lhs"], d["rhs"], sizes, rows_per_group=args.ref_rows, seed=1000 + s)
+        times.append(info["seconds"])
+        vals.append(info["value"])
+    total = sum(times)
+    flops = 2.0 * info["rows"] * n * k
+    value = flops * args.steps / total / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": int(m), "k": int(k), "n": int(n), "groups": int(sizes.size),
+                   "group_sizes": sizes.tolist(), "l2": "not applicable (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["threads"], "kind": "oracle",
+                         "sample": f"{info['rows']} rows ({args.ref_rows} per group) of the workload per step, "
+                                   f"every column, fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gmm", choices=["gmm", "reference"])
+    ap.add_argument("--no-suite", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=64, help="rows per group in the CPU-baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=1, help="rows per group per step of the reference arm")
+    ap.add_argument("--ncu-case", choices=sorted(NCU_CASES), default=None,
+                    help="run one small profiling case a few times and exit (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ["LOCAL_RANK"])))
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

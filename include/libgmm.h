@@ -89,6 +89,11 @@ size_t gmm_workspace_bytes(void);
  *   group_offset first local group; 0 <= group_offset <= num_total_groups - num_local_groups.
  *   rhs_scale    NULL (s = 1, one block) or device f32 [num_local_groups, num_quant_blocks, 1, n];
  *                block b covers kk in [b*k/nb, (b+1)*k/nb); k % num_quant_blocks == 0.
+ *                With rhs_scale given or an e4m3 rhs, the block-scaled kernel runs: it needs
+ *                transpose_rhs != 0 (else GMM_ERR_DTYPE), k % 128 == 0 and
+ *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  It is built for
+ *                decode-sized groups (a few rows each): it streams every weight tile once per
+ *                16 rows of its group.
  *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
  *   out          [m, n] of out_dtype (BF16 or F32).
  *   Sizes: m >= 0, k >= 8, n >= 8, k % 8 == 0, n % 8 == 0 (16-byte rows); lhs, rhs,

@@ -148,6 +148,12 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   if (rhs_scale != nullptr) {
     if (num_quant_blocks < 1 || k % num_quant_blocks != 0) return GMM_ERR_SHAPE;
   }
+  // Block-scaled / e4m3 path: NT layout, k and the quant-block width multiples of 128.
+  const int32_t nb = rhs_scale != nullptr ? num_quant_blocks : 1;
+  if (scaled_path) {
+    if (!transpose_rhs) return GMM_ERR_DTYPE;
+    if (k % 128 != 0 || (k / nb) % 128 != 0) return GMM_ERR_SHAPE;
+  }
   if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || (rhs_bias && !aligned16(rhs_bias)) ||
       (rhs_scale && !aligned16(rhs_scale)))
     return GMM_ERR_ALIGN;
@@ -158,7 +164,42 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* err = static_cast<uint32_t*>(workspace);
 
-  if (scaled_path) return GMM_ERR_DTYPE;
+  if (scaled_path) {
+    const int64_t items = ((m + 15) / 16 + num_local_groups) * ((n + 127) / 128);
+    if (items > INT32_MAX) return GMM_ERR_SHAPE;
+    gmmk::ScaledLaunch S{};
+    {
+      const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
+      const uint32_t box[2] = {64, 16};
+      if (int st = make_map(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return st;
+    }
+    {
+      const bool e4m3 = rhs_dtype == GMM_DTYPE_E4M3;
+      const uint64_t dims[3] = {uint64_t(k), uint64_t(n), uint64_t(num_local_groups)};
+      const uint32_t box[3] = {e4m3 ? 128u : 64u, 128u, 1u};
+      if (int st = make_map(&S.tm_rhs, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            e4m3 ? 1 : 2, 3, rhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return st;
+    }
+    S.group_sizes = group_sizes;
+    S.num_total_groups = num_total_groups;
+    S.group_offset = group_offset;
+    S.num_local_groups = num_local_groups;
+    S.m = int32_t(m);
+    S.n = int32_t(n);
+    S.k = int32_t(k);
+    S.scale = rhs_scale;
+    S.num_blocks = nb;
+    S.bias = rhs_bias;
+    S.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
+    S.out = out;
+    S.err = err;
+    cudaError_t e = gmmk::launch_scaled(S, rhs_dtype == GMM_DTYPE_E4M3, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GMM_OK;
+  }
 
   gmmk::GemmLaunch L{};
   {
