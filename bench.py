@@ -325,6 +325,24 @@ def run_suite(dev, peaks):
     record("moe128_tgmm_f32", ms, 2 * rows * 2048 * 2048, rows * 2048 * 2 * 2 + dw.numel() * 4)
     del mo, dw
     torch.cuda.empty_cache()
+
+    fd = W.fp8_decode(dev)
+    sizes = fd["group_sizes"]
+    gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    n, k = fd["rhs"].shape[1], fd["rhs"].shape[2]
+    nb = fd["rhs_scale"].shape[1]
+    o = torch.empty((fd["lhs"].shape[0], n), dtype=torch.bfloat16, device=dev)
+    for go in (0, 32):
+        rhs, sc, bi = fd["rhs"][go:], fd["rhs_scale"][go:], fd["rhs_bias"][go:]
+        local = sizes[go:]
+        rows = float(local.sum())
+        live = int((local > 0).sum())
+        ms = _time_call(torch, lambda: G.gmm(fd["lhs"], rhs, gs, rhs_scale=sc, rhs_bias=bi, group_offset=go, out=o))
+        # weights, scales and bias of non-empty local experts, their lhs rows, the whole output
+        bytes_ = live * (n * k + nb * n * 4 + n * 2) + rows * k * 2 + fd["lhs"].shape[0] * n * 2
+        record(f"fp8_decode_go{go}", ms, 2 * rows * n * k, bytes_)
+    del fd, o
+    torch.cuda.empty_cache()
     return res
 
 
@@ -346,7 +364,13 @@ def _ncu_tgmm(torch, G, W, dev):
     return lambda: G.tgmm(mo["lhs"], mo["dout"], gs, out=dw)
 
 
-NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm}
+def _ncu_fp8_decode(torch, G, W, dev):
+    fd = W.fp8_decode(dev)
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
+    return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"])
+
+
+NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode}
 
 
 def run_ncu_case(name):
