@@ -124,6 +124,39 @@ int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64
          const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
          size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array compiled into the library for gmm_noalloc(). */
+#define GMM_NOALLOC_SCRATCH_BYTES 256
+
+/*
+ * gmm_noalloc: gmm() without a caller-supplied workspace.  The pages have no
+ * counterpart to this call.
+ *
+ * For callers that cannot allocate device memory: code whose device memory is
+ * owned by another component's allocator with no way to ask it for a buffer,
+ * or code on a path where cudaMalloc is not allowed (it may synchronise the
+ * device and its latency is unbounded).  Instead of a workspace it uses a
+ * GMM_NOALLOC_SCRATCH_BYTES-byte __device__ array compiled into the library,
+ * which every GPU that loads the library holds until the process exits.  It
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  - Arguments, layouts, results and host-side errors are those of gmm() (the
+ *    same kernels run); GMM_ERR_WORKSPACE if the library's scratch need ever
+ *    exceeded the array (it is one word of error flags, independent of the
+ *    problem size, so every size gmm() accepts fits).
+ *  - The first call on a device sets up that device: with the device current
+ *    it takes the array's device address (cudaGetSymbolAddress).  Make that
+ *    first call before any stream capture.
+ *  - Every call on a device shares the array, and the array keeps the last
+ *    call's contents; each call first clears the error-flag word (an
+ *    asynchronous memset on `stream`).  Calls that overlap on the GPU (on
+ *    different streams) race on it.  The device error flags of this variant
+ *    cannot be read back; callers that need them use gmm() with a workspace.
+ */
+int gmm_noalloc(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+                const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the sticky device error flags
  * (GMM_DEVERR_*) of `workspace` into *flags.  Returns GMM_OK or GMM_ERR_CUDA.

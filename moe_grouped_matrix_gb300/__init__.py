@@ -43,6 +43,7 @@ SIGNATURES = {
     "gmm_workspace_bytes": ([], _SZ),
     "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
     "tgmm": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _P, _I, _P, _SZ, _P], _I),
+    "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
     "gmm_read_device_errors": ([_P, _P, _U32P], _I),
     "gmm_status_string": ([_I], ctypes.c_char_p),
     "gmm_last_cuda_error": ([], _I),

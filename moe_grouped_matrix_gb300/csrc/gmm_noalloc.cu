@@ -1,0 +1,70 @@
+// gmm_noalloc: the forward grouped matmul for callers that cannot allocate
+// device memory.
+//
+// gmm() needs a small caller-owned device workspace (the kernel's error-flag
+// word).  Some callers cannot provide one: code whose device memory is owned
+// entirely by another component's allocator and that has no way to request a
+// buffer from it, or code on a path where calling cudaMalloc is not allowed
+// (cudaMalloc may synchronise the device and its latency is unbounded).  This
+// entry point serves them by using a scratch array compiled into the library
+// instead: a file-scope __device__ array that every GPU which loads the
+// library holds until the process exits.  It calls no cudaMalloc, cudaFree or
+// allocating library routine.
+//
+// The kernels' scratch need does not grow with the problem: it is one 32-bit
+// word of device-side error flags, so any problem size the ABI accepts fits
+// the fixed array below; the size check guards the library's own invariant.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/libgmm.h"
+
+namespace {
+
+// The scratch: error flags in word 0, the rest reserved.  Shared by every call
+// on a device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[GMM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {};
+cudaError_t g_setup_status[kMaxDevices] = {};
+std::once_flag g_setup_once[kMaxDevices];
+
+// The host-side name g_noalloc_scratch is only a stand-in for the symbol, not a
+// device address; the device address comes from cudaGetSymbolAddress, taken
+// once per device with that device current.
+int scratch_for_current_device(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GMM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GMM_ERR_ARCH;
+  std::call_once(g_setup_once[dev], [dev] {
+    void* p = nullptr;
+    g_setup_status[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    g_scratch_ptr[dev] = p;
+  });
+  if (g_setup_status[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return GMM_ERR_CUDA;
+  *ptr = g_scratch_ptr[dev];
+  return GMM_OK;
+}
+
+}  // namespace
+
+extern "C" int gmm_noalloc(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                           int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                           int32_t num_total_groups, int32_t group_offset, const float* rhs_scale,
+                           int32_t num_quant_blocks, const void* rhs_bias, int bias_dtype, void* out,
+                           int out_dtype, void* stream) {
+  const size_t need = gmm_workspace_bytes();
+  if (need > sizeof(g_noalloc_scratch)) return GMM_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (int st = scratch_for_current_device(&scratch)) return st;
+  // The flags must start at zero for this call; the array keeps whatever the
+  // previous call on this device left in it.
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GMM_ERR_CUDA;
+  return gmm(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+             num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype,
+             scratch, sizeof(g_noalloc_scratch), stream);
+}
