@@ -80,22 +80,37 @@ struct Params {
 };
 
 // 16 e4m3fn codes (one 16-byte chunk, lowest k first) -> 16 bf16 (8 words).
+// Per pair of codes: the two bytes go to the high byte of each 16-bit half,
+// their 7 exponent/mantissa bits move to bf16 bits 4..10 (a bf16 number equal
+// to 2^-120 times the code's value, subnormal codes included), a bf16x2 fma
+// multiplies by 2^120 (exact) and the sign bit is merged back.  The two NaN
+// codes (low 7 bits all ones) would come out as +-480; a chunk holding one is
+// rare, so it is found with a zero-byte test and fixed on a separate path.
 __device__ __forceinline__ void decode16(const uint4 raw, uint32_t (&o)[8]) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t nan_any = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ~w[i] & 0x7F7F7F7Fu;  // a zero byte marks a NaN code
+    nan_any |= (t - 0x01010101u) & 0x80808080u;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      // bytes (2h, 2h+1) of w[i] into the high byte of each 16-bit half
       const uint32_t v = __byte_perm(w[i], 0u, h == 0 ? 0x1404u : 0x3424u);
-      // sign stays at bit 15; exponent+mantissa (bits 8..14) move to bits 4..10
-      const uint32_t x = (v & 0x80008000u) | ((v >> 4) & 0x07F007F0u);
+      const uint32_t mag = (v >> 4) & 0x07F007F0u;
       uint32_t y;
-      // times 2^120 (bf16 0x7B80), exact; adding -0 keeps the sign of zero
-      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(x), "r"(0x7B807B80u), "r"(0x80008000u));
-      // codes with all of bits 0..6 set are NaN
-      const uint32_t nan_half = __vcmpeq2(v & 0x7F007F00u, 0x7F007F00u);
-      o[2 * i + h] = (y & ~nan_half) | (0x7FC07FC0u & nan_half);
+      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mag), "r"(0x7B807B80u), "r"(0u));
+      o[2 * i + h] = y | (v & 0x80008000u);
+    }
+  }
+  if (nan_any != 0u) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t v = __byte_perm(w[i], 0u, h == 0 ? 0x1404u : 0x3424u);
+        if ((v & 0x00007F00u) == 0x00007F00u) o[2 * i + h] = (o[2 * i + h] & 0xFFFF0000u) | 0x7FC0u;
+        if ((v & 0x7F000000u) == 0x7F000000u) o[2 * i + h] = (o[2 * i + h] & 0x0000FFFFu) | 0x7FC00000u;
+      }
     }
   }
 }
@@ -329,10 +344,13 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
     }
   } else if constexpr (kE4M3) {
     // ---------------------------------------------------------------- e4m3 -> bf16 decoders
-    // Unit u of a stage = (row r, 16-byte raw chunk c): r = u / 8, c = u % 8.
+    // Unit u of a stage = (row r, 16-byte raw chunk c) with r = u % 8 + 8 * (u / 64)
+    // and c = (u / 8) % 8, so the 8 lanes of each quarter-warp (one shared-memory
+    // phase of a 16-byte access) take the same chunk of 8 consecutive rows.
     // Raw row r holds k [0, 128) as 8 chunks at positions c ^ (r % 8); the bf16
     // A operand holds k [0, 64) and [64, 128) in two atoms whose rows hold 8
-    // chunks of 8 bf16 at positions j ^ (r % 8).
+    // chunks of 8 bf16 at positions j ^ (r % 8): the 8 lanes of a phase hit 8
+    // different positions on every load and store.
     const int ct = threadIdx.x - 192;
     uint32_t stage = 0, phase = 0;
     bool ok = true;
@@ -347,7 +365,7 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
 #pragma unroll
         for (int i = 0; i < (BMW * 8) / kConvThreads; ++i) {
           const int u = ct + i * kConvThreads;
-          const int r = u >> 3, c = u & 7, sw = r & 7;
+          const int r = (u & 7) + ((u >> 6) << 3), c = (u >> 3) & 7, sw = r & 7;
           uint4 raw;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)

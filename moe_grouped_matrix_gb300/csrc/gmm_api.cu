@@ -201,6 +201,9 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
     return GMM_OK;
   }
 
+  // Groups of a few hundred rows or more run on SM pairs (256-row tiles);
+  // smaller ones on single SMs (128-row tiles waste less on group tails).
+  const bool pair_path = m >= int64_t(192) * num_total_groups;
   gmmk::GemmLaunch L{};
   {
     const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
@@ -211,7 +214,7 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   }
   if (transpose_rhs) {
     const uint64_t dims[3] = {uint64_t(k), uint64_t(n), uint64_t(num_local_groups)};
-    const uint32_t box[3] = {64, 256, 1};
+    const uint32_t box[3] = {64, pair_path ? 128u : 256u, 1};
     if (int st = make_map(&L.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, rhs, dims, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
@@ -237,7 +240,9 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   // Work items = m-tiles x n-tiles must fit in int32.
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
   if (m_tiles_max * ((n + 255) / 256) > INT32_MAX) return GMM_ERR_SHAPE;
-  cudaError_t e = gmmk::launch_gemm_bf16(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+  cudaError_t e = pair_path
+                      ? gmmk::launch_gemm_bf16_2sm(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s)
+                      : gmmk::launch_gemm_bf16(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
 }
@@ -275,6 +280,14 @@ int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64
     const uint32_t box[2] = {64, 64};
     if (int st = make_map(&L.tm_dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dout, dims, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  {
+    const bool f32 = out_dtype == GMM_DTYPE_F32;
+    const uint64_t dims[3] = {uint64_t(n), uint64_t(k), uint64_t(num_groups)};
+    const uint32_t box[3] = {f32 ? 32u : 64u, 32u, 1u};
+    if (int st = make_map(&L.tm_out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          f32 ? 4 : 2, 3, out, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
   }
   L.group_sizes = group_sizes;

@@ -24,10 +24,15 @@ struct GemmLaunch {
 
 cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
 
+// Same computation on SM pairs (256 x 256 tiles, cta_group::2).  tm_rhs boxes:
+// NT {64, 128, 1}; NN {64, 64, 1}.  Launches at most max_ctas CTAs.
+cudaError_t launch_gemm_bf16_2sm(const GemmLaunch& p, bool nt, bool out_f32, int max_ctas, cudaStream_t stream);
+
 // tgmm: out[g] = lhs_g^T dout_g (bf16 operands, fp32 accumulate).
 struct TgmmLaunch {
   CUtensorMap tm_lhs;   // lhs  [m, k], box {64, 64}
   CUtensorMap tm_dout;  // dout [m, n], box {64, 64}
+  CUtensorMap tm_out;   // out [G, k, n], box {128 bytes of n, 32, 1}
   const int32_t* group_sizes;
   int32_t num_groups;
   int32_t m, n, k;

@@ -13,8 +13,11 @@
 // operands) before issuing, so no other group's data enters the sum.
 //
 // Same CTA shape as the forward kernel: warp 0 TMA, warp 1 TMEM + MMA,
-// warps 2-5 epilogue (fp32 or bf16 stores of 128 x 256 output tiles; empty
-// groups' tiles are written as zeros without touching TMEM).
+// warps 2-5 epilogue.  The output (fp32 [G, k, n] by default) is the bulk of
+// the bytes, so each epilogue warp stages its 32 rows x 128 bytes of the tile
+// in a 128-byte-swizzled shared-memory slice (two per warp, alternating) and
+// writes it with a TMA bulk tensor store; the TMA clips the k and n tails.
+// Empty groups' tiles are written as zeros the same way, without TMEM.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -27,7 +30,7 @@ namespace {
 constexpr int BM = 128;  // output rows (lhs columns)
 constexpr int BN = 256;  // output columns (dout columns)
 constexpr int BR = 64;   // contraction rows per stage
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64-feature x 64-row box
@@ -36,9 +39,12 @@ constexpr uint32_t B_BYTES = (BN / 64) * BOX_BYTES;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
+constexpr uint32_t SLICE_BYTES = 32 * 128;  // one warp's 32 rows x 128 bytes of output
+
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = STAGES * A_BYTES;
-constexpr uint32_t OFF_CTRL = STAGES * STAGE_BYTES;
+constexpr uint32_t OFF_OUT = STAGES * STAGE_BYTES;  // 4 warps x 2 slices
+constexpr uint32_t OFF_CTRL = OFF_OUT + 8 * SLICE_BYTES;
 constexpr uint32_t OFF_FULL = OFF_CTRL;
 constexpr uint32_t OFF_EMPTY = OFF_FULL + 8 * STAGES;
 constexpr uint32_t OFF_ACCF = OFF_EMPTY + 8 * STAGES;
@@ -59,29 +65,29 @@ struct Params {
   uint32_t* err;
 };
 
+// One warp writes its 32 rows x 128 bytes (32 fp32 or 64 bf16 columns) into a
+// swizzled slice: row `lane`, 16-byte chunk j at position j ^ (lane % 8), the
+// layout a 128-byte-swizzled TMA box of {128 bytes, 32 rows} expects.
 template <bool kOutF32>
-__device__ __forceinline__ void store_chunk(const Params& p, int64_t out_row, int32_t col0, const float (&f)[32]) {
-  if constexpr (kOutF32) {
-    float* o = static_cast<float*>(p.out) + out_row * p.n + col0;
+__device__ __forceinline__ void stage_row(uint32_t slice, int lane, const float* f) {
+  const uint32_t row = slice + uint32_t(lane) * 128u;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (col0 + 4 * q < p.n)
-        st_global_v4(o + 4 * q, __float_as_uint(f[4 * q]), __float_as_uint(f[4 * q + 1]),
-                     __float_as_uint(f[4 * q + 2]), __float_as_uint(f[4 * q + 3]));
-  } else {
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + out_row * p.n + col0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (col0 + 8 * q < p.n)
-        st_global_v4(o + 8 * q, pack_bf16x2(f[8 * q], f[8 * q + 1]), pack_bf16x2(f[8 * q + 2], f[8 * q + 3]),
-                     pack_bf16x2(f[8 * q + 4], f[8 * q + 5]), pack_bf16x2(f[8 * q + 6], f[8 * q + 7]));
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t dst = row + ((uint32_t(j) ^ uint32_t(lane & 7)) << 4);
+    if constexpr (kOutF32) {
+      st_shared_v4(dst, __float_as_uint(f[4 * j]), __float_as_uint(f[4 * j + 1]), __float_as_uint(f[4 * j + 2]),
+                   __float_as_uint(f[4 * j + 3]));
+    } else {
+      st_shared_v4(dst, pack_bf16x2(f[8 * j], f[8 * j + 1]), pack_bf16x2(f[8 * j + 2], f[8 * j + 3]),
+                   pack_bf16x2(f[8 * j + 4], f[8 * j + 5]), pack_bf16x2(f[8 * j + 6], f[8 * j + 7]));
+    }
   }
 }
 
 template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     tgmm_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_dout,
-                const Params p) {
+                const __grid_constant__ CUtensorMap tm_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -109,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch(&tm_lhs);
     tma_prefetch(&tm_dout);
+    tma_prefetch(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(sbase + OFF_TMEM, TMEM_COLS);
@@ -230,42 +237,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
+    constexpr int kColsPerBox = kOutF32 ? 32 : 64;  // 128 bytes of output per row
     const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t slices = sbase + OFF_OUT + uint32_t(quarter) * 2u * SLICE_BYTES;
+    uint32_t slot = 0;
+    // Hands the slice `slot` to this warp: the store issued from it two boxes
+    // ago has finished reading shared memory.
+    auto acquire_slice = [&]() {
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+      return slices + slot * SLICE_BYTES;
+    };
+    auto release_slice = [&](int32_t col, int32_t krow0, int32_t g) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_out, slices + slot * SLICE_BYTES, col, krow0, g);
+        tma_store_commit();
+      }
+      slot ^= 1u;
+    };
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t w = blockIdx.x; w < total; w += gridDim.x) {
       const int32_t g = w / per_group;
       const int32_t r = w - g * per_group;
       const int32_t kt = r / n_tiles, nt = r - kt * n_tiles;
       const int32_t rows = offs[g + 1] - offs[g];
-      const int32_t krow = kt * BM + row_in_tile;
-      const int64_t out_row = int64_t(g) * p.k + krow;
+      const int32_t krow0 = kt * BM + quarter * 32;
       if (rows == 0) {
-        float z[32];
+        float z[kColsPerBox];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0.f;
-        if (krow < p.k)
-          for (int c = 0; c < BN / 32; ++c)
-            if (nt * BN + c * 32 < p.n) store_chunk<kOutF32>(p, out_row, nt * BN + c * 32, z);
+        for (int i = 0; i < kColsPerBox; ++i) z[i] = 0.f;
+        for (int c = 0; c < BN; c += kColsPerBox) {
+          if (nt * BN + c >= p.n || krow0 >= p.k) break;
+          stage_row<kOutF32>(acquire_slice(), lane, z);
+          release_slice(nt * BN + c, krow0, g);
+        }
         continue;
       }
       if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32cols(tbase + c * 32, v);
-        if (c == BN / 32 - 1) {
+      for (int c = 0; c < BN; c += kColsPerBox) {
+        float f[kColsPerBox];
+#pragma unroll
+        for (int h = 0; h < kColsPerBox / 32; ++h) {
+          uint32_t v[32];
+          tmem_ld_32cols(tbase + c + 32 * h, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[32 * h + i] = __uint_as_float(v[i]);
+        }
+        if (c + kColsPerBox == BN) {
           tc_fence_before();
           mbar_arrive(acce_bar(acc));
         }
-        const int32_t col0 = nt * BN + c * 32;
-        if (krow < p.k && col0 < p.n) {
-          float f[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-          store_chunk<kOutF32>(p, out_row, col0, f);
+        if (nt * BN + c < p.n && krow0 < p.k) {
+          stage_row<kOutF32>(acquire_slice(), lane, f);
+          release_slice(nt * BN + c, krow0, g);
         }
       }
       if (++acc == 2) {
@@ -273,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -289,7 +320,7 @@ cudaError_t launch_impl(const TgmmLaunch& L, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_groups, L.m, L.n, L.k, L.out, L.err};
-  kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, p);
+  kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, L.tm_out, p);
   return cudaGetLastError();
 }
 

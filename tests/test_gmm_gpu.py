@@ -186,3 +186,50 @@ def test_tgmm_sums_to_dense_when_groups_cover_all_rows():
     out = G.tgmm(lhs, dout, _gs(sizes))
     dense = lhs.double().T @ dout.double()
     assert torch.allclose(out.double().sum(0), dense, rtol=1e-4, atol=1e-3)
+
+
+# ------------------------------------------------ SM-pair kernel (>= 192 rows per group on average)
+@pytest.mark.parametrize("transpose_rhs", LAYOUTS)
+@pytest.mark.parametrize("out_dtype", ODT)
+def test_pair_ragged_tiles_and_tails(transpose_rhs, out_dtype):
+    # 256-row pair tiles over groups of 300, 0, 513, 1, 400 rows (sum 1214 < m = 1500);
+    # k = 200 and n = 520 leave tails in both dimensions.
+    _gmm_case(1500, 200, 520, [300, 0, 513, 1, 400], transpose_rhs=transpose_rhs, out_dtype=out_dtype, seed=3)
+
+
+@pytest.mark.parametrize("go,local", [(0, 3), (2, 3), (5, 1)])
+def test_pair_group_offset_slices(go, local):
+    _gmm_case(1800, 192, 264, [250, 0, 333, 700, 7, 300], group_offset=go, local=local, seed=10 + go)
+
+
+def test_pair_bias_and_single_group():
+    _gmm_case(1024, 256, 520, [1024], bias_dtype=torch.bfloat16, out_dtype=torch.float32, seed=17)
+
+
+@pytest.mark.parametrize("transpose_rhs", LAYOUTS)
+def test_pair_integer_inputs_bit_exact(transpose_rhs):
+    m, k, n = 1100, 256, 264
+    sizes = np.array([257, 0, 255, 400, 1], np.int32)
+    lhs = W.integer_valued((m, k), -8, 8, 13, DEV)
+    base = W.integer_valued((n, k), -8, 8, 14, DEV, dtype=torch.float32)
+    w_nk = torch.stack([(g + 1) * base for g in range(sizes.size)]).to(torch.bfloat16)
+    rhs = w_nk if transpose_rhs else w_nk.transpose(1, 2).contiguous()
+    out = G.gmm(lhs, rhs, _gs(sizes), transpose_rhs=transpose_rhs, out_dtype=torch.float32)
+    ref, _ = oracle_gmm(lhs, rhs, sizes, transpose_rhs=transpose_rhs)
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), ref)
+
+
+def test_pair_and_single_sm_kernels_agree():
+    # The same rows and experts run once on the SM-pair kernel (m / G = 192) and once on
+    # the single-SM kernel (two trailing empty groups with junk experts make m / G < 192).
+    # Both feed identical products to the tensor core in the same k order.
+    m, k, n = 1536, 320, 512
+    sizes = np.array([200, 340, 0, 300, 150, 0, 400, 146], np.int32)
+    lhs = W.normal((m, k), 1.0, 21, DEV)
+    w = W.normal((8, n, k), 0.05, 22, DEV)
+    pair = G.gmm(lhs, w, _gs(sizes), out_dtype=torch.float32)
+    w10 = torch.cat([w, W.normal((2, n, k), 3.0, 23, DEV)])
+    single = G.gmm(lhs, w10, _gs(np.concatenate([sizes, [0, 0]])), out_dtype=torch.float32)
+    assert torch.equal(pair, single)
+    ref, mag = oracle_gmm(lhs, w, sizes)
+    check_close(pair, ref, mag, "pair")
