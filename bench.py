@@ -33,8 +33,8 @@ METRIC = "grouped-GEMM useful TFLOP/s and % of GB300 dense peak (HBM GB/s for de
 UNIT = "TFLOP/s"
 WORKLOAD = ("mixtral_up: gmm NT, lhs [16384,4096] bf16, rhs [8,28672,4096] bf16, "
             "group_sizes from softmax top-2 of 8 (seeded N(0,1) logits), bf16 out")
-PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_nt_mixtral_up.md")
-KERNEL_SRC = os.path.join(ROOT, "moe_grouped_matrix_gb300", "csrc", "gemm_bf16.cu")
+PROFILE = os.path.join(ROOT, "profiles", "gemm_bf16_2sm_nt_mixtral_up.md")
+KERNEL_SRC = os.path.join(ROOT, "moe_grouped_matrix_gb300", "csrc", "gemm_bf16_2sm.cu")
 
 
 def load_peaks():
@@ -263,7 +263,7 @@ def run_gpu(args, rank, world):
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16"], "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 burst", "kernel": "gemm_bf16_kernel<NT, bf16 out>",
+                     "peak_source": f"{peaks['source']} bf16 burst", "kernel": "gemm_bf16_2sm_kernel<NT, bf16 out>",
                      "kernel_ms": kernel_ms, "flops_per_launch": flops},
         "gpu_launches": args.steps,
         "clocks": clock_info,
@@ -370,7 +370,15 @@ def _ncu_fp8_decode(torch, G, W, dev):
     return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"])
 
 
-NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode}
+def _ncu_moe128_wi(torch, G, W, dev):
+    mo = W.moe128(dev, which=("lhs", "wi"))
+    gs = torch.tensor(mo["group_sizes"], dtype=torch.int32, device=dev)
+    out = torch.empty((32768, 2048), dtype=torch.bfloat16, device=dev)
+    return lambda: G.gmm(mo["lhs"], mo["wi"], gs, out=out)
+
+
+NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode,
+             "moe128_wi": _ncu_moe128_wi}
 
 
 def run_ncu_case(name):
