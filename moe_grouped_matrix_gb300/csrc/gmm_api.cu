@@ -8,6 +8,8 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/libgmm.h"
@@ -93,6 +95,29 @@ int make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, int rank,
 }
 
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
+
+// The bf16 forward kernels:
+//   kPair   256 x 256 tiles on SM pairs: the fastest per MMA, but a group's last
+//           256-row tile may be mostly padding;
+//   kSwap   weights on the MMA's M side, a group's rows (up to 256, rounded to
+//           16) on its N side: almost no padding, one SM per tile;
+//   kSingle 128 x 256 tiles on one SM.
+// Groups averaging 128 rows or more go to kPair, smaller ones to kSwap: with
+// few rows per tile the swapped kernel pulls a weight tile per 16 token rows and
+// becomes bound by L2 -> SM traffic, so it only wins where pair tiles would be
+// mostly padding (decode-sized groups).  GMM_BF16_KERNEL =
+// single | pair | swap overrides the choice (for tuning and tests).
+enum class BF16Kernel { kSingle, kPair, kSwap, kInvalid };
+
+BF16Kernel choose_bf16_kernel(int64_t m, int32_t num_total_groups) {
+  if (const char* env = std::getenv("GMM_BF16_KERNEL")) {
+    if (std::strcmp(env, "single") == 0) return BF16Kernel::kSingle;
+    if (std::strcmp(env, "pair") == 0) return BF16Kernel::kPair;
+    if (std::strcmp(env, "swap") == 0) return BF16Kernel::kSwap;
+    if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return BF16Kernel::kInvalid;
+  }
+  return m >= int64_t(128) * num_total_groups ? BF16Kernel::kPair : BF16Kernel::kSwap;
+}
 
 }  // namespace
 
@@ -201,20 +226,19 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
     return GMM_OK;
   }
 
-  // Groups of a few hundred rows or more run on SM pairs (256-row tiles);
-  // smaller ones on single SMs (128-row tiles waste less on group tails).
-  const bool pair_path = m >= int64_t(192) * num_total_groups;
+  const BF16Kernel kind = choose_bf16_kernel(m, num_total_groups);
+  if (kind == BF16Kernel::kInvalid) return GMM_ERR_SHAPE;
   gmmk::GemmLaunch L{};
   {
     const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
-    const uint32_t box[2] = {64, 128};
+    const uint32_t box[2] = {64, kind == BF16Kernel::kSwap ? 64u : 128u};
     if (int st = make_map(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
   }
   if (transpose_rhs) {
     const uint64_t dims[3] = {uint64_t(k), uint64_t(n), uint64_t(num_local_groups)};
-    const uint32_t box[3] = {64, pair_path ? 128u : 256u, 1};
+    const uint32_t box[3] = {64, kind == BF16Kernel::kSingle ? 256u : 128u, 1};
     if (int st = make_map(&L.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3, rhs, dims, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
@@ -237,12 +261,13 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   L.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
   L.err = err;
   L.raster = 8;
-  // Work items = m-tiles x n-tiles must fit in int32.
+  // Work items (row tiles x n tiles, at most (m/128 + groups) x n/128) must fit in int32.
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
-  if (m_tiles_max * ((n + 255) / 256) > INT32_MAX) return GMM_ERR_SHAPE;
-  cudaError_t e = pair_path
-                      ? gmmk::launch_gemm_bf16_2sm(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s)
-                      : gmmk::launch_gemm_bf16(L, transpose_rhs != 0, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+  if (m_tiles_max * ((n + 127) / 128) > INT32_MAX) return GMM_ERR_SHAPE;
+  const bool nt = transpose_rhs != 0, f32 = out_dtype == GMM_DTYPE_F32;
+  cudaError_t e = kind == BF16Kernel::kPair   ? gmmk::launch_gemm_bf16_2sm(L, nt, f32, dev.sms, s)
+                  : kind == BF16Kernel::kSwap ? gmmk::launch_gemm_bf16_swap(L, nt, f32, dev.sms, s)
+                                              : gmmk::launch_gemm_bf16(L, nt, f32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
 }

@@ -26,6 +26,11 @@ cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int gri
 
 // Same computation on SM pairs (256 x 256 tiles, cta_group::2).  tm_rhs boxes:
 // NT {64, 128, 1}; NN {64, 64, 1}.  Launches at most max_ctas CTAs.
+// Same computation with the roles swapped for small groups: 128 weight rows
+// on the MMA's M side, up to 256 of a group's rows on its N side.  tm_lhs box
+// {64, 64}; tm_rhs boxes: NT {64, 128, 1}; NN {64, 64, 1}.
+cudaError_t launch_gemm_bf16_swap(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
+
 cudaError_t launch_gemm_bf16_2sm(const GemmLaunch& p, bool nt, bool out_f32, int max_ctas, cudaStream_t stream);
 
 // tgmm: out[g] = lhs_g^T dout_g (bf16 operands, fp32 accumulate).

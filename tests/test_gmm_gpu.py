@@ -50,32 +50,40 @@ def _gmm_case(m, k, n, sizes, *, transpose_rhs=True, out_dtype=torch.bfloat16, g
 
 LAYOUTS = [pytest.param(True, id="NT"), pytest.param(False, id="NN")]
 ODT = [pytest.param(torch.bfloat16, id="bf16out"), pytest.param(torch.float32, id="f32out")]
+KERNELS = ["single", "pair", "swap"]
+
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    """Runs the test once per bf16 forward kernel (GMM_BF16_KERNEL override)."""
+    monkeypatch.setenv("GMM_BF16_KERNEL", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
 @pytest.mark.parametrize("out_dtype", ODT)
-def test_ragged_tiles_and_tails(transpose_rhs, out_dtype):
+def test_ragged_tiles_and_tails(transpose_rhs, out_dtype, kernel):
     # 5 groups (one empty, one of a single row), sum 588 < m = 700; k = 200 is
     # 3 full 64-wide steps plus 8; n = 520 is two 256-wide tiles plus 8.
     _gmm_case(700, 200, 520, [130, 0, 257, 1, 200], transpose_rhs=transpose_rhs, out_dtype=out_dtype)
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
-def test_small_m_single_tile(transpose_rhs):
+def test_small_m_single_tile(transpose_rhs, kernel):
     _gmm_case(50, 64, 256, [20, 30], transpose_rhs=transpose_rhs, out_dtype=torch.float32)
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
-def test_one_group_is_dense(transpose_rhs):
+def test_one_group_is_dense(transpose_rhs, kernel):
     _gmm_case(384, 512, 768, [384], transpose_rhs=transpose_rhs)
 
 
-def test_all_groups_empty_gives_zeros():
+def test_all_groups_empty_gives_zeros(kernel):
     out = _gmm_case(300, 128, 256, [0, 0, 0])
     assert (out == 0).all()
 
 
-def test_many_groups_multi_chunk_scan():
+def test_many_groups_multi_chunk_scan(kernel):
     rng = np.random.default_rng(3)
     sizes = rng.integers(0, 9, 300).astype(np.int32)
     sizes[rng.choice(300, 60, replace=False)] = 0
@@ -83,17 +91,17 @@ def test_many_groups_multi_chunk_scan():
 
 
 @pytest.mark.parametrize("go,local", [(0, 3), (2, 3), (3, 3), (5, 1)])
-def test_group_offset_slices(go, local):
+def test_group_offset_slices(go, local, kernel):
     _gmm_case(900, 192, 264, [150, 0, 333, 100, 7, 200], group_offset=go, local=local, seed=go)
 
 
 @pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float32])
-def test_bias(bias_dtype):
+def test_bias(bias_dtype, kernel):
     _gmm_case(400, 128, 264, [100, 0, 250], bias_dtype=bias_dtype, out_dtype=torch.float32)
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
-def test_integer_inputs_bit_exact(transpose_rhs):
+def test_integer_inputs_bit_exact(transpose_rhs, kernel):
     # Each group's expert is (g+1) * base: a row multiplied by the wrong expert
     # is off by an integer factor, and every sum is exact in fp32.
     m, k, n = 520, 256, 264
@@ -121,7 +129,7 @@ def test_nt_matches_nn_on_transposed_weight():
     assert torch.equal(nt, nn)
 
 
-def test_device_error_flags_and_clamping():
+def test_device_error_flags_and_clamping(kernel):
     m, k, n = 256, 64, 256
     lhs = W.normal((m, k), 1.0, 31, DEV)
     rhs = W.normal((3, n, k), 0.05, 32, DEV)
@@ -191,23 +199,27 @@ def test_tgmm_sums_to_dense_when_groups_cover_all_rows():
 # ------------------------------------------------ SM-pair kernel (>= 192 rows per group on average)
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
 @pytest.mark.parametrize("out_dtype", ODT)
-def test_pair_ragged_tiles_and_tails(transpose_rhs, out_dtype):
+def test_pair_ragged_tiles_and_tails(transpose_rhs, out_dtype, monkeypatch):
+    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
     # 256-row pair tiles over groups of 300, 0, 513, 1, 400 rows (sum 1214 < m = 1500);
     # k = 200 and n = 520 leave tails in both dimensions.
     _gmm_case(1500, 200, 520, [300, 0, 513, 1, 400], transpose_rhs=transpose_rhs, out_dtype=out_dtype, seed=3)
 
 
 @pytest.mark.parametrize("go,local", [(0, 3), (2, 3), (5, 1)])
-def test_pair_group_offset_slices(go, local):
+def test_pair_group_offset_slices(go, local, monkeypatch):
+    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
     _gmm_case(1800, 192, 264, [250, 0, 333, 700, 7, 300], group_offset=go, local=local, seed=10 + go)
 
 
-def test_pair_bias_and_single_group():
+def test_pair_bias_and_single_group(monkeypatch):
+    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
     _gmm_case(1024, 256, 520, [1024], bias_dtype=torch.bfloat16, out_dtype=torch.float32, seed=17)
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
-def test_pair_integer_inputs_bit_exact(transpose_rhs):
+def test_pair_integer_inputs_bit_exact(transpose_rhs, monkeypatch):
+    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
     m, k, n = 1100, 256, 264
     sizes = np.array([257, 0, 255, 400, 1], np.int32)
     lhs = W.integer_valued((m, k), -8, 8, 13, DEV)
@@ -219,17 +231,26 @@ def test_pair_integer_inputs_bit_exact(transpose_rhs):
     np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), ref)
 
 
-def test_pair_and_single_sm_kernels_agree():
-    # The same rows and experts run once on the SM-pair kernel (m / G = 192) and once on
-    # the single-SM kernel (two trailing empty groups with junk experts make m / G < 192).
-    # Both feed identical products to the tensor core in the same k order.
+def test_three_kernels_agree_on_the_same_problem(monkeypatch):
+    # The same rows and experts through each bf16 forward kernel: every result is
+    # inside the bound, and the pair and single-SM kernels (same tile orientation,
+    # same k order) agree bit for bit.
     m, k, n = 1536, 320, 512
     sizes = np.array([200, 340, 0, 300, 150, 0, 400, 146], np.int32)
     lhs = W.normal((m, k), 1.0, 21, DEV)
     w = W.normal((8, n, k), 0.05, 22, DEV)
-    pair = G.gmm(lhs, w, _gs(sizes), out_dtype=torch.float32)
-    w10 = torch.cat([w, W.normal((2, n, k), 3.0, 23, DEV)])
-    single = G.gmm(lhs, w10, _gs(np.concatenate([sizes, [0, 0]])), out_dtype=torch.float32)
-    assert torch.equal(pair, single)
     ref, mag = oracle_gmm(lhs, w, sizes)
-    check_close(pair, ref, mag, "pair")
+    outs = {}
+    for kern in KERNELS:
+        monkeypatch.setenv("GMM_BF16_KERNEL", kern)
+        outs[kern] = G.gmm(lhs, w, _gs(sizes), out_dtype=torch.float32)
+        check_close(outs[kern], ref, mag, kern)
+    assert torch.equal(outs["pair"], outs["single"])
+
+
+def test_unknown_kernel_override_is_rejected(monkeypatch):
+    monkeypatch.setenv("GMM_BF16_KERNEL", "fastest")
+    lhs = W.normal((64, 64), 1.0, 1, DEV)
+    w = W.normal((1, 64, 64), 0.05, 2, DEV)
+    with pytest.raises(G.GmmError):
+        G.gmm(lhs, w, _gs([64]))
