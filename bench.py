@@ -145,6 +145,7 @@ def run_gpu(args, rank, world):
     import moe_grouped_matrix_gb300 as G
     from moe_grouped_matrix_gb300 import build as B
     from moe_grouped_matrix_gb300 import workloads as W
+    from moe_grouped_matrix_gb300.sharding import max_over_ranks
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -191,10 +192,7 @@ def run_gpu(args, rank, world):
     clock_info = clocks.stop() if clocks else None
     total_ms = t_start.elapsed_time(t_end)
     per_launch = [s.elapsed_time(e) for s, e in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)
     if G.read_device_errors() != 0:
         raise RuntimeError("device error flags set during the benchmark")
 
@@ -230,10 +228,7 @@ def run_gpu(args, rank, world):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, device=dev)
         h2d = h_lhs.numel() * 2 + h_rhs.numel() * 2 + h_gs.numel() * 4
         d2h = h_out.numel() * 2
         e2e = {"value": flops * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
