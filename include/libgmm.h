@@ -94,12 +94,13 @@ size_t gmm_workspace_bytes(void);
  *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  It is built for
  *                decode-sized groups (a few rows each): it streams every weight tile once per
  *                16 rows of its group.
- *                Without scale, bf16 weights run on one of three kernels chosen from the average
- *                group size m / num_total_groups (SM-pair 256x256 tiles for >= 128 rows, else
- *                weights-as-M tiles whose token side is a group's rows rounded to 16); the
- *                environment variable GMM_BF16_KERNEL = auto | pair | swap | single overrides
- *                the choice (any other value: GMM_ERR_SHAPE).  All give results within the
- *                same bound; they may differ in the last bits.
+ *                Without scale, bf16 weights run on one of four kernels chosen from the average
+ *                group size m / num_total_groups: SM-pair 256x256 row tiles (>= 1024 rows),
+ *                SM-pair tiles of 256 weight rows x up to 256 group rows rounded to 32 (>= 16),
+ *                or single-SM tiles of 128 weight rows x group rows rounded to 16 (fewer).
+ *                The environment variable GMM_BF16_KERNEL = auto | pair | swap_pair | swap |
+ *                single overrides the choice (any other value: GMM_ERR_SHAPE).  All give
+ *                results within the same bound; they may differ in the last bits.
  *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
  *   out          [m, n] of out_dtype (BF16 or F32).
  *   Sizes: m >= 0, k >= 8, n >= 8, k % 8 == 0, n % 8 == 0 (16-byte rows); lhs, rhs,

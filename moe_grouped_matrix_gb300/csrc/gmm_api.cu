@@ -97,26 +97,29 @@ int make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, int rank,
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 
 // The bf16 forward kernels:
-//   kPair   256 x 256 tiles on SM pairs: the fastest per MMA, but a group's last
-//           256-row tile may be mostly padding;
-//   kSwap   weights on the MMA's M side, a group's rows (up to 256, rounded to
-//           16) on its N side: almost no padding, one SM per tile;
-//   kSingle 128 x 256 tiles on one SM.
-// Groups averaging 128 rows or more go to kPair, smaller ones to kSwap: with
-// few rows per tile the swapped kernel pulls a weight tile per 16 token rows and
-// becomes bound by L2 -> SM traffic, so it only wins where pair tiles would be
-// mostly padding (decode-sized groups).  GMM_BF16_KERNEL =
-// single | pair | swap overrides the choice (for tuning and tests).
-enum class BF16Kernel { kSingle, kPair, kSwap, kInvalid };
+//   kPair     256 x 256 tiles of rows x n on SM pairs: the fastest per MMA, but
+//             a group's last 256-row tile may be mostly padding;
+//   kSwapPair SM pairs with 256 weight rows on the MMA's M side and up to 256
+//             of a group's rows on its N side (rounded to 32): little padding,
+//             pair-level traffic per SM;
+//   kSwap     one SM, 128 weight rows x up to 256 rows (rounded to 16);
+//   kSingle   one SM, 128 x 256 tiles of rows x n.
+// Groups averaging 1024 rows or more go to kPair, 16 or more to kSwapPair,
+// fewer to kSwap.  GMM_BF16_KERNEL = single | pair | swap | swap_pair
+// overrides the choice (for tuning and tests).
+enum class BF16Kernel { kSingle, kPair, kSwap, kSwapPair, kInvalid };
 
 BF16Kernel choose_bf16_kernel(int64_t m, int32_t num_total_groups) {
   if (const char* env = std::getenv("GMM_BF16_KERNEL")) {
     if (std::strcmp(env, "single") == 0) return BF16Kernel::kSingle;
     if (std::strcmp(env, "pair") == 0) return BF16Kernel::kPair;
     if (std::strcmp(env, "swap") == 0) return BF16Kernel::kSwap;
+    if (std::strcmp(env, "swap_pair") == 0) return BF16Kernel::kSwapPair;
     if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return BF16Kernel::kInvalid;
   }
-  return m >= int64_t(128) * num_total_groups ? BF16Kernel::kPair : BF16Kernel::kSwap;
+  if (m >= int64_t(1024) * num_total_groups) return BF16Kernel::kPair;
+  if (m >= int64_t(16) * num_total_groups) return BF16Kernel::kSwapPair;
+  return BF16Kernel::kSwap;
 }
 
 }  // namespace
@@ -231,7 +234,8 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   gmmk::GemmLaunch L{};
   {
     const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
-    const uint32_t box[2] = {64, kind == BF16Kernel::kSwap ? 64u : 128u};
+    const bool swapped = kind == BF16Kernel::kSwap || kind == BF16Kernel::kSwapPair;
+    const uint32_t box[2] = {64, swapped ? 64u : 128u};
     if (int st = make_map(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
@@ -265,9 +269,10 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
   if (m_tiles_max * ((n + 127) / 128) > INT32_MAX) return GMM_ERR_SHAPE;
   const bool nt = transpose_rhs != 0, f32 = out_dtype == GMM_DTYPE_F32;
-  cudaError_t e = kind == BF16Kernel::kPair   ? gmmk::launch_gemm_bf16_2sm(L, nt, f32, dev.sms, s)
-                  : kind == BF16Kernel::kSwap ? gmmk::launch_gemm_bf16_swap(L, nt, f32, dev.sms, s)
-                                              : gmmk::launch_gemm_bf16(L, nt, f32, dev.sms, s);
+  cudaError_t e = kind == BF16Kernel::kPair       ? gmmk::launch_gemm_bf16_2sm(L, nt, f32, dev.sms, s)
+                  : kind == BF16Kernel::kSwapPair ? gmmk::launch_gemm_bf16_2sm_swap(L, nt, f32, dev.sms, s)
+                  : kind == BF16Kernel::kSwap     ? gmmk::launch_gemm_bf16_swap(L, nt, f32, dev.sms, s)
+                                                  : gmmk::launch_gemm_bf16(L, nt, f32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
 }

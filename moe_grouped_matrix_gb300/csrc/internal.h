@@ -31,6 +31,12 @@ cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int gri
 // {64, 64}; tm_rhs boxes: NT {64, 128, 1}; NN {64, 64, 1}.
 cudaError_t launch_gemm_bf16_swap(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
 
+// Pairs with the roles swapped: 256 weight rows on the MMA's M side (128 per
+// CTA), up to 256 of a group's rows on its N side.  tm_lhs box {64, 64};
+// tm_rhs boxes: NT {64, 128, 1}; NN {64, 64, 1}.
+cudaError_t launch_gemm_bf16_2sm_swap(const GemmLaunch& p, bool nt, bool out_f32, int max_ctas,
+                                      cudaStream_t stream);
+
 cudaError_t launch_gemm_bf16_2sm(const GemmLaunch& p, bool nt, bool out_f32, int max_ctas, cudaStream_t stream);
 
 // tgmm: out[g] = lhs_g^T dout_g (bf16 operands, fp32 accumulate).

@@ -50,7 +50,7 @@ def _gmm_case(m, k, n, sizes, *, transpose_rhs=True, out_dtype=torch.bfloat16, g
 
 LAYOUTS = [pytest.param(True, id="NT"), pytest.param(False, id="NN")]
 ODT = [pytest.param(torch.bfloat16, id="bf16out"), pytest.param(torch.float32, id="f32out")]
-KERNELS = ["single", "pair", "swap"]
+KERNELS = ["single", "pair", "swap", "swap_pair"]
 
 
 @pytest.fixture(params=KERNELS)
