@@ -48,8 +48,13 @@ def load_peaks():
 
 
 def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the headline kernel's source and the headers it includes."""
+    h = hashlib.sha256()
+    for path in (KERNEL_SRC, os.path.join(os.path.dirname(KERNEL_SRC), "ptx.cuh"),
+                 os.path.join(os.path.dirname(KERNEL_SRC), "worklist.cuh")):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profile_traffic():
@@ -298,6 +303,24 @@ def run_suite(dev, peaks):
         res[name] = {"ms": ms, "tflops": flops / t / 1e12, "gbs": bytes_ / t / 1e9,
                      "bound": "tensor" if flops / (peaks["bf16"] * 1e12) > bytes_ / (peaks["hbm"] * 1e9) else "hbm",
                      "roofline_frac": floor / t, "frac_of_bf16_peak": flops / t / 1e12 / peaks["bf16"]}
+
+    # Context, not the reference arm: cuBLAS batched matmul on the dense equivalent of
+    # the headline (8 experts x 2048 rows, k 4096 -> n 28672), same GPU, same run.
+    a = W.normal((8, 2048, 4096), 1.0, 91, dev)
+    wt = W.normal((8, 28672, 4096), 0.02, 92, dev)
+    c = torch.empty((8, 2048, 28672), dtype=torch.bfloat16, device=dev)
+    ms = _time_call(torch, lambda: torch.bmm(a, wt.transpose(1, 2), out=c), iters=10)
+    record("cublas_bmm_dense_equivalent", ms, 2.0 * 8 * 2048 * 28672 * 4096,
+           a.numel() * 2 + wt.numel() * 2 + c.numel() * 2)
+    # ours on the same shapes (8 groups of 2048 rows), timed the same short way right after
+    gs8 = torch.full((8,), 2048, dtype=torch.int32, device=dev)
+    a2 = a.view(16384, 4096)
+    c2 = c.view(16384, 28672)
+    ms = _time_call(torch, lambda: G.gmm(a2, wt, gs8, transpose_rhs=True, out=c2), iters=10)
+    record("gmm_same_shapes_as_cublas_line", ms, 2.0 * 8 * 2048 * 28672 * 4096,
+           a.numel() * 2 + wt.numel() * 2 + c.numel() * 2)
+    del a, wt, c, a2, c2
+    torch.cuda.empty_cache()
 
     mo = W.moe128(dev)
     sizes = mo["group_sizes"]
