@@ -63,7 +63,7 @@ enum {
 #define GMM_DEVERR_GROUP_SIZES_EXCEED_M 0x2u /* sum(group_sizes) > m (groups cut at row m) */
 #define GMM_DEVERR_TIMEOUT 0x4u              /* an internal pipeline wait gave up; output is undefined */
 
-/* Largest num_total_groups (gmm) or num_groups (tgmm) accepted. */
+/* Largest num_total_groups (gmm, tgmm_local) or num_groups (tgmm) accepted. */
 #define GMM_MAX_GROUPS 1024
 
 /* Size in bytes of the workspace every call needs (a small constant). */
@@ -114,6 +114,29 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
         size_t workspace_bytes, void* stream);
 
 /*
+ * gmm_into: gmm() writing into an output the caller has already filled (page
+ * "tpu-inference ...", gmm.py: the existing_out argument, aliased to the
+ * output, whose tiles are first seeded from existing_out; the zeroing pass
+ * _zero_uninitialized_memory runs only when no existing_out is given).
+ *
+ *   Rows of the local groups are computed exactly as gmm() computes them (same
+ *   kernels, same rounding).  Every other row of out (rows of non-local groups,
+ *   rows at or past sum(group_sizes)) is neither read nor written: it keeps what
+ *   the caller put there.  The pages' existing_out has the output's dtype, so
+ *   here it is simply `out`, of out_dtype.
+ *
+ *   Arguments, layouts, alignment and errors are those of gmm().  A typical use
+ *   is expert parallelism without a combine: shards whose expert slices are
+ *   disjoint call gmm_into on one shared [m, n] buffer, one after another or on
+ *   streams ordered so that no two run at once on overlapping rows.
+ */
+int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+             int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+             int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+             const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/*
  * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS
  * gmm_v2 kernel ...", Context section; gmm.py make_group_metadata docstring on
  * visiting empty groups so that their output is zeroed).
@@ -130,6 +153,29 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
 int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
          const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
          size_t workspace_bytes, void* stream);
+
+/*
+ * tgmm_local: tgmm() over one contiguous slice of the groups, the drhs of an
+ * expert shard (page "tpu-inference ...", gmm.py make_group_metadata:
+ * start_group and num_nonzero_groups select the groups a shard computes, and
+ * visit_empty_groups keeps a tile for every empty group so that its output is
+ * zeroed).
+ *
+ *   out[l, kk, c] = sum_{r in group group_offset + l} lhs[r, kk] * dout[r, c]
+ *   for 0 <= l < num_local_groups; group rows come from the prefix sum of all
+ *   num_total_groups sizes, so rows of the groups outside the slice are not read.
+ *
+ *   group_sizes  device int32 [num_total_groups], 1 <= num_total_groups <= GMM_MAX_GROUPS.
+ *   group_offset first group of the slice; 1 <= num_local_groups and
+ *                0 <= group_offset <= num_total_groups - num_local_groups
+ *                (else GMM_ERR_SHAPE / GMM_ERR_GROUP_OFFSET).
+ *   out          [num_local_groups, k, n] F32 or BF16.
+ *   Everything else as tgmm(), which is tgmm_local(..., num_groups, 0, num_groups, ...).
+ */
+int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,
+               int64_t n, const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
+               int32_t num_local_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+               void* stream);
 
 /* Size of the device scratch array compiled into the library for gmm_noalloc(). */
 #define GMM_NOALLOC_SCRATCH_BYTES 256

@@ -43,6 +43,8 @@ SIGNATURES = {
     "gmm_workspace_bytes": ([], _SZ),
     "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
     "tgmm": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _P, _I, _P, _SZ, _P], _I),
+    "gmm_into": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
+    "tgmm_local": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
     "gmm_read_device_errors": ([_P, _P, _U32P], _I),
     "gmm_status_string": ([_I], ctypes.c_char_p),
@@ -108,10 +110,8 @@ def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
     return t
 
 
-def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
-        out_dtype=torch.bfloat16, workspace=None, stream=None):
-    """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
-    for each row r of local group g; all other rows of out are zero."""
+def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out, out_dtype,
+              workspace, stream):
     lib = load_library()
     _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
     if group_sizes.dtype != torch.int32:
@@ -124,6 +124,8 @@ def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True
     if out is None:
         out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
     _dev(out, "out")
+    if tuple(out.shape) != (m, n):
+        raise ValueError(f"out must be [{m}, {n}], got {list(out.shape)}")
     ws = workspace if workspace is not None else workspace_for(lhs.device)
     nb = 0
     if rhs_scale is not None:
@@ -131,13 +133,60 @@ def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True
         nb = rhs_scale.shape[1]
     if rhs_bias is not None:
         _dev(rhs_bias, "rhs_bias")
-    rc = lib.gmm(lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n,
-                 int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
-                 None if rhs_scale is None else rhs_scale.data_ptr(), nb,
-                 None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
-                 out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+    rc = getattr(lib, fn)(
+        lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n, int(bool(transpose_rhs)),
+        group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
+        None if rhs_scale is None else rhs_scale.data_ptr(), nb,
+        None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
+        out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
     if rc != 0:
-        raise GmmError("gmm", rc)
+        raise GmmError(fn, rc)
+    return out
+
+
+def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
+        out_dtype=torch.bfloat16, workspace=None, stream=None):
+    """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
+    for each row r of local group g; all other rows of out are zero."""
+    return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
+                     out_dtype, workspace, stream)
+
+
+def gmm_into(lhs, rhs, group_sizes, out, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0,
+             workspace=None, stream=None):
+    """As gmm, but only the local groups' rows of `out` are written; every other row keeps the
+    caller's contents (the existing-output mode)."""
+    if out is None:
+        raise ValueError("gmm_into needs an output tensor")
+    return _gmm_call("gmm_into", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
+                     out.dtype, workspace, stream)
+
+
+def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, out=None, out_dtype=torch.float32,
+               workspace=None, stream=None):
+    """out[l] = lhs_g^T @ dout_g for g = group_offset + l, 0 <= l < num_local_groups (zero blocks for
+    empty groups); group rows come from all of group_sizes."""
+    lib = load_library()
+    _dev(lhs, "lhs"), _dev(dout, "dout"), _dev(group_sizes, "group_sizes")
+    if group_sizes.dtype != torch.int32:
+        raise TypeError("group_sizes must be int32")
+    m, k = lhs.shape
+    if dout.shape[0] != m:
+        raise ValueError("lhs and dout must have the same number of rows")
+    n = dout.shape[1]
+    G = group_sizes.shape[0]
+    L = G - int(group_offset) if num_local_groups is None else int(num_local_groups)
+    if out is None:
+        out = torch.empty((max(L, 0), k, n), dtype=out_dtype, device=lhs.device)
+    _dev(out, "out")
+    if tuple(out.shape) != (L, k, n):
+        raise ValueError(f"out must be [{L}, {k}, {n}], got {list(out.shape)}")
+    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    rc = lib.tgmm_local(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(),
+                        G, int(group_offset), L, out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(),
+                        _stream(lhs.device, stream))
+    if rc != 0:
+        raise GmmError("tgmm_local", rc)
     return out
 
 

@@ -98,6 +98,7 @@ struct Params {
   int32_t bias_f32;
   void* out;
   uint32_t* err;
+  int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
 };
 
 // 16 e4m3fn codes (one 16-byte chunk, lowest k first) -> 16 bf16 (8 words).
@@ -425,16 +426,19 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
         }
       }
     }
-    // Rows outside [offs[first local], offs[last local + 1]) are zero.
-    const int64_t row_bytes = int64_t(p.n) * (kOutF32 ? 4 : 2);
-    const int64_t lo_bytes = int64_t(offs[p.group_offset]) * row_bytes;
-    const int64_t hi_begin = int64_t(offs[p.group_offset + p.num_local_groups]) * row_bytes;
-    const int64_t n_lo = lo_bytes / 16;
-    const int64_t n_all = n_lo + (int64_t(p.m) * row_bytes - hi_begin) / 16;
-    const int64_t stride = int64_t(gridDim.x) * 128;
-    for (int64_t i = int64_t(blockIdx.x) * 128 + (threadIdx.x - 64); i < n_all; i += stride) {
-      const int64_t byte = i < n_lo ? i * 16 : hi_begin + (i - n_lo) * 16;
-      st_global_v4(static_cast<uint8_t*>(p.out) + byte, 0u, 0u, 0u, 0u);
+    // Rows outside [offs[first local], offs[last local + 1]) are zero, unless the
+    // caller keeps them (gmm_into).
+    if (p.zero_rest) {
+      const int64_t row_bytes = int64_t(p.n) * (kOutF32 ? 4 : 2);
+      const int64_t lo_bytes = int64_t(offs[p.group_offset]) * row_bytes;
+      const int64_t hi_begin = int64_t(offs[p.group_offset + p.num_local_groups]) * row_bytes;
+      const int64_t n_lo = lo_bytes / 16;
+      const int64_t n_all = n_lo + (int64_t(p.m) * row_bytes - hi_begin) / 16;
+      const int64_t stride = int64_t(gridDim.x) * 128;
+      for (int64_t i = int64_t(blockIdx.x) * 128 + (threadIdx.x - 64); i < n_all; i += stride) {
+        const int64_t byte = i < n_lo ? i * 16 : hi_begin + (i - n_lo) * 16;
+        st_global_v4(static_cast<uint8_t*>(p.out) + byte, 0u, 0u, 0u, 0u);
+      }
     }
   } else if constexpr (kE4M3) {
     // ---------------------------------------------------------------- e4m3 -> bf16 decoders
@@ -510,7 +514,7 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Layout<kE4M3>::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
-           L.num_blocks, L.bias, L.bias_f32, L.out, L.err};
+           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest};
   kern<<<grid, kE4M3 ? 192 + kConvThreads : 192, Layout<kE4M3>::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

@@ -155,11 +155,18 @@ int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags) {
   return GMM_OK;
 }
 
-int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
-        int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
-        int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
-        const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
-        void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of gmm and gmm_into: zero_rest says whether rows of the
+// groups outside the local slice are written as zero (gmm) or left as the
+// caller filled them (gmm_into).
+int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+             int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+             int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+             const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
+             size_t workspace_bytes, void* stream, int32_t zero_rest) {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (rhs_dtype != GMM_DTYPE_BF16 && rhs_dtype != GMM_DTYPE_E4M3) return GMM_ERR_DTYPE;
@@ -224,6 +231,7 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
     S.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
     S.out = out;
     S.err = err;
+    S.zero_rest = zero_rest;
     cudaError_t e = gmmk::launch_scaled(S, rhs_dtype == GMM_DTYPE_E4M3, out_dtype == GMM_DTYPE_F32, dev.sms, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return GMM_OK;
@@ -265,6 +273,7 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   L.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
   L.err = err;
   L.raster = 8;
+  L.zero_rest = zero_rest;
   // Work items (row tiles x n tiles, at most (m/128 + groups) x n/128) must fit in int32.
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
   if (m_tiles_max * ((n + 127) / 128) > INT32_MAX) return GMM_ERR_SHAPE;
@@ -277,18 +286,46 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
   return GMM_OK;
 }
 
-int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
-         const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
-         size_t workspace_bytes, void* stream) {
+}  // namespace
+
+extern "C" {
+
+int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+        int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+        int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+        const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+        void* stream) {
+  return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                  num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out,
+                  out_dtype, workspace, workspace_bytes, stream, 1);
+}
+
+int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+             int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+             int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+             const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
+             size_t workspace_bytes, void* stream) {
+  return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                  num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out,
+                  out_dtype, workspace, workspace_bytes, stream, 0);
+}
+
+int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,
+               int64_t n, const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
+               int32_t num_local_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
   if (lhs == nullptr || dout == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16 || dout_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (!fits_i32(m) || !fits_i32(k) || !fits_i32(n) || k < 8 || n < 8 || k % 8 != 0 || n % 8 != 0)
     return GMM_ERR_SHAPE;
-  if (num_groups < 1 || num_groups > GMM_MAX_GROUPS) return GMM_ERR_SHAPE;
+  if (num_total_groups < 1 || num_total_groups > GMM_MAX_GROUPS || num_local_groups < 1 ||
+      num_local_groups > num_total_groups)
+    return GMM_ERR_SHAPE;
+  if (group_offset < 0 || group_offset > num_total_groups - num_local_groups) return GMM_ERR_GROUP_OFFSET;
   if (!aligned16(lhs) || !aligned16(dout) || !aligned16(out)) return GMM_ERR_ALIGN;
   if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
-  const int64_t items = int64_t(num_groups) * ((k + 127) / 128) * ((n + 255) / 256);
+  const int64_t items = int64_t(num_local_groups) * ((k + 127) / 128) * ((n + 255) / 256);
   if (items > INT32_MAX) return GMM_ERR_SHAPE;
   DeviceInfo dev;
   if (int st = current_device(&dev)) return st;
@@ -314,14 +351,16 @@ int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64
   }
   {
     const bool f32 = out_dtype == GMM_DTYPE_F32;
-    const uint64_t dims[3] = {uint64_t(n), uint64_t(k), uint64_t(num_groups)};
+    const uint64_t dims[3] = {uint64_t(n), uint64_t(k), uint64_t(num_local_groups)};
     const uint32_t box[3] = {f32 ? 32u : 64u, 32u, 1u};
     if (int st = make_map(&L.tm_out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                           f32 ? 4 : 2, 3, out, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return st;
   }
   L.group_sizes = group_sizes;
-  L.num_groups = num_groups;
+  L.num_total_groups = num_total_groups;
+  L.group_offset = group_offset;
+  L.num_local_groups = num_local_groups;
   L.m = int32_t(m);
   L.n = int32_t(n);
   L.k = int32_t(k);
@@ -330,6 +369,13 @@ int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64
   cudaError_t e = gmmk::launch_tgmm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
+}
+
+int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
+         const int32_t* group_sizes, int32_t num_groups, void* out, int out_dtype, void* workspace,
+         size_t workspace_bytes, void* stream) {
+  return tgmm_local(lhs, lhs_dtype, dout, dout_dtype, m, k, n, group_sizes, num_groups, 0, num_groups, out,
+                    out_dtype, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -19,7 +19,8 @@ struct GemmLaunch {
   const void* bias;  // NULL or [L, 1, n]
   int32_t bias_f32;  // bias dtype: 1 = f32, 0 = bf16
   uint32_t* err;
-  int32_t raster;  // n-tiles per L2 super-column
+  int32_t raster;     // n-tiles per L2 super-column
+  int32_t zero_rest;  // 1: zero rows outside the local groups; 0: leave them as they are
 };
 
 cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
@@ -43,11 +44,11 @@ cudaError_t launch_gemm_bf16_2sm(const GemmLaunch& p, bool nt, bool out_f32, int
 struct TgmmLaunch {
   CUtensorMap tm_lhs;   // lhs  [m, k], box {64, 64}
   CUtensorMap tm_dout;  // dout [m, n], box {64, 64}
-  CUtensorMap tm_out;   // out [G, k, n], box {128 bytes of n, 32, 1}
-  const int32_t* group_sizes;
-  int32_t num_groups;
+  CUtensorMap tm_out;   // out [L, k, n], box {128 bytes of n, 32, 1}
+  const int32_t* group_sizes;  // [num_total_groups]
+  int32_t num_total_groups, group_offset, num_local_groups;
   int32_t m, n, k;
-  void* out;  // [G, k, n]
+  void* out;  // [L, k, n]: local group g is group group_offset + g
   uint32_t* err;
 };
 
@@ -67,6 +68,7 @@ struct ScaledLaunch {
   int32_t bias_f32;
   void* out;
   uint32_t* err;
+  int32_t zero_rest;  // 1: zero rows outside the local groups; 0: leave them as they are
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);

@@ -1,10 +1,13 @@
 // Backward weight gradient per group: out[g] = lhs_g^T @ dout_g.
 //
-// For every group g (page "Megablox: transposed-RHS gmm_v2 kernel for the
-// backward dlhs", Context: the drhs of the grouped matmul; page
+// For every local group g (page "Megablox: transposed-RHS gmm_v2 kernel for
+// the backward dlhs", Context: the drhs of the grouped matmul; page
 // "tpu-inference ...", gmm.py make_group_metadata: empty groups are still
-// visited so that their output is zeroed):
-//   out[g, kk, c] = sum_{r in group g} lhs[r, kk] * dout[r, c].
+// visited so that their output is zeroed, and start_group / num_nonzero_groups
+// pick the slice of groups a shard computes):
+//   out[g, kk, c] = sum_{r in group group_offset + g} lhs[r, kk] * dout[r, c].
+// Group offsets run over all num_total_groups sizes, so rows of the groups
+// before the slice are skipped.
 // The contraction runs over the group's rows.  Both operands are read in
 // place from their row-major [rows, features] layout as MN-major tcgen05
 // operands (A = lhs_g^T: 128 lhs columns x 64 rows; B = dout_g: 256 dout
@@ -59,7 +62,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
   const int32_t* group_sizes;
-  int32_t num_groups;
+  int32_t num_total_groups, group_offset, num_local_groups;
   int32_t m, n, k;
   void* out;
   uint32_t* err;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + OFF_TMEM, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_group_offsets(p.group_sizes, p.num_groups, p.m, offs, p.err);
+  if (warp == 2) build_group_offsets(p.group_sizes, p.num_total_groups, p.m, offs, p.err);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -130,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t k_tiles = (p.k + BM - 1) / BM;
   const int32_t n_tiles = (p.n + BN - 1) / BN;
   const int32_t per_group = k_tiles * n_tiles;
-  const int32_t total = p.num_groups * per_group;
+  const int32_t total = p.num_local_groups * per_group;
+  // Work item w covers local group g = w / per_group; its rows start at
+  // loffs[g] (offsets run over all groups) and it writes out[g].
+  const int32_t* loffs = offs + p.group_offset;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t g = w / per_group;
         const int32_t r = w - g * per_group;
         const int32_t kt = r / n_tiles, nt = r - kt * n_tiles;
-        const int32_t row_begin = offs[g], rows = offs[g + 1] - offs[g];
+        const int32_t row_begin = loffs[g], rows = loffs[g + 1] - loffs[g];
         for (int32_t c = 0; c * BR < rows; ++c) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const int32_t g = w / per_group;
-      const int32_t rows = offs[g + 1] - offs[g];
+      const int32_t rows = loffs[g + 1] - loffs[g];
       if (rows == 0) continue;  // the epilogue writes zeros; no accumulator is used
       if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
       tc_fence_after();
@@ -262,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t g = w / per_group;
       const int32_t r = w - g * per_group;
       const int32_t kt = r / n_tiles, nt = r - kt * n_tiles;
-      const int32_t rows = offs[g + 1] - offs[g];
+      const int32_t rows = loffs[g + 1] - loffs[g];
       const int32_t krow0 = kt * BM + quarter * 32;
       if (rows == 0) {
         float z[kColsPerBox];
@@ -319,7 +325,7 @@ cudaError_t launch_impl(const TgmmLaunch& L, int grid, cudaStream_t stream) {
   auto kern = tgmm_kernel<kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  Params p{L.group_sizes, L.num_groups, L.m, L.n, L.k, L.out, L.err};
+  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.err};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, L.tm_out, p);
   return cudaGetLastError();
 }

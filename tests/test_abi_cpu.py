@@ -29,7 +29,7 @@ def lib():
 def test_header_declares_the_expected_calls():
     assert declared_functions() == sorted(
         ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error",
-         "gmm_noalloc"])
+         "gmm_noalloc", "gmm_into", "tgmm_local"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -48,13 +48,13 @@ def test_status_strings(lib):
 FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
 
 
-def call_gmm(lib, **over):
+def call_gmm(lib, fn="gmm", **over):
     a = dict(lhs=FAKE, lhs_dtype=0, m=256, k=128, rhs=FAKE, rhs_dtype=0, L=4, n=256, trhs=1, gs=FAKE, G=4, go=0,
              scale=None, nb=0, bias=None, bias_dtype=0, out=FAKE, out_dtype=0, ws=FAKE, ws_bytes=256, stream=None)
     a.update(over)
-    return lib.gmm(a["lhs"], a["lhs_dtype"], a["m"], a["k"], a["rhs"], a["rhs_dtype"], a["L"], a["n"], a["trhs"],
-                   a["gs"], a["G"], a["go"], a["scale"], a["nb"], a["bias"], a["bias_dtype"], a["out"],
-                   a["out_dtype"], a["ws"], a["ws_bytes"], a["stream"])
+    return getattr(lib, fn)(a["lhs"], a["lhs_dtype"], a["m"], a["k"], a["rhs"], a["rhs_dtype"], a["L"], a["n"], a["trhs"],
+                                a["gs"], a["G"], a["go"], a["scale"], a["nb"], a["bias"], a["bias_dtype"],
+                                a["out"], a["out_dtype"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("over,status", [
@@ -68,8 +68,9 @@ def call_gmm(lib, **over):
     (dict(lhs=ctypes.c_void_p((1 << 20) + 8)), 4), (dict(out=ctypes.c_void_p((1 << 20) + 4)), 4),
     (dict(ws=None), 6), (dict(ws_bytes=8), 6),
 ])
-def test_gmm_host_validation(lib, over, status):
-    assert call_gmm(lib, **over) == status
+@pytest.mark.parametrize("fn", ["gmm", "gmm_into"])
+def test_gmm_host_validation(lib, fn, over, status):
+    assert call_gmm(lib, fn, **over) == status
 
 
 def test_tgmm_host_validation(lib):
@@ -83,3 +84,17 @@ def test_tgmm_host_validation(lib):
     assert t(G=0) == 3
     assert t(out=ctypes.c_void_p((1 << 20) + 2)) == 4
     assert t(wb=0) == 6
+
+
+def test_tgmm_local_host_validation(lib):
+    t = lambda **o: lib.tgmm_local(o.get("lhs", FAKE), 0, FAKE, 0, o.get("m", 64), 128, 256, o.get("gs", FAKE),
+                                   o.get("G", 8), o.get("go", 2), o.get("L", 4), o.get("out", FAKE), 1, FAKE, 256,
+                                   None)
+    assert t(lhs=None) == 1
+    assert t(gs=None) == 1
+    assert t(L=0) == 3
+    assert t(L=9) == 3
+    assert t(G=2000, L=4) == 3
+    assert t(go=5) == 5
+    assert t(go=-1) == 5
+    assert t(out=ctypes.c_void_p((1 << 20) + 4)) == 4
