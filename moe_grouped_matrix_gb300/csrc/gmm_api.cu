@@ -122,6 +122,17 @@ BF16Kernel choose_bf16_kernel(int64_t m, int32_t num_total_groups) {
   return BF16Kernel::kSwap;
 }
 
+// e4m3 weights run on the e4m3 tensor-core kernel (gemm_fp8.cu) by default;
+// GMM_E4M3_KERNEL = decode selects the kernel that decodes the weights to bf16
+// (gemm_scaled.cu), kept for comparison.  -1: unknown value.
+int choose_e4m3_decode() {
+  if (const char* env = std::getenv("GMM_E4M3_KERNEL")) {
+    if (std::strcmp(env, "decode") == 0) return 1;
+    if (std::strcmp(env, "auto") != 0 && std::strcmp(env, "mma") != 0 && env[0] != '\0') return -1;
+  }
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,7 +243,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.out = out;
     S.err = err;
     S.zero_rest = zero_rest;
-    cudaError_t e = gmmk::launch_scaled(S, rhs_dtype == GMM_DTYPE_E4M3, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+    const bool e4m3 = rhs_dtype == GMM_DTYPE_E4M3;
+    const int decode = e4m3 ? choose_e4m3_decode() : 1;
+    if (decode < 0) return GMM_ERR_SHAPE;
+    cudaError_t e = decode ? gmmk::launch_scaled(S, e4m3, out_dtype == GMM_DTYPE_F32, dev.sms, s)
+                           : gmmk::launch_fp8(S, out_dtype == GMM_DTYPE_F32, dev.sms, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return GMM_OK;
   }

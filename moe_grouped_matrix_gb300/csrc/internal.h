@@ -73,4 +73,8 @@ struct ScaledLaunch {
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
 
+// The same operation for e4m3 weights on the e4m3 tensor-core path (weights
+// stay e4m3; activations are split exactly into two e4m3 terms).
+cudaError_t launch_fp8(const ScaledLaunch& p, bool out_f32, int grid, cudaStream_t stream);
+
 }  // namespace gmmk

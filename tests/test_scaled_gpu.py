@@ -23,6 +23,14 @@ def library():
     oracle.build()
 
 
+@pytest.fixture(autouse=True, params=["mma", "decode"])
+def e4m3_kernel(request, monkeypatch):
+    """Every test runs on both e4m3 kernels: the e4m3 tensor-core kernel (default) and the
+    kernel that decodes the weights to bf16 (GMM_E4M3_KERNEL=decode)."""
+    monkeypatch.setenv("GMM_E4M3_KERNEL", request.param)
+    return request.param
+
+
 def _gs(sizes):
     return torch.tensor(np.asarray(sizes, np.int32), dtype=torch.int32, device=DEV)
 
@@ -128,3 +136,58 @@ def test_fp8_decode_workload_full(go):
     if go:
         offs = oracle.group_offsets(sizes, 256)
         assert (out[: offs[go]] == 0).all()
+
+
+def test_activation_split_is_exact_for_eight_bit_values():
+    # lhs: every bf16 significand (8 bits) times 2^e, e in [-2, 2]; weights: +-2^j, j in [-1, 1];
+    # two quant blocks with scales 2^{-1,0,1}.  Every product is a multiple of 2^-10 below 2^4,
+    # so each block's sum (< 2^11) and the scaled total (multiples of 2^-11 below 2^13) are exact
+    # in fp32 whatever the order: the result must equal the oracle bit for bit, i.e. the e4m3
+    # kernel's h + l / 16 split of the activations loses nothing.
+    m, k, n = 40, 256, 256
+    sizes = np.array([9, 31], np.int32)
+    g = torch.Generator().manual_seed(71)
+    mant = 1.0 + torch.randint(0, 128, (m, k), generator=g).double() / 128.0
+    ex = torch.randint(-2, 3, (m, k), generator=g).double()
+    sign = torch.where(torch.rand((m, k), generator=g) < 0.5, -1.0, 1.0).double()
+    lhs = (sign * mant * torch.pow(2.0, ex)).to(torch.bfloat16).to(DEV)
+    wj = torch.randint(-1, 2, (2, n, k), generator=g).double()
+    ws = torch.where(torch.rand((2, n, k), generator=g) < 0.5, -1.0, 1.0).double()
+    rhs = (ws * torch.pow(2.0, wj)).float().to(torch.float8_e4m3fn).to(DEV)
+    scale = torch.pow(2.0, torch.randint(-1, 2, (2, 2, 1, n), generator=g).float()).to(DEV)
+    out = G.gmm(lhs, rhs, _gs(sizes), rhs_scale=scale, out_dtype=torch.float32)
+    ref, _ = oracle_gmm(lhs, rhs, sizes, rhs_scale=scale)
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), ref)
+
+
+def test_wide_dynamic_range_activations():
+    # Within one 128-wide k step values span 2^-40 .. 2^8 (many below 2^-14 of the step's
+    # largest); whole rows scaled by 2^100 and 2^-100.
+    m, k, n = 24, 384, 256
+    sizes = np.array([24], np.int32)
+    g = torch.Generator().manual_seed(72)
+    x = torch.randn((m, k), generator=g).double() * torch.pow(2.0, torch.randint(-40, 9, (m, k), generator=g).double())
+    x[3] *= 2.0 ** 100
+    x[7] *= 2.0 ** -100
+    lhs = x.to(torch.bfloat16).to(DEV)
+    rhs = W.e4m3_normal((1, n, k), 73, DEV)
+    scale = W.uniform((1, 3, 1, n), 0.5 / 448, 2.0 / 448, 74, DEV)
+    out = G.gmm(lhs, rhs, _gs(sizes), rhs_scale=scale, out_dtype=torch.float32)
+    ref, mag = oracle_gmm(lhs, rhs, sizes, rhs_scale=scale)
+    check_close(out, ref, mag, "wide dynamic range")
+
+
+def test_zero_rows_give_the_bias_and_nan_propagates():
+    m, k, n = 20, 256, 256
+    sizes = np.array([20], np.int32)
+    lhs = W.normal((m, k), 1.0, 81, DEV)
+    lhs[4] = 0
+    lhs[9, 130] = float("nan")
+    rhs = W.e4m3_normal((1, n, k), 82, DEV)
+    bias = W.normal((1, 1, n), 1.0, 83, DEV, dtype=torch.float32)
+    out = G.gmm(lhs, rhs, _gs(sizes), rhs_bias=bias, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(out[4], bias[0, 0])
+    assert torch.isnan(out[9]).all()
+    keep = [r for r in range(m) if r != 9]
+    assert torch.isfinite(out[keep]).all()
