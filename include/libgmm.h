@@ -89,11 +89,17 @@ size_t gmm_workspace_bytes(void);
  *   group_offset first local group; 0 <= group_offset <= num_total_groups - num_local_groups.
  *   rhs_scale    NULL (s = 1, one block) or device f32 [num_local_groups, num_quant_blocks, 1, n];
  *                block b covers kk in [b*k/nb, (b+1)*k/nb); k % num_quant_blocks == 0.
- *                With rhs_scale given or an e4m3 rhs, the block-scaled kernel runs: it needs
+ *                With rhs_scale given or an e4m3 rhs, a block-scaled kernel runs: it needs
  *                transpose_rhs != 0 (else GMM_ERR_DTYPE), k % 128 == 0 and
- *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  It is built for
- *                decode-sized groups (a few rows each): it streams every weight tile once per
- *                16 rows of its group.
+ *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  These are built for
+ *                decode-sized groups (a few rows each) and stream every weight tile once per
+ *                chunk of rows of its group (32 rows for e4m3 weights, 16 for bf16).
+ *                e4m3 weights stay e4m3 on the e4m3 tensor cores; each lhs row is split per
+ *                256-wide k step into two e4m3 terms times a power of two, exactly for every
+ *                value within 2^14 of the step's largest magnitude (smaller ones are off by at
+ *                most 2^-21 of it), and a NaN or infinity in a row makes that output row NaN.
+ *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
+ *                value than auto, mma or decode: GMM_ERR_SHAPE).
  *                Without scale, bf16 weights run on one of four kernels chosen from the average
  *                group size m / num_total_groups: SM-pair 256x256 row tiles (>= 1024 rows),
  *                SM-pair tiles of 256 weight rows x up to 256 group rows rounded to 32 (>= 16),
