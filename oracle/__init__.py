@@ -10,7 +10,10 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 the CUDA library never imports it.
 
 Inputs are numpy arrays holding the stored bits of each dtype:
-``uint16`` for bf16, ``float32``/``uint32`` for f32, ``uint8`` for e4m3fn.
+``uint16`` for bf16, ``float32``/``uint32`` for f32, ``uint8`` for e4m3fn (the
+default for ``uint8``), e5m2 and the 4-bit formats, ``int8`` for int8.  int4,
+uint4 and e2m1 are packed two values per byte, the even-indexed value in the low
+nibble, so a row of k values is k / 2 bytes; pass their dtype code explicitly.
 Outputs are fp64 ``ref`` (the exact-product, fp64-sum result) and ``mag``
 (the same sum over absolute values, in which the tolerance is stated).
 """
@@ -24,7 +27,8 @@ import threading
 
 import numpy as np
 
-BF16, F32, E4M3 = 0, 1, 2
+BF16, F32, E4M3, E5M2, INT8, INT4, UINT4, E2M1 = 0, 1, 2, 3, 4, 5, 6, 7
+PACKED = (INT4, UINT4, E2M1)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
@@ -81,6 +85,8 @@ def _dtype_code(a: np.ndarray, declared: int | None) -> int:
         return F32
     if a.dtype == np.uint8:
         return E4M3
+    if a.dtype == np.int8:
+        return INT8
     raise TypeError(f"unsupported stored dtype {a.dtype}")
 
 
@@ -103,14 +109,15 @@ def gmm(lhs, rhs, group_sizes, *, transpose_rhs=True, group_offset=0, rhs_scale=
     scale = None if rhs_scale is None else np.ascontiguousarray(rhs_scale, dtype=np.float32)
     m, k = lhs.shape
     L = rhs.shape[0]
-    n = rhs.shape[1] if transpose_rhs else rhs.shape[2]
+    rcode = _dtype_code(rhs, rhs_dtype)
+    n = rhs.shape[1] if transpose_rhs else rhs.shape[2] * (2 if rcode in PACKED else 1)
     nb = 0 if scale is None else scale.shape[1]
     rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     count = m if rows_arr is None else rows_arr.shape[0]
     ref = np.zeros((count, n), dtype=np.float64)
     mag = np.zeros((count, n), dtype=np.float64)
     rc = _load().oracle_gmm(
-        _ptr(lhs), _dtype_code(lhs, lhs_dtype), m, k, _ptr(rhs), _dtype_code(rhs, rhs_dtype), L, n,
+        _ptr(lhs), _dtype_code(lhs, lhs_dtype), m, k, _ptr(rhs), rcode, L, n,
         int(bool(transpose_rhs)), _ptr(gs), gs.shape[0], int(group_offset), _ptr(scale), nb,
         _ptr(bias), 0 if bias is None else _dtype_code(bias, bias_dtype), _ptr(rows_arr), count,
         _ptr(ref), _ptr(mag), int(threads))
@@ -138,9 +145,13 @@ def tgmm(lhs, dout, group_sizes, *, k_rows=None, lhs_dtype=None, dout_dtype=None
 
 
 def decode(stored: np.ndarray, dtype: int | None = None) -> np.ndarray:
-    """Decodes stored bf16 / f32 / e4m3fn bits to fp64 by the format definitions."""
+    """Decodes stored values to fp64 by the format definitions.  For the packed 4-bit
+    formats the last axis doubles (two values per byte, low nibble first)."""
     a = np.ascontiguousarray(stored)
-    out = np.zeros(a.size, dtype=np.float64)
-    if _load().oracle_decode(_ptr(a), _dtype_code(a, dtype), a.size, _ptr(out)) != 0:
+    code = _dtype_code(a, dtype)
+    count = a.size * (2 if code in PACKED else 1)
+    out = np.zeros(count, dtype=np.float64)
+    if _load().oracle_decode(_ptr(a), code, count, _ptr(out)) != 0:
         raise ValueError("bad dtype")
-    return out.reshape(a.shape)
+    shape = a.shape[:-1] + (a.shape[-1] * 2,) if code in PACKED else a.shape
+    return out.reshape(shape)

@@ -7,7 +7,9 @@
 // library.
 //
 // Sources (page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230",
-// files tpu_inference/kernels/megablox/gmm.py and common.py):
+// files tpu_inference/kernels/megablox/gmm.py and common.py; common.py's
+// assert_is_supported_dtype lists the operand formats bf16, f32, e4m3fn, e5m2,
+// int8, int4, e2m1fn and uint4):
 //   * gmm docstring: row block of group i of lhs [m,k] times the group's rhs;
 //     rhs is [num_groups, n, k] and the contraction is over the last dim of both
 //     operands (the dot_general in the kernel body contracts dim 1 with dim 1).
@@ -33,7 +35,9 @@
 // tolerance |gpu - ref| <= 1e-3 * mag + 2^-8 * |ref| is stated in.
 //
 // Pins: tests/test_oracle_pins.py checks this file against hand-worked values,
-// brute-force dense per-group products, the format definition of e4m3fn, and
+// brute-force dense per-group products, the format definitions of e4m3fn,
+// e5m2, int8, int4, uint4 and e2m1 (and PyTorch's own conversions where it
+// has them), and
 // the invariants of the method (zero tail rows, empty groups, NT == NN on the
 // transposed weight, tgmm == per-group lhs_g^T dout_g, group_offset slicing).
 
@@ -47,7 +51,10 @@
 
 namespace {
 
-enum { DT_BF16 = 0, DT_F32 = 1, DT_E4M3 = 2 };
+// Stored formats.  The 4-bit ones hold two values per byte, the even-indexed
+// value in the low nibble; element i of such an array is nibble i % 2 of byte
+// i / 2.
+enum { DT_BF16 = 0, DT_F32 = 1, DT_E4M3 = 2, DT_E5M2 = 3, DT_INT8 = 4, DT_INT4 = 5, DT_UINT4 = 6, DT_E2M1 = 7 };
 
 // bfloat16: the top 16 bits of an IEEE binary32.
 double decode_bf16(uint16_t bits) {
@@ -75,16 +82,54 @@ double decode_e4m3fn(uint8_t code) {
   return s ? -mag : mag;
 }
 
+// float8_e5m2 (in common.py's list): 1 sign bit, 5 exponent bits with bias 15,
+// 2 mantissa bits, IEEE-style: exponent 31 is infinity (mantissa 0) or NaN;
+// exponent 0 encodes subnormals m/4 * 2^-14.
+double decode_e5m2(uint8_t code) {
+  const int s = code >> 7;
+  const int e = (code >> 2) & 0x1F;
+  const int m = code & 0x3;
+  double mag;
+  if (e == 31)
+    mag = m == 0 ? HUGE_VAL : std::nan("");
+  else
+    mag = (e == 0) ? std::ldexp(m / 4.0, -14) : std::ldexp(1.0 + m / 4.0, e - 15);
+  return s ? -mag : mag;
+}
+
+// float4_e2m1fn (in common.py's list): 1 sign bit, 2 exponent bits with bias 1,
+// 1 mantissa bit, no infinities or NaN; exponent 0 encodes the subnormal m/2.
+double decode_e2m1(uint8_t nibble) {
+  const int s = (nibble >> 3) & 1;
+  const int e = (nibble >> 1) & 0x3;
+  const int m = nibble & 1;
+  const double mag = (e == 0) ? m / 2.0 : std::ldexp(1.0 + m / 2.0, e - 1);
+  return s ? -mag : mag;
+}
+
+// int4: two's complement in 4 bits (-8 .. 7); uint4: 0 .. 15.
+double decode_int4(uint8_t nibble) { return nibble >= 8 ? double(int(nibble) - 16) : double(nibble); }
+
+uint8_t nibble_at(const void* base, int64_t idx) {
+  const uint8_t byte = static_cast<const uint8_t*>(base)[idx / 2];
+  return (idx % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+}
+
 double load(const void* base, int dtype, int64_t idx) {
   switch (dtype) {
     case DT_BF16: return decode_bf16(static_cast<const uint16_t*>(base)[idx]);
     case DT_F32: return decode_f32(static_cast<const uint32_t*>(base)[idx]);
     case DT_E4M3: return decode_e4m3fn(static_cast<const uint8_t*>(base)[idx]);
+    case DT_E5M2: return decode_e5m2(static_cast<const uint8_t*>(base)[idx]);
+    case DT_INT8: return double(static_cast<const int8_t*>(base)[idx]);
+    case DT_INT4: return decode_int4(nibble_at(base, idx));
+    case DT_UINT4: return double(nibble_at(base, idx));
+    case DT_E2M1: return decode_e2m1(nibble_at(base, idx));
   }
   return std::nan("");
 }
 
-bool valid_dtype(int d) { return d == DT_BF16 || d == DT_F32 || d == DT_E4M3; }
+bool valid_dtype(int d) { return d >= DT_BF16 && d <= DT_E2M1; }
 
 int resolve_threads(int threads) {
   if (threads > 0) return threads;

@@ -87,6 +87,55 @@ def test_e4m3fn_all_codes_match_format_definition_and_torch():
     assert got[0x00] == 0.0 and np.signbit(got[0x80])
 
 
+def test_e5m2_all_codes_match_format_definition_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode(codes, oracle.E5M2)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+    nan = np.isnan(got)
+    assert set(np.flatnonzero(nan)) == {0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF}
+    np.testing.assert_array_equal(got[~nan], lib[~nan])
+    assert np.isnan(lib[nan]).all()
+    # bias 15, 2 mantissa bits, IEEE infinities, subnormals at 2^-14 * m/4
+    assert got[0x3C] == 1.0 and got[0x40] == 2.0 and got[0xBC] == -1.0
+    assert got[0x7C] == np.inf and got[0xFC] == -np.inf
+    assert got[0x7B] == 57344.0 and got[0x01] == 2.0 ** -16 and got[0x04] == 2.0 ** -14
+
+
+def test_int8_all_codes():
+    codes = np.arange(-128, 128, dtype=np.int64).astype(np.int8)
+    np.testing.assert_array_equal(oracle.decode(codes), np.arange(-128, 128, dtype=np.float64))
+
+
+# e2m1 (OCP microscaling formats): sign, 2 exponent bits with bias 1, 1 mantissa bit.
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_4bit_formats_values_and_nibble_order():
+    # byte 0x7A holds element 0 = 0xA (low nibble) and element 1 = 0x7
+    b = np.array([0x7A], np.uint8)
+    np.testing.assert_array_equal(oracle.decode(b, oracle.INT4), [-6.0, 7.0])
+    np.testing.assert_array_equal(oracle.decode(b, oracle.UINT4), [10.0, 7.0])
+    np.testing.assert_array_equal(oracle.decode(b, oracle.E2M1), [-1.0, 6.0])
+    # all 16 nibbles in both positions
+    lo = np.arange(16, dtype=np.uint8)
+    both = (lo | (lo[::-1] << 4)).astype(np.uint8)
+    for code, table in ((oracle.INT4, [v if v < 8 else v - 16 for v in range(16)]),
+                        (oracle.UINT4, list(range(16))), (oracle.E2M1, E2M1_TABLE)):
+        got = oracle.decode(both, code).reshape(16, 2)
+        np.testing.assert_array_equal(got[:, 0], np.asarray(table, np.float64))
+        np.testing.assert_array_equal(got[:, 1], np.asarray(table, np.float64)[::-1])
+    assert np.signbit(oracle.decode(np.array([0x08], np.uint8), oracle.E2M1)[0])
+
+
+def unpack_nibbles(packed: np.ndarray, table) -> np.ndarray:
+    """[..., k/2] bytes -> [..., k] values, low nibble first (independent of the oracle)."""
+    t = np.asarray(table, np.float64)
+    out = np.empty(packed.shape[:-1] + (packed.shape[-1] * 2,), np.float64)
+    out[..., 0::2] = t[packed & 0xF]
+    out[..., 1::2] = t[packed >> 4]
+    return out
+
+
 def test_bf16_all_codes_match_torch():
     codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     got = oracle.decode(codes)
@@ -193,6 +242,36 @@ def test_e4m3_weights_with_scale_against_brute_force():
     ref, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_scale=scale)
     exp = brute_force_gmm(bf16_values(lhs), w_v, sizes, True, scale=scale.astype(np.float64))
     np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "int8", "int4", "uint4", "e2m1"])
+def test_other_weight_formats_against_brute_force(fmt):
+    # NT weights [G, n, k] in each stored format, with quant-block scales and bias.
+    rng = np.random.default_rng(12)
+    m, k, n, G, nb = 20, 64, 8, 3, 2
+    sizes = [6, 0, 11]
+    lhs = rand_bf16(rng, (m, k))
+    if fmt == "e5m2":
+        x = torch.from_numpy(np.clip(rng.standard_normal((G, n, k)) * 300, -57344, 57344).astype(np.float32))
+        w = x.to(torch.float8_e5m2).view(torch.uint8).numpy()
+        w_v = torch.from_numpy(w.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+        code = oracle.E5M2
+    elif fmt == "int8":
+        w = rng.integers(-128, 128, (G, n, k)).astype(np.int8)
+        w_v = w.astype(np.float64)
+        code = oracle.INT8
+    else:
+        w = rng.integers(0, 256, (G, n, k // 2)).astype(np.uint8)
+        table = {"int4": [v if v < 8 else v - 16 for v in range(16)], "uint4": list(range(16)),
+                 "e2m1": E2M1_TABLE}[fmt]
+        w_v = unpack_nibbles(w, table)
+        code = {"int4": oracle.INT4, "uint4": oracle.UINT4, "e2m1": oracle.E2M1}[fmt]
+    scale = rng.uniform(0.5, 2, (G, nb, 1, n)).astype(np.float32) / 64
+    bias = rand_bf16(rng, (G, 1, n))
+    ref, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_scale=scale, rhs_bias=bias, rhs_dtype=code)
+    exp = brute_force_gmm(bf16_values(lhs), w_v, sizes, True, scale=scale.astype(np.float64),
+                          bias_v=bf16_values(bias))
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-12)
 
 
 # ------------------------------------------------------------------ invariants
