@@ -42,7 +42,13 @@ extern "C" {
 enum {
   GMM_DTYPE_BF16 = 0, /* bfloat16 */
   GMM_DTYPE_F32 = 1,  /* IEEE binary32 */
-  GMM_DTYPE_E4M3 = 2  /* float8_e4m3fn: bias 7, no infinities, 0x7F/0xFF NaN */
+  GMM_DTYPE_E4M3 = 2, /* float8_e4m3fn: bias 7, no infinities, 0x7F/0xFF NaN */
+  GMM_DTYPE_E5M2 = 3, /* float8_e5m2: bias 15, IEEE infinities and NaN */
+  GMM_DTYPE_INT8 = 4, /* two's complement int8 */
+  /* 4-bit formats: two values per byte, the even-indexed value in the low nibble */
+  GMM_DTYPE_INT4 = 5,  /* two's complement, -8 .. 7 */
+  GMM_DTYPE_UINT4 = 6, /* 0 .. 15 */
+  GMM_DTYPE_E2M1 = 7   /* float4_e2m1fn: values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives */
 };
 
 /* Status codes returned by every entry point. */
@@ -84,20 +90,24 @@ size_t gmm_workspace_bytes(void);
  *   lhs          [m, k], lhs_dtype must be GMM_DTYPE_BF16.
  *   rhs          transpose_rhs != 0: [num_local_groups, n, k] (the pages' layout,
  *                W(g, c, kk) = rhs[g, c, kk]); transpose_rhs == 0: [num_local_groups, k, n].
- *                rhs_dtype GMM_DTYPE_BF16, or GMM_DTYPE_E4M3 (transpose_rhs != 0 only).
+ *                rhs_dtype GMM_DTYPE_BF16, or (transpose_rhs != 0 only) one of the weight
+ *                formats of common.py's supported list: E4M3, E5M2, INT8, INT4, UINT4, E2M1;
+ *                a row of the 4-bit formats is k / 2 bytes.
  *   group_sizes  device int32 [num_total_groups], 1 <= num_total_groups <= GMM_MAX_GROUPS.
  *   group_offset first local group; 0 <= group_offset <= num_total_groups - num_local_groups.
  *   rhs_scale    NULL (s = 1, one block) or device f32 [num_local_groups, num_quant_blocks, 1, n];
  *                block b covers kk in [b*k/nb, (b+1)*k/nb); k % num_quant_blocks == 0.
- *                With rhs_scale given or an e4m3 rhs, a block-scaled kernel runs: it needs
+ *                With rhs_scale given or a non-bf16 rhs, a block-scaled kernel runs: it needs
  *                transpose_rhs != 0 (else GMM_ERR_DTYPE), k % 128 == 0 and
  *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  These are built for
  *                decode-sized groups (a few rows each) and stream every weight tile once per
  *                chunk of rows of its group (32 rows for e4m3 weights, 16 for bf16).
- *                e4m3 weights stay e4m3 on the e4m3 tensor cores; each lhs row is split per
- *                256-wide k step into two e4m3 terms times a power of two, exactly for every
- *                value within 2^14 of the step's largest magnitude (smaller ones are off by at
- *                most 2^-21 of it), and a NaN or infinity in a row makes that output row NaN.
+ *                8- and 4-bit weights run on the fp8 tensor cores: e4m3 and e5m2 as stored,
+ *                the others rewritten exactly as e4m3 (int8 as 16 * high nibble + low nibble,
+ *                two e4m3 terms).  Each lhs row is split per k step (256 wide; 128 for int8)
+ *                into two e4m3 terms times a power of two, exactly for every value within
+ *                2^14 of the step's largest magnitude (smaller ones are off by at most 2^-21
+ *                of it); a NaN or infinity in a row makes that output row NaN.
  *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
  *                value than auto, mma or decode: GMM_ERR_SHAPE).
  *                Without scale, bf16 weights run on one of four kernels chosen from the average

@@ -22,15 +22,18 @@ import threading
 
 import torch
 
-__all__ = ["gmm", "tgmm", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
+__all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
            "DEVERR_NEGATIVE_GROUP_SIZE", "DEVERR_GROUP_SIZES_EXCEED_M", "DEVERR_TIMEOUT"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
 
-DTYPE_BF16, DTYPE_F32, DTYPE_E4M3 = 0, 1, 2
+DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1 = range(8)
+# Packed 4-bit weight formats (uint8 tensors [L, n, k / 2], even k in the low nibble), by name.
+PACKED_FORMATS = {"int4": DTYPE_INT4, "uint4": DTYPE_UINT4, "e2m1": DTYPE_E2M1}
 DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
-_TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3}
+_TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3,
+                  torch.float8_e5m2: DTYPE_E5M2, torch.int8: DTYPE_INT8}
 
 _lock = threading.Lock()
 _lib = None
@@ -111,14 +114,20 @@ def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out, out_dtype,
-              workspace, stream):
+              workspace, stream, rhs_format):
     lib = load_library()
     _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
     if group_sizes.dtype != torch.int32:
         raise TypeError("group_sizes must be int32")
+    if rhs_format is None:
+        rcode = _code(rhs)
+    else:
+        if rhs_format not in PACKED_FORMATS or rhs.dtype != torch.uint8:
+            raise TypeError("rhs_format names a packed 4-bit format (int4, uint4, e2m1) of a uint8 tensor")
+        rcode = PACKED_FORMATS[rhs_format]
     m, k = lhs.shape
     n = rhs.shape[1] if transpose_rhs else rhs.shape[2]
-    kr = rhs.shape[2] if transpose_rhs else rhs.shape[1]
+    kr = (rhs.shape[2] if transpose_rhs else rhs.shape[1]) * (2 if rhs_format is not None else 1)
     if kr != k:
         raise ValueError(f"lhs has k={k} but rhs has k={kr}")
     if out is None:
@@ -134,7 +143,7 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
     if rhs_bias is not None:
         _dev(rhs_bias, "rhs_bias")
     rc = getattr(lib, fn)(
-        lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n, int(bool(transpose_rhs)),
+        lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), rcode, rhs.shape[0], n, int(bool(transpose_rhs)),
         group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
         None if rhs_scale is None else rhs_scale.data_ptr(), nb,
         None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
@@ -145,21 +154,23 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
 
 
 def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
-        out_dtype=torch.bfloat16, workspace=None, stream=None):
+        out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None):
     """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
-    for each row r of local group g; all other rows of out are zero."""
+    for each row r of local group g; all other rows of out are zero.  rhs is bf16, float8_e4m3fn,
+    float8_e5m2 or int8, or a uint8 tensor [G_local, n, k / 2] of packed 4-bit weights with
+    rhs_format = "int4", "uint4" or "e2m1"."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out_dtype, workspace, stream)
+                     out_dtype, workspace, stream, rhs_format)
 
 
 def gmm_into(lhs, rhs, group_sizes, out, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0,
-             workspace=None, stream=None):
+             workspace=None, stream=None, rhs_format=None):
     """As gmm, but only the local groups' rows of `out` are written; every other row keeps the
     caller's contents (the existing-output mode)."""
     if out is None:
         raise ValueError("gmm_into needs an output tensor")
     return _gmm_call("gmm_into", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out.dtype, workspace, stream)
+                     out.dtype, workspace, stream, rhs_format)
 
 
 def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, out=None, out_dtype=torch.float32,

@@ -180,17 +180,19 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              size_t workspace_bytes, void* stream, int32_t zero_rest) {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
-  if (rhs_dtype != GMM_DTYPE_BF16 && rhs_dtype != GMM_DTYPE_E4M3) return GMM_ERR_DTYPE;
+  if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (rhs_bias != nullptr && bias_dtype != GMM_DTYPE_BF16 && bias_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
-  if (rhs_dtype == GMM_DTYPE_E4M3 && !transpose_rhs) return GMM_ERR_DTYPE;
+  const bool quantized = rhs_dtype != GMM_DTYPE_BF16;
+  const bool packed4 = rhs_dtype == GMM_DTYPE_INT4 || rhs_dtype == GMM_DTYPE_UINT4 || rhs_dtype == GMM_DTYPE_E2M1;
+  if (quantized && !transpose_rhs) return GMM_ERR_DTYPE;
   if (!fits_i32(m) || !fits_i32(k) || !fits_i32(n) || k < 8 || n < 8 || k % 8 != 0 || n % 8 != 0)
     return GMM_ERR_SHAPE;
   if (num_total_groups < 1 || num_total_groups > GMM_MAX_GROUPS || num_local_groups < 1 ||
       num_local_groups > num_total_groups)
     return GMM_ERR_SHAPE;
   if (group_offset < 0 || group_offset > num_total_groups - num_local_groups) return GMM_ERR_GROUP_OFFSET;
-  const bool scaled_path = rhs_dtype == GMM_DTYPE_E4M3 || rhs_scale != nullptr;
+  const bool scaled_path = quantized || rhs_scale != nullptr;
   if (rhs_scale != nullptr) {
     if (num_quant_blocks < 1 || k % num_quant_blocks != 0) return GMM_ERR_SHAPE;
   }
@@ -222,11 +224,12 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
         return st;
     }
     {
-      const bool e4m3 = rhs_dtype == GMM_DTYPE_E4M3;
-      const uint64_t dims[3] = {uint64_t(k), uint64_t(n), uint64_t(num_local_groups)};
-      const uint32_t box[3] = {e4m3 ? 128u : 64u, 128u, 1u};
-      if (int st = make_map(&S.tm_rhs, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                            e4m3 ? 1 : 2, 3, rhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      // Weight rows as bytes: k of an 8-bit format, k / 2 of a 4-bit one; bf16 as elements.
+      const uint64_t row = packed4 ? uint64_t(k / 2) : uint64_t(k);
+      const uint64_t dims[3] = {row, uint64_t(n), uint64_t(num_local_groups)};
+      const uint32_t box[3] = {quantized ? 128u : 64u, 128u, 1u};
+      if (int st = make_map(&S.tm_rhs, quantized ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            quantized ? 1 : 2, 3, rhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return st;
     }
     S.group_sizes = group_sizes;
@@ -243,11 +246,22 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.out = out;
     S.err = err;
     S.zero_rest = zero_rest;
-    const bool e4m3 = rhs_dtype == GMM_DTYPE_E4M3;
-    const int decode = e4m3 ? choose_e4m3_decode() : 1;
-    if (decode < 0) return GMM_ERR_SHAPE;
-    cudaError_t e = decode ? gmmk::launch_scaled(S, e4m3, out_dtype == GMM_DTYPE_F32, dev.sms, s)
-                           : gmmk::launch_fp8(S, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+    const bool f32 = out_dtype == GMM_DTYPE_F32;
+    cudaError_t e;
+    if (rhs_dtype == GMM_DTYPE_BF16) {
+      e = gmmk::launch_scaled(S, false, f32, dev.sms, s);
+    } else if (rhs_dtype == GMM_DTYPE_E4M3) {
+      const int decode = choose_e4m3_decode();
+      if (decode < 0) return GMM_ERR_SHAPE;
+      e = decode ? gmmk::launch_scaled(S, true, f32, dev.sms, s) : gmmk::launch_fp8(S, gmmk::kWeightE4M3, f32, dev.sms, s);
+    } else {
+      const int fmt = rhs_dtype == GMM_DTYPE_E5M2   ? gmmk::kWeightE5M2
+                      : rhs_dtype == GMM_DTYPE_INT8  ? gmmk::kWeightInt8
+                      : rhs_dtype == GMM_DTYPE_INT4  ? gmmk::kWeightInt4
+                      : rhs_dtype == GMM_DTYPE_UINT4 ? gmmk::kWeightUint4
+                                                     : gmmk::kWeightE2M1;
+      e = gmmk::launch_fp8(S, fmt, f32, dev.sms, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return GMM_OK;
   }

@@ -73,8 +73,20 @@ struct ScaledLaunch {
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
 
-// The same operation for e4m3 weights on the e4m3 tensor-core path (weights
-// stay e4m3; activations are split exactly into two e4m3 terms).
-cudaError_t launch_fp8(const ScaledLaunch& p, bool out_f32, int grid, cudaStream_t stream);
+// The same operation for 8- and 4-bit weights on the fp8 tensor cores (the
+// bf16 activations are split exactly into two e4m3 terms; e4m3 / e5m2 weights
+// are used as stored, the other formats rewritten exactly as e4m3 tiles).
+// tm_rhs for the 4-bit formats spans [L, n, k / 2] bytes with box {128, 128, 1}.
+enum WeightFormat : int {
+  kWeightE4M3 = 0,
+  kWeightE5M2 = 1,
+  kWeightInt8 = 2,
+  kWeightInt4 = 3,
+  kWeightUint4 = 4,
+  kWeightE2M1 = 5,
+};
+cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
+cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
+                                 cudaStream_t stream);
 
 }  // namespace gmmk

@@ -148,14 +148,40 @@ def moe128(device="cpu", seed: int = 2, which=("lhs", "wi", "wo", "lhs_wo", "dou
     return d
 
 
-def fp8_decode(device="cpu", seed: int = 4):
+# Largest magnitude of each weight format (the quant scales below are U(0.5, 2) / this).
+FORMAT_MAX = {"e4m3": 448.0, "e5m2": 448.0, "int8": 127.0, "int4": 8.0, "uint4": 15.0, "e2m1": 6.0}
+PACKED = ("int4", "uint4", "e2m1")
+
+
+def weights(fmt: str, shape, seed: int, device="cpu") -> torch.Tensor:
+    """Weights [G, n, k] in a stored format: e4m3 / e5m2 from N(0,1) (e4m3 clipped to
+    +-448), int8 uniform over all 256 codes, the 4-bit formats as uniform random bytes
+    (every code equally likely), packed [G, n, k / 2] with the even k in the low nibble."""
+    if fmt == "e4m3":
+        return e4m3_normal(shape, seed, device)
+    if fmt == "e5m2":
+        x = torch.randn(*shape, generator=_gen(seed, device), device=device, dtype=torch.float32)
+        return x.to(torch.float8_e5m2)
+    if fmt == "int8":
+        return torch.randint(-128, 128, shape, generator=_gen(seed, device), device=device).to(torch.int8)
+    if fmt in PACKED:
+        packed = tuple(shape[:-1]) + (shape[-1] // 2,)
+        return torch.randint(0, 256, packed, generator=_gen(seed, device), device=device).to(torch.uint8)
+    raise ValueError(fmt)
+
+
+def fp8_decode(device="cpu", seed: int = 4, fmt: str = "e4m3"):
+    """The decode workload; `fmt` other than e4m3 swaps in weights of that format (same
+    shapes, scales U(0.5, 2) / the format's largest magnitude)."""
     gs = group_sizes_uniform_topk(seed, 64, 64, 4)
+    top = FORMAT_MAX[fmt]
     return dict(
         lhs=normal((256, 4096), 1.0, seed + 1, device),
-        rhs=e4m3_normal((64, 2048, 4096), seed + 2, device),
-        rhs_scale=uniform((64, 32, 1, 2048), 0.5 / 448.0, 2.0 / 448.0, seed + 3, device),
+        rhs=weights(fmt, (64, 2048, 4096), seed + 2, device),
+        rhs_scale=uniform((64, 32, 1, 2048), 0.5 / top, 2.0 / top, seed + 3, device),
         rhs_bias=normal((64, 1, 2048), 1.0, seed + 4, device),
-        group_sizes=gs, transpose_rhs=True, out_dtype=torch.bfloat16)
+        group_sizes=gs, transpose_rhs=True, out_dtype=torch.bfloat16,
+        rhs_format=fmt if fmt in PACKED else None)
 
 
 def sample_rows(seed: int, offsets: np.ndarray, per_group: int) -> np.ndarray:
@@ -178,8 +204,8 @@ def stored_bits(t: torch.Tensor) -> np.ndarray:
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.uint16).numpy()
-    if t.dtype == torch.float8_e4m3fn:
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
         return t.view(torch.uint8).numpy()
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.int8, torch.uint8):
         return t.numpy()
     raise TypeError(t.dtype)

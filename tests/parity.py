@@ -32,11 +32,19 @@ def check_close(gpu: torch.Tensor, ref: np.ndarray, mag: np.ndarray, what: str):
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside the bound; {details}")
 
 
+# Stored-format names of the weights -> the oracle's dtype codes (None: from the array's dtype).
+ORACLE_FORMAT = {None: None, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8, "int4": oracle.INT4,
+                 "uint4": oracle.UINT4, "e2m1": oracle.E2M1}
+
+
 def oracle_gmm(lhs, rhs, group_sizes_np, *, transpose_rhs=True, group_offset=0, rhs_scale=None, rhs_bias=None,
-               rows=None):
+               rows=None, rhs_format=None):
+    if rhs_format is None and rhs.dtype == torch.float8_e5m2:
+        rhs_format = "e5m2"
     return oracle.gmm(bits(lhs), bits(rhs), group_sizes_np, transpose_rhs=transpose_rhs, group_offset=group_offset,
                       rhs_scale=None if rhs_scale is None else bits(rhs_scale),
-                      rhs_bias=None if rhs_bias is None else bits(rhs_bias), rows=rows)
+                      rhs_bias=None if rhs_bias is None else bits(rhs_bias), rows=rows,
+                      rhs_dtype=ORACLE_FORMAT[rhs_format])
 
 
 def oracle_tgmm(lhs, dout, group_sizes_np, k_rows=None):

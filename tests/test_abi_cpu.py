@@ -63,7 +63,8 @@ def call_gmm(lib, fn="gmm", **over):
     (dict(bias=FAKE, bias_dtype=2), 2),
     (dict(k=100), 3), (dict(n=12), 3), (dict(m=-1), 3), (dict(L=5), 3), (dict(G=0), 3), (dict(G=2000, L=4), 3),
     (dict(scale=FAKE, nb=3), 3), (dict(scale=FAKE, nb=2, k=128), 3), (dict(rhs_dtype=2, k=200), 3),
-    (dict(scale=FAKE, nb=1, trhs=0), 2),
+    (dict(scale=FAKE, nb=1, trhs=0), 2), (dict(rhs_dtype=8), 2), (dict(rhs_dtype=5, trhs=0), 2),
+    (dict(rhs_dtype=4, trhs=0), 2), (dict(rhs_dtype=7, k=200), 3), (dict(rhs_dtype=3, k=192, scale=FAKE, nb=2), 3),
     (dict(G=8, L=4, go=5), 5), (dict(G=8, L=4, go=-1), 5),
     (dict(lhs=ctypes.c_void_p((1 << 20) + 8)), 4), (dict(out=ctypes.c_void_p((1 << 20) + 4)), 4),
     (dict(ws=None), 6), (dict(ws_bytes=8), 6),
