@@ -111,7 +111,7 @@ struct Cfg {
   static constexpr uint32_t OFF_RAWFULL = OFF_CTRL;
   static constexpr uint32_t OFF_RAWEMPTY = OFF_RAWFULL + 8 * RAWST;
   static constexpr uint32_t OFF_CONVFULL = OFF_RAWEMPTY + 8 * RAWST;
-  static constexpr uint32_t OFF_DONEB = OFF_CONVFULL + 8 * 2;
+  static constexpr uint32_t OFF_DONEB = OFF_CONVFULL + 8 * (CST > 0 ? CST : 1);
   static constexpr uint32_t OFF_RFULL = OFF_DONEB + 8 * NDONE;
   static constexpr uint32_t OFF_REMPTY = OFF_RFULL + 8 * RTS;
   static constexpr uint32_t OFF_BFULL = OFF_REMPTY + 8 * RTS;
@@ -181,70 +181,59 @@ __device__ __forceinline__ void split_e4m3(const float (&y)[N], uint32_t (&hw)[N
 }
 
 // ------------------------------------------------------------------ weight rewrite
-// Two f16 values (an f16x2 word, low half first) -> two e4m3fn bytes, low first.
-// Only exact conversions are asked of it (every value below is an e4m3 value).
-__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+// 4-bit codes become e4m3 bytes through 16-entry byte tables held in four words
+// (entries 0..7 in t0/t1, 8..15 in t2/t3, little-endian, bit 7 clear) and
+// prmt.  In prmt's default mode a selector nibble with bit 3 set replicates the
+// sign bit of the byte it selects, so prmt(0x80808080, 0x80808080, codes) gives
+// 0x80 for codes 0..7 and 0xFF for codes 8..15: the mask that picks the upper
+// half of the table, and (shifted left by one) the sign bit of negative values.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
 
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+// Four 4-bit codes (bits 0..15 of `codes`, k order) -> four e4m3 bytes (k order).
+template <uint32_t T0, uint32_t T1, uint32_t T2, uint32_t T3, bool kSigned>
+__device__ __forceinline__ uint32_t lut4(uint32_t codes) {
+  const uint32_t idx = codes & 0x7777u;
+  const uint32_t upper = prmt(0x80808080u, 0x80808080u, codes);
+  uint32_t r = prmt(T0, T1, idx);
+  if constexpr (T0 != T2 || T1 != T3) r = (prmt(T2, T3, idx) & upper) | (r & ~upper);
+  if constexpr (kSigned) r |= (upper << 1) & 0x80808080u;
   return r;
 }
 
-// p holds two 4-bit codes at bits 0..3 and 16..19 (zero elsewhere); returns
-// their values as an f16x2 word, exactly.
-//   uint4: 1024 + u is the f16 0x6400 | u, less 1024.
-//   int4:  the code's value is (u ^ 8) - 8: 0x6400 | (u ^ 8), less 1032.
-//   e2m1:  the 3 magnitude bits go to f16 bits 9..11 (exponent field's two low
-//          bits and the top mantissa bit) under the sign: 2^-14 times the
-//          code's value, subnormal code included; then times 2^14.
+// e4m3 bytes of 0..15 (the unsigned table, also the low half of int4's).
+constexpr uint32_t kU0 = 0x44403800u, kU1 = 0x4E4C4A48u, kU2 = 0x53525150u, kU3 = 0x57565554u;
+// int4 codes 8..15 are -8..-1: magnitudes 8, 7, ..., 1 (the sign comes from the mask).
+constexpr uint32_t kI2 = 0x4A4C4E50u, kI3 = 0x38404448u;
+// e2m1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (sign-magnitude codes).
+constexpr uint32_t kF0 = 0x3C383000u, kF1 = 0x4C484440u;
+// 16 times the int4 value: magnitudes 0, 16, ..., 112 and 128, 112, ..., 16.
+constexpr uint32_t kH0 = 0x64605800u, kH1 = 0x6E6C6A68u, kH2 = 0x6A6C6E70u, kH3 = 0x58606468u;
+
 template <WFmt F>
-__device__ __forceinline__ uint32_t nibbles_to_f16x2(uint32_t p) {
-  if constexpr (F == WFmt::kUint4) {
-    return f16x2_sub(p | 0x64006400u, 0x64006400u);
-  } else if constexpr (F == WFmt::kInt4) {
-    return f16x2_sub((p ^ 0x00080008u) | 0x64006400u, 0x64086408u);
-  } else {
-    static_assert(F == WFmt::kE2M1, "4-bit format");
-    return f16x2_mul(((p & 0x00070007u) << 9) | ((p & 0x00080008u) << 12), 0x74007400u);
-  }
+__device__ __forceinline__ uint32_t nibble4_to_e4m3(uint32_t codes) {
+  if constexpr (F == WFmt::kUint4) return lut4<kU0, kU1, kU2, kU3, false>(codes);
+  else if constexpr (F == WFmt::kInt4) return lut4<kU0, kU1, kI2, kI3, true>(codes);
+  else return lut4<kF0, kF1, kF0, kF1, true>(codes);
 }
 
 // 8 packed 4-bit codes (one word, k order from the low nibble) -> 8 e4m3 bytes.
-// Even and odd codes are converted in pairs (n0, n2), (n1, n3), ... and the
-// results interleaved back into k order.
 template <WFmt F>
 __device__ __forceinline__ void nibble8_to_e4m3(uint32_t w, uint32_t& o0, uint32_t& o1) {
-  const uint32_t ev = w & 0x0F0F0F0Fu;         // bytes: n0 n2 n4 n6
-  const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;  // bytes: n1 n3 n5 n7
-  const uint32_t e02 = f16x2_to_e4m3x2(nibbles_to_f16x2<F>(__byte_perm(ev, 0u, 0x4140u)));
-  const uint32_t e46 = f16x2_to_e4m3x2(nibbles_to_f16x2<F>(__byte_perm(ev, 0u, 0x4342u)));
-  const uint32_t o13 = f16x2_to_e4m3x2(nibbles_to_f16x2<F>(__byte_perm(od, 0u, 0x4140u)));
-  const uint32_t o57 = f16x2_to_e4m3x2(nibbles_to_f16x2<F>(__byte_perm(od, 0u, 0x4342u)));
-  o0 = __byte_perm(e02, o13, 0x5140u);
-  o1 = __byte_perm(e46, o57, 0x5140u);
+  o0 = nibble4_to_e4m3<F>(w);
+  o1 = nibble4_to_e4m3<F>(w >> 16);
 }
 
 // 4 int8 values (one word, k order) -> e4m3 bytes of 16 h (hi) and l (lo),
-// w = 16 h + l, h the signed high nibble, l the unsigned low nibble.
+// w = 16 h + l, h the signed high nibble, l the unsigned low nibble.  The four
+// low (high) nibbles are first packed into bits 0..15 as table selectors.
 __device__ __forceinline__ void int8x4_to_e4m3(uint32_t w, uint32_t& hi, uint32_t& lo) {
-  const uint32_t l = w & 0x0F0F0F0Fu;         // bytes: l0 l1 l2 l3
-  const uint32_t h = (w >> 4) & 0x0F0F0F0Fu;  // bytes: h0 h1 h2 h3 (4-bit two's complement)
-  lo = f16x2_to_e4m3x2(nibbles_to_f16x2<WFmt::kUint4>(__byte_perm(l, 0u, 0x4140u))) |
-       (f16x2_to_e4m3x2(nibbles_to_f16x2<WFmt::kUint4>(__byte_perm(l, 0u, 0x4342u))) << 16);
-  constexpr uint32_t k16 = 0x4C004C00u;  // 16.0 in both halves
-  hi = f16x2_to_e4m3x2(f16x2_mul(nibbles_to_f16x2<WFmt::kInt4>(__byte_perm(h, 0u, 0x4140u)), k16)) |
-       (f16x2_to_e4m3x2(f16x2_mul(nibbles_to_f16x2<WFmt::kInt4>(__byte_perm(h, 0u, 0x4342u)), k16)) << 16);
+  const uint32_t l = w & 0x0F0F0F0Fu, h = (w >> 4) & 0x0F0F0F0Fu;
+  lo = lut4<kU0, kU1, kU2, kU3, false>(prmt(l | (l >> 4), 0u, 0x0020u));
+  hi = lut4<kH0, kH1, kH2, kH3, true>(prmt(h | (h >> 4), 0u, 0x0020u));
 }
 
 template <int N>
