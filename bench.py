@@ -361,6 +361,23 @@ def run_suite(dev, peaks):
         record(f"fp8_decode_go{go}", ms, 2 * rows * n * k, bytes_)
     del fd, o
     torch.cuda.empty_cache()
+
+    # The decode workload with the other weight formats of the pages' dtype list (group_offset 0).
+    for fmt in ("e5m2", "int8", "int4", "uint4", "e2m1"):
+        fd = W.fp8_decode(dev, fmt=fmt)
+        sizes = fd["group_sizes"]
+        gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+        o = torch.empty((fd["lhs"].shape[0], n), dtype=torch.bfloat16, device=dev)
+        kw = {"rhs_format": fd["rhs_format"]} if fd["rhs_format"] else {}
+        rows = float(sizes.sum())
+        live = int((sizes > 0).sum())
+        ms = _time_call(torch, lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"],
+                                             rhs_bias=fd["rhs_bias"], out=o, **kw))
+        wbytes = n * k // 2 if fmt in W.PACKED else n * k
+        bytes_ = live * (wbytes + nb * n * 4 + n * 2) + rows * k * 2 + fd["lhs"].shape[0] * n * 2
+        record(f"decode_{fmt}_weights", ms, 2 * rows * n * k, bytes_)
+        del fd, o
+        torch.cuda.empty_cache()
     return res
 
 
