@@ -517,13 +517,22 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
               }
               const float* ts = tscale + sc * BT;
               const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
-              float d[T8];
-              tmem_ld_cols<T8>(col0, d);
+              if constexpr (T8 < 32) {
+                // h and l columns in one load
+                float d[2 * T8];
+                tmem_ld_cols<2 * T8>(col0, d);
 #pragma unroll
-              for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
-              tmem_ld_cols<T8>(col0 + T8, d);
+                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], fmaf(d[T8 + i], 0.0625f, d[i]), acc[i]);
+              } else {
+                // 32 h columns, then 32 l columns (fewer live registers)
+                float d[T8];
+                tmem_ld_cols<T8>(col0, d);
 #pragma unroll
-              for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i] * 0.0625f, d[i], acc[i]);
+                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
+                tmem_ld_cols<T8>(col0 + T8, d);
+#pragma unroll
+                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i] * 0.0625f, d[i], acc[i]);
+              }
               ++q;
               if (h == QPS - 1 || q == nq) {
                 tc_fence_before();
