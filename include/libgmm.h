@@ -68,6 +68,7 @@ enum {
 #define GMM_DEVERR_NEGATIVE_GROUP_SIZE 0x1u /* some group_sizes[g] < 0 (counted as 0) */
 #define GMM_DEVERR_GROUP_SIZES_EXCEED_M 0x2u /* sum(group_sizes) > m (groups cut at row m) */
 #define GMM_DEVERR_TIMEOUT 0x4u              /* an internal pipeline wait gave up; output is undefined */
+#define GMM_DEVERR_GROUP_OFFSET 0x8u         /* gmm_device_offset: offset out of range; nothing written */
 
 /* Largest num_total_groups (gmm, tgmm_local) or num_groups (tgmm) accepted. */
 #define GMM_MAX_GROUPS 1024
@@ -151,6 +152,28 @@ int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
              const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
              size_t workspace_bytes, void* stream);
+
+/*
+ * gmm_device_offset: gmm() or gmm_into() with group_offset read from device
+ * memory (page "tpu-inference ...", gmm.py: group_offset is a ()-shaped int32
+ * jnp array, a device value, turned into the kernels' scalar prefetch).
+ *
+ *   group_offset      device int32 [1], 4-byte aligned; read by the kernel when it
+ *                     runs, so a captured CUDA graph can be replayed with another
+ *                     offset written into it, and an offset computed on the device
+ *                     needs no copy to the host.
+ *   keep_other_rows   0: rows outside the local groups are set to 0 (gmm);
+ *                     1: they keep the caller's contents (gmm_into).
+ *   Everything else as gmm().  The host cannot check the offset: a value outside
+ *   [0, num_total_groups - num_local_groups] sets GMM_DEVERR_GROUP_OFFSET in the
+ *   workspace and the call writes nothing.  GMM_ERR_NULL if group_offset is NULL,
+ *   GMM_ERR_ALIGN if it is not 4-byte aligned.
+ */
+int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                      int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                      int32_t num_total_groups, const int32_t* group_offset, const float* rhs_scale,
+                      int32_t num_quant_blocks, const void* rhs_bias, int bias_dtype, void* out, int out_dtype,
+                      int keep_other_rows, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
 DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1 = range(8)
 # Packed 4-bit weight formats (uint8 tensors [L, n, k / 2], even k in the low nibble), by name.
 PACKED_FORMATS = {"int4": DTYPE_INT4, "uint4": DTYPE_UINT4, "e2m1": DTYPE_E2M1}
-DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT, DEVERR_GROUP_OFFSET = 0x1, 0x2, 0x4, 0x8
 
 _TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3,
                   torch.float8_e5m2: DTYPE_E5M2, torch.int8: DTYPE_INT8}
@@ -47,6 +47,8 @@ SIGNATURES = {
     "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
     "tgmm": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_into": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
+    "gmm_device_offset": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _P, _P, _I32, _P, _I, _P, _I, _I, _P,
+                           _SZ, _P], _I),
     "tgmm_local": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
     "gmm_read_device_errors": ([_P, _P, _U32P], _I),
@@ -142,12 +144,21 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
         nb = rhs_scale.shape[1]
     if rhs_bias is not None:
         _dev(rhs_bias, "rhs_bias")
-    rc = getattr(lib, fn)(
-        lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), rcode, rhs.shape[0], n, int(bool(transpose_rhs)),
-        group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
-        None if rhs_scale is None else rhs_scale.data_ptr(), nb,
-        None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
-        out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+    head = (lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), rcode, rhs.shape[0], n, int(bool(transpose_rhs)),
+            group_sizes.data_ptr(), group_sizes.shape[0])
+    tail = (None if rhs_scale is None else rhs_scale.data_ptr(), nb,
+            None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
+            out.data_ptr(), _code(out))
+    if isinstance(group_offset, torch.Tensor):
+        # a device scalar, read by the kernel when it runs (gmm_device_offset)
+        _dev(group_offset, "group_offset")
+        if group_offset.dtype != torch.int32 or group_offset.numel() != 1:
+            raise TypeError("a tensor group_offset must be one int32 on the device")
+        rc = lib.gmm_device_offset(*head, group_offset.data_ptr(), *tail, int(fn == "gmm_into"), ws.data_ptr(),
+                                   ws.numel(), _stream(lhs.device, stream))
+        fn = "gmm_device_offset"
+    else:
+        rc = getattr(lib, fn)(*head, int(group_offset), *tail, ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
     if rc != 0:
         raise GmmError(fn, rc)
     return out
@@ -156,7 +167,8 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
 def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
         out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None):
     """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
-    for each row r of local group g; all other rows of out are zero.  rhs is bf16, float8_e4m3fn,
+    for each row r of local group g; all other rows of out are zero.  group_offset is an int, or a
+    one-element int32 CUDA tensor that the kernel reads when it runs.  rhs is bf16, float8_e4m3fn,
     float8_e5m2 or int8, or a uint8 tensor [G_local, n, k / 2] of packed 4-bit weights with
     rhs_format = "int4", "uint4" or "e2m1"."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,

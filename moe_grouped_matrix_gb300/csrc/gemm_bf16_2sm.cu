@@ -68,6 +68,7 @@ struct Params {
   uint32_t* err;
   int32_t raster;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
+  const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
 };
 
 template <bool kOutF32>
@@ -111,6 +112,9 @@ template <bool kNT, bool kOutF32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_bf16_2sm_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_rhs,
                          const Params p) {
+  int32_t go;
+  if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
+    return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -150,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (warp == 2) {
     build_group_offsets(p.group_sizes, p.num_total_groups, p.m, offs, p.err);
-    build_tile_prefix(offs, p.group_offset, p.num_local_groups, PAIR_M, tiles);
+    build_tile_prefix(offs, go, p.num_local_groups, PAIR_M, tiles);
   }
   tc_fence_before();
   __syncthreads();
@@ -163,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int32_t k_blocks = (p.k + BK - 1) / BK;
   const int32_t total = m_tiles * n_tiles;
   auto tile_of = [&](int32_t w) {
-    return decode_gemm_tile(w, m_tiles, n_tiles, p.raster, tiles, offs, p.group_offset, p.num_local_groups,
+    return decode_gemm_tile(w, m_tiles, n_tiles, p.raster, tiles, offs, go, p.num_local_groups,
                             PAIR_M);
   };
 
@@ -288,8 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // caller keeps them (gmm_into).
     if (p.zero_rest) {
       const int64_t row_bytes = int64_t(p.n) * (kOutF32 ? 4 : 2);
-      const int64_t lo_bytes = int64_t(offs[p.group_offset]) * row_bytes;
-      const int64_t hi_begin = int64_t(offs[p.group_offset + p.num_local_groups]) * row_bytes;
+      const int64_t lo_bytes = int64_t(offs[go]) * row_bytes;
+      const int64_t hi_begin = int64_t(offs[go + p.num_local_groups]) * row_bytes;
       const int64_t n_lo = lo_bytes / 16;
       const int64_t n_all = n_lo + (int64_t(p.m) * row_bytes - hi_begin) / 16;
       const int64_t stride = int64_t(gridDim.x) * 128;
@@ -325,7 +329,7 @@ cudaError_t launch_impl(const GemmLaunch& L, int max_ctas, cudaStream_t stream) 
   if (clusters < 1) return cudaErrorLaunchOutOfResources;
   const int grid = 2 * (clusters < max_ctas / 2 ? clusters : max_ctas / 2);
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.bias,
-           L.bias_f32, L.err, L.raster, L.zero_rest};
+           L.bias_f32, L.err, L.raster, L.zero_rest, L.group_offset_dev};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

@@ -145,6 +145,7 @@ struct Params {
   void* out;
   uint32_t* err;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
+  const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
 };
 
 // Operand rows per half for a chunk of t token rows.
@@ -275,6 +276,9 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
                     const Params p) {
   using C = Cfg<F>;
   constexpr int QPS = C::QPS, NACC = C::NACC, NDONE = C::NDONE, NSC = C::NSC;
+  int32_t go;
+  if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
+    return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
   }
   if (warp == 2) {
     build_group_offsets(p.group_sizes, p.num_total_groups, p.m, offs, p.err);
-    build_tile_prefix(offs, p.group_offset, p.num_local_groups, BT, tiles);
+    build_tile_prefix(offs, go, p.num_local_groups, BT, tiles);
   }
   tc_fence_before();
   __syncthreads();
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
   const int32_t total = t_tiles * n_tiles;
   // Items: row chunks outer, the weight tiles of the chunk's group inner.
   auto item_of = [&](int32_t w) {
-    return decode_gemm_tile(w, t_tiles, n_tiles, n_tiles, tiles, offs, p.group_offset, p.num_local_groups, BT);
+    return decode_gemm_tile(w, t_tiles, n_tiles, n_tiles, tiles, offs, go, p.num_local_groups, BT);
   };
   auto halves = [&](int32_t ks) { return min(QPS, nq - QPS * ks); };
   // Step j's operand / converted stage is reused by step j + depth once step j's MMAs are done.
@@ -580,8 +584,8 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
     // caller keeps them (gmm_into).
     if (p.zero_rest) {
       const int64_t row_bytes = int64_t(p.n) * (kOutF32 ? 4 : 2);
-      const int64_t lo_bytes = int64_t(offs[p.group_offset]) * row_bytes;
-      const int64_t hi_begin = int64_t(offs[p.group_offset + p.num_local_groups]) * row_bytes;
+      const int64_t lo_bytes = int64_t(offs[go]) * row_bytes;
+      const int64_t hi_begin = int64_t(offs[go + p.num_local_groups]) * row_bytes;
       const int64_t n_lo = lo_bytes / 16;
       const int64_t n_all = n_lo + (int64_t(p.m) * row_bytes - hi_begin) / 16;
       const int64_t stride = int64_t(gridDim.x) * 128;
@@ -786,7 +790,7 @@ cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) 
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<F>::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
-           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest};
+           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev};
   kern<<<grid, Cfg<F>::kThreads, Cfg<F>::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

@@ -177,7 +177,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
              int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
              const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
-             size_t workspace_bytes, void* stream, int32_t zero_rest) {
+             size_t workspace_bytes, void* stream, int32_t zero_rest, const int32_t* group_offset_dev) {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -191,7 +191,10 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   if (num_total_groups < 1 || num_total_groups > GMM_MAX_GROUPS || num_local_groups < 1 ||
       num_local_groups > num_total_groups)
     return GMM_ERR_SHAPE;
-  if (group_offset < 0 || group_offset > num_total_groups - num_local_groups) return GMM_ERR_GROUP_OFFSET;
+  // A device-side offset is checked by the kernels (GMM_DEVERR_GROUP_OFFSET).
+  if (group_offset_dev == nullptr && (group_offset < 0 || group_offset > num_total_groups - num_local_groups))
+    return GMM_ERR_GROUP_OFFSET;
+  if (group_offset_dev != nullptr && reinterpret_cast<uintptr_t>(group_offset_dev) % 4 != 0) return GMM_ERR_ALIGN;
   const bool scaled_path = quantized || rhs_scale != nullptr;
   if (rhs_scale != nullptr) {
     if (num_quant_blocks < 1 || k % num_quant_blocks != 0) return GMM_ERR_SHAPE;
@@ -246,6 +249,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.out = out;
     S.err = err;
     S.zero_rest = zero_rest;
+    S.group_offset_dev = group_offset_dev;
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     cudaError_t e;
     if (rhs_dtype == GMM_DTYPE_BF16) {
@@ -303,6 +307,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   L.err = err;
   L.raster = 8;
   L.zero_rest = zero_rest;
+  L.group_offset_dev = group_offset_dev;
   // Work items (row tiles x n tiles, at most (m/128 + groups) x n/128) must fit in int32.
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
   if (m_tiles_max * ((n + 127) / 128) > INT32_MAX) return GMM_ERR_SHAPE;
@@ -326,7 +331,7 @@ int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, i
         void* stream) {
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out,
-                  out_dtype, workspace, workspace_bytes, stream, 1);
+                  out_dtype, workspace, workspace_bytes, stream, 1, nullptr);
 }
 
 int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
@@ -336,7 +341,18 @@ int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              size_t workspace_bytes, void* stream) {
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out,
-                  out_dtype, workspace, workspace_bytes, stream, 0);
+                  out_dtype, workspace, workspace_bytes, stream, 0, nullptr);
+}
+
+int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                      int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                      int32_t num_total_groups, const int32_t* group_offset, const float* rhs_scale,
+                      int32_t num_quant_blocks, const void* rhs_bias, int bias_dtype, void* out, int out_dtype,
+                      int keep_other_rows, void* workspace, size_t workspace_bytes, void* stream) {
+  if (group_offset == nullptr) return GMM_ERR_NULL;
+  return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                  num_total_groups, 0, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype, workspace,
+                  workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset);
 }
 
 int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,

@@ -20,7 +20,8 @@ struct GemmLaunch {
   int32_t bias_f32;  // bias dtype: 1 = f32, 0 = bf16
   uint32_t* err;
   int32_t raster;     // n-tiles per L2 super-column
-  int32_t zero_rest;  // 1: zero rows outside the local groups; 0: leave them as they are
+  int32_t zero_rest;                // 1: zero rows outside the local groups; 0: leave them as they are
+  const int32_t* group_offset_dev;  // NULL, or a device int32 that replaces group_offset
 };
 
 cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
@@ -68,7 +69,8 @@ struct ScaledLaunch {
   int32_t bias_f32;
   void* out;
   uint32_t* err;
-  int32_t zero_rest;  // 1: zero rows outside the local groups; 0: leave them as they are
+  int32_t zero_rest;                // 1: zero rows outside the local groups; 0: leave them as they are
+  const int32_t* group_offset_dev;  // NULL, or a device int32 that replaces group_offset
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);

@@ -12,6 +12,7 @@ namespace gmmk {
 constexpr uint32_t kErrNegativeSize = 0x1u;
 constexpr uint32_t kErrSizesExceedM = 0x2u;
 constexpr uint32_t kErrTimeout = 0x4u;
+constexpr uint32_t kErrGroupOffset = 0x8u;
 
 // A pipeline wait gives up after this many SM cycles (about 2 s at 2 GHz);
 // the kernel then records kErrTimeout and unwinds instead of hanging.

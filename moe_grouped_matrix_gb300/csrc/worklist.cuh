@@ -52,6 +52,20 @@ __device__ __forceinline__ void build_group_offsets(const int32_t* __restrict__ 
   __syncwarp();
 }
 
+// The first local group: the host value, or the device scalar when one is given
+// (the pages pass group_offset as a device array).  Every thread reads the same
+// value; an out-of-range device value records kErrGroupOffset and the caller
+// returns before touching shared memory, barriers or TMEM, writing nothing.
+__device__ __forceinline__ bool resolve_group_offset(const int32_t* dev, int32_t host, int32_t total, int32_t local,
+                                                     uint32_t* err, int32_t& go) {
+  go = host;
+  if (dev == nullptr) return true;
+  go = __ldg(dev);
+  if (go >= 0 && go <= total - local) return true;
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, kErrGroupOffset);
+  return false;
+}
+
 // tiles[0..L]: exclusive prefix sum over local groups l of ceil(rows_l / bm),
 // rows_l = offs[first + l + 1] - offs[first + l].  All 32 lanes of one warp.
 __device__ __forceinline__ void build_tile_prefix(const int32_t* offs, int32_t first, int32_t local, int32_t bm,

@@ -29,7 +29,7 @@ def lib():
 def test_header_declares_the_expected_calls():
     assert declared_functions() == sorted(
         ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error",
-         "gmm_noalloc", "gmm_into", "tgmm_local"])
+         "gmm_noalloc", "gmm_into", "tgmm_local", "gmm_device_offset"])
 
 
 def test_library_exports_every_declared_symbol(lib):
