@@ -61,7 +61,8 @@ enum {
   GMM_ERR_GROUP_OFFSET = 5, /* group_offset outside [0, num_total_groups - num_local_groups] */
   GMM_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or smaller than gmm_workspace_bytes() */
   GMM_ERR_ARCH = 7,         /* current device is not compute capability 10.3 */
-  GMM_ERR_CUDA = 8          /* a CUDA runtime or driver call failed; see gmm_last_cuda_error() */
+  GMM_ERR_CUDA = 8,         /* a CUDA runtime or driver call failed; see gmm_last_cuda_error() */
+  GMM_ERR_IO = 9            /* a tiling-table file could not be read, parsed or written */
 };
 
 /* Sticky device-side error flags kept in the workspace. */
@@ -115,8 +116,10 @@ size_t gmm_workspace_bytes(void);
  *                group size m / num_total_groups: SM-pair 256x256 row tiles (>= 1024 rows),
  *                SM-pair tiles of 256 weight rows x up to 256 group rows rounded to 32 (>= 16),
  *                or single-SM tiles of 128 weight rows x group rows rounded to 16 (fewer).
- *                The environment variable GMM_BF16_KERNEL = auto | pair | swap_pair | swap |
- *                single overrides the choice (any other value: GMM_ERR_SHAPE).  All give
+ *                A tiling-table entry for the problem's class (gmm_tune, gmm_tuning_set)
+ *                replaces that rule.  The environment variable GMM_BF16_KERNEL = auto |
+ *                pair | swap_pair | swap | single overrides both (any other value:
+ *                GMM_ERR_SHAPE).  All give
  *                results within the same bound; they may differ in the last bits.
  *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
  *   out          [m, n] of out_dtype (BF16 or F32).
@@ -248,6 +251,61 @@ int gmm_noalloc(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void
                 int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
                 int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
                 const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* stream);
+
+/* ------------------------------------------------------------------ tiling table
+ * The pages let `tiling` be a callable that looks the problem dimensions up in a
+ * LUT of tuned tile sizes (page "tpu-inference ...", gmm.py: gmm).  Here each
+ * kernel's tiles are fixed and the per-problem choice is which bf16 kernel runs
+ * (and, for the row-tile kernels, the width of the L2 raster's super-columns).
+ * A process-wide table maps a problem class to that choice:
+ *   rows_log2 = floor(log2(m / num_total_groups)) (average rows per group),
+ *   k, n, num_total_groups, transpose_rhs (0/1), out_dtype.
+ * gmm(), gmm_into() and gmm_device_offset() with bf16 weights and no scale use
+ * the table's entry for their class when there is one (the GMM_BF16_KERNEL
+ * environment variable still overrides it), else the built-in rule.  The table is
+ * guarded by a mutex; calls on any thread see every completed update.
+ */
+enum {
+  GMM_KERNEL_AUTO = 0,      /* no entry / built-in rule */
+  GMM_KERNEL_PAIR = 1,      /* SM-pair 256 x 256 row tiles */
+  GMM_KERNEL_SWAP_PAIR = 2, /* SM-pair, 256 weight rows x up to 256 group rows */
+  GMM_KERNEL_SWAP = 3,      /* one SM, 128 weight rows x up to 256 group rows */
+  GMM_KERNEL_SINGLE = 4     /* one SM, 128 x 256 row tiles */
+};
+
+/* Sets the entry of one problem class.  raster: 0 (default, 8) or 1..64 n tiles
+ * per super-column (used by PAIR and SINGLE).  GMM_ERR_SHAPE for invalid values. */
+int gmm_tuning_set(int32_t rows_log2, int64_t k, int64_t n, int32_t num_total_groups, int transpose_rhs,
+                   int out_dtype, int kernel, int raster);
+
+/* *kernel = the entry's kernel (GMM_KERNEL_AUTO if the class has none), *raster its raster. */
+int gmm_tuning_get(int32_t rows_log2, int64_t k, int64_t n, int32_t num_total_groups, int transpose_rhs,
+                   int out_dtype, int* kernel, int* raster);
+
+/* Empties the table. */
+int gmm_tuning_clear(void);
+
+/* Writes the table to `path` as text: a first line "# libgmm tiling table 1", then
+ * one line per entry "rows_log2 k n num_total_groups transpose_rhs out_dtype kernel
+ * raster".  gmm_tuning_load() reads such a file and adds its entries (replacing
+ * entries of the same class); on any malformed line it adds nothing and returns
+ * GMM_ERR_IO, as it does when the file cannot be opened. */
+int gmm_tuning_save(const char* path);
+int gmm_tuning_load(const char* path);
+
+/*
+ * Times every bf16 kernel choice (PAIR with rasters 4, 8 and 16, SWAP_PAIR, SWAP,
+ * SINGLE with raster 8) on this problem, with the caller's buffers (`out` is
+ * written), `iterations` launches each after one warm-up launch, using CUDA events
+ * on `stream`, which it synchronises.  Records the fastest in the table and returns
+ * it in *kernel, *raster and its mean time in *ms.  Arguments as gmm(); bf16
+ * weights without scale only (else GMM_ERR_DTYPE); iterations in 1..1000.
+ */
+int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+             int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+             int32_t num_total_groups, int32_t group_offset, const void* rhs_bias, int bias_dtype, void* out,
+             int out_dtype, void* workspace, size_t workspace_bytes, void* stream, int iterations, int* kernel,
+             int* raster, float* ms);
 
 /*
  * Synchronises `stream`, then reads and clears the sticky device error flags

@@ -22,7 +22,8 @@ import threading
 
 import torch
 
-__all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
+__all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "tune", "tuning_set", "tuning_get", "tuning_clear",
+           "tuning_save", "tuning_load", "tuning_rows_log2", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
            "DEVERR_NEGATIVE_GROUP_SIZE", "DEVERR_GROUP_SIZES_EXCEED_M", "DEVERR_TIMEOUT"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
@@ -30,6 +31,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
 DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1 = range(8)
 # Packed 4-bit weight formats (uint8 tensors [L, n, k / 2], even k in the low nibble), by name.
 PACKED_FORMATS = {"int4": DTYPE_INT4, "uint4": DTYPE_UINT4, "e2m1": DTYPE_E2M1}
+# bf16 forward kernels, as the tiling table names them.
+KERNEL_AUTO, KERNEL_PAIR, KERNEL_SWAP_PAIR, KERNEL_SWAP, KERNEL_SINGLE = range(5)
 DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT, DEVERR_GROUP_OFFSET = 0x1, 0x2, 0x4, 0x8
 
 _TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3,
@@ -42,6 +45,7 @@ _workspaces: dict[int, torch.Tensor] = {}
 # Every function the header declares, with its ctypes signature.
 _P, _I, _I32, _I64, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
                                   ctypes.POINTER(ctypes.c_uint32))
+_IP = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "gmm_workspace_bytes": ([], _SZ),
     "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
@@ -51,6 +55,13 @@ SIGNATURES = {
                            _SZ, _P], _I),
     "tgmm_local": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
+    "gmm_tuning_set": ([_I32, _I64, _I64, _I32, _I, _I, _I, _I], _I),
+    "gmm_tuning_get": ([_I32, _I64, _I64, _I32, _I, _I, _IP, _IP], _I),
+    "gmm_tuning_clear": ([], _I),
+    "gmm_tuning_save": ([ctypes.c_char_p], _I),
+    "gmm_tuning_load": ([ctypes.c_char_p], _I),
+    "gmm_tune": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I, _P, _I, _P, _SZ, _P, _I, _IP,
+                  _IP, ctypes.POINTER(ctypes.c_float)], _I),
     "gmm_read_device_errors": ([_P, _P, _U32P], _I),
     "gmm_status_string": ([_I], ctypes.c_char_p),
     "gmm_last_cuda_error": ([], _I),
@@ -233,6 +244,66 @@ def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=No
     if rc != 0:
         raise GmmError("tgmm", rc)
     return out
+
+
+def tuning_rows_log2(m: int, num_total_groups: int) -> int:
+    """The table's row class: floor(log2(m // num_total_groups)), 0 when that is 0."""
+    avg = m // num_total_groups if num_total_groups > 0 else m
+    return max(avg.bit_length() - 1, 0)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise GmmError(fn, rc)
+
+
+def tuning_set(rows_log2, k, n, num_total_groups, transpose_rhs, out_dtype, kernel, raster=0):
+    """Records the bf16 kernel (KERNEL_*) and raster for a problem class."""
+    _check("gmm_tuning_set", load_library().gmm_tuning_set(rows_log2, k, n, num_total_groups, int(bool(transpose_rhs)),
+                                                           _TORCH_TO_CODE[out_dtype], kernel, raster))
+
+
+def tuning_get(rows_log2, k, n, num_total_groups, transpose_rhs, out_dtype):
+    """(kernel, raster) recorded for a problem class; kernel is KERNEL_AUTO if none."""
+    kern, ras = ctypes.c_int(0), ctypes.c_int(0)
+    _check("gmm_tuning_get", load_library().gmm_tuning_get(rows_log2, k, n, num_total_groups, int(bool(transpose_rhs)),
+                                                           _TORCH_TO_CODE[out_dtype], ctypes.byref(kern),
+                                                           ctypes.byref(ras)))
+    return kern.value, ras.value
+
+
+def tuning_clear():
+    _check("gmm_tuning_clear", load_library().gmm_tuning_clear())
+
+
+def tuning_save(path: str):
+    _check("gmm_tuning_save", load_library().gmm_tuning_save(os.fsencode(path)))
+
+
+def tuning_load(path: str):
+    _check("gmm_tuning_load", load_library().gmm_tuning_load(os.fsencode(path)))
+
+
+def tune(lhs, rhs, group_sizes, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
+         out_dtype=torch.bfloat16, iterations=10, workspace=None, stream=None):
+    """Times every bf16 kernel choice on this problem (writing `out`), records the fastest in the
+    tiling table and returns (kernel, raster, mean ms)."""
+    lib = load_library()
+    _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
+    m, k = lhs.shape
+    n = rhs.shape[1] if transpose_rhs else rhs.shape[2]
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
+    _dev(out, "out")
+    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    kern, ras, ms = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_float(0)
+    rc = lib.gmm_tune(lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n,
+                      int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
+                      None if rhs_bias is None else rhs_bias.data_ptr(), 0 if rhs_bias is None else _code(rhs_bias),
+                      out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream),
+                      int(iterations), ctypes.byref(kern), ctypes.byref(ras), ctypes.byref(ms))
+    _check("gmm_tune", rc)
+    return kern.value, ras.value, ms.value
 
 
 def read_device_errors(device=None, workspace=None, stream=None) -> int:

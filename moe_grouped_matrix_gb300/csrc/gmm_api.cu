@@ -105,11 +105,27 @@ bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 //   kSwap     one SM, 128 weight rows x up to 256 rows (rounded to 16);
 //   kSingle   one SM, 128 x 256 tiles of rows x n.
 // Groups averaging 1024 rows or more go to kPair, 16 or more to kSwapPair,
-// fewer to kSwap.  GMM_BF16_KERNEL = single | pair | swap | swap_pair
-// overrides the choice (for tuning and tests).
+// fewer to kSwap, unless the tiling table has an entry for the problem's class
+// (tuning.cu).  GMM_BF16_KERNEL = single | pair | swap | swap_pair overrides both
+// (for tuning and tests).
 enum class BF16Kernel { kSingle, kPair, kSwap, kSwapPair, kInvalid };
 
-BF16Kernel choose_bf16_kernel(int64_t m, int32_t num_total_groups) {
+BF16Kernel kernel_of_id(int id) {
+  switch (id) {
+    case GMM_KERNEL_PAIR: return BF16Kernel::kPair;
+    case GMM_KERNEL_SWAP_PAIR: return BF16Kernel::kSwapPair;
+    case GMM_KERNEL_SWAP: return BF16Kernel::kSwap;
+    case GMM_KERNEL_SINGLE: return BF16Kernel::kSingle;
+  }
+  return BF16Kernel::kInvalid;
+}
+
+// The kernel and raster (0: default) for a problem; `forced` (a GMM_KERNEL_* id,
+// from gmm_tune) wins over everything.
+BF16Kernel choose_bf16_kernel(int64_t m, int64_t k, int64_t n, int32_t num_total_groups, int transpose_rhs,
+                              int out_dtype, int forced, int32_t* raster) {
+  *raster = 0;
+  if (forced != GMM_KERNEL_AUTO) return kernel_of_id(forced);
   if (const char* env = std::getenv("GMM_BF16_KERNEL")) {
     if (std::strcmp(env, "single") == 0) return BF16Kernel::kSingle;
     if (std::strcmp(env, "pair") == 0) return BF16Kernel::kPair;
@@ -117,6 +133,10 @@ BF16Kernel choose_bf16_kernel(int64_t m, int32_t num_total_groups) {
     if (std::strcmp(env, "swap_pair") == 0) return BF16Kernel::kSwapPair;
     if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return BF16Kernel::kInvalid;
   }
+  int32_t id = GMM_KERNEL_AUTO;
+  if (gmmk::tuning_lookup(gmmk::tuning_rows_log2(m, num_total_groups), k, n, num_total_groups, transpose_rhs != 0,
+                          out_dtype, &id, raster))
+    return kernel_of_id(id);
   if (m >= int64_t(1024) * num_total_groups) return BF16Kernel::kPair;
   if (m >= int64_t(16) * num_total_groups) return BF16Kernel::kSwapPair;
   return BF16Kernel::kSwap;
@@ -150,6 +170,7 @@ const char* gmm_status_string(int status) {
     case GMM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case GMM_ERR_ARCH: return "current device is not compute capability 10.3";
     case GMM_ERR_CUDA: return "CUDA call failed";
+    case GMM_ERR_IO: return "tiling-table file could not be read, parsed or written";
   }
   return "unknown status";
 }
@@ -177,7 +198,8 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
              int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
              const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
-             size_t workspace_bytes, void* stream, int32_t zero_rest, const int32_t* group_offset_dev) {
+             size_t workspace_bytes, void* stream, int32_t zero_rest, const int32_t* group_offset_dev,
+             int forced_kernel = GMM_KERNEL_AUTO, int32_t forced_raster = 0) {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -270,8 +292,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     return GMM_OK;
   }
 
-  const BF16Kernel kind = choose_bf16_kernel(m, num_total_groups);
+  int32_t raster = 0;
+  const BF16Kernel kind =
+      choose_bf16_kernel(m, k, n, num_total_groups, transpose_rhs, out_dtype, forced_kernel, &raster);
   if (kind == BF16Kernel::kInvalid) return GMM_ERR_SHAPE;
+  if (forced_kernel != GMM_KERNEL_AUTO) raster = forced_raster;
   gmmk::GemmLaunch L{};
   {
     const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
@@ -305,7 +330,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   L.bias = rhs_bias;
   L.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
   L.err = err;
-  L.raster = 8;
+  L.raster = raster > 0 ? raster : 8;
   L.zero_rest = zero_rest;
   L.group_offset_dev = group_offset_dev;
   // Work items (row tiles x n tiles, at most (m/128 + groups) x n/128) must fit in int32.
@@ -353,6 +378,63 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, 0, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype, workspace,
                   workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset);
+}
+
+int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+             int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+             int32_t num_total_groups, int32_t group_offset, const void* rhs_bias, int bias_dtype, void* out,
+             int out_dtype, void* workspace, size_t workspace_bytes, void* stream, int iterations, int* kernel,
+             int* raster, float* ms) {
+  if (kernel == nullptr || raster == nullptr || ms == nullptr) return GMM_ERR_NULL;
+  if (rhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  if (iterations < 1 || iterations > 1000) return GMM_ERR_SHAPE;
+  struct Candidate {
+    int kernel;
+    int32_t raster;
+  };
+  static const Candidate kCandidates[] = {{GMM_KERNEL_PAIR, 4},      {GMM_KERNEL_PAIR, 8}, {GMM_KERNEL_PAIR, 16},
+                                          {GMM_KERNEL_SWAP_PAIR, 0}, {GMM_KERNEL_SWAP, 0}, {GMM_KERNEL_SINGLE, 8}};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t t0 = nullptr, t1 = nullptr;
+  cudaError_t e = cudaEventCreate(&t0);
+  if (e == cudaSuccess) e = cudaEventCreate(&t1);
+  if (e != cudaSuccess) {
+    if (t0) cudaEventDestroy(t0);
+    return cuda_fail(e);
+  }
+  int status = GMM_OK;
+  float best = -1.f;
+  Candidate chosen{GMM_KERNEL_AUTO, 0};
+  for (const Candidate& c : kCandidates) {
+    auto run = [&]() {
+      return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                      num_total_groups, group_offset, nullptr, 0, rhs_bias, bias_dtype, out, out_dtype, workspace,
+                      workspace_bytes, stream, 1, nullptr, c.kernel, c.raster);
+    };
+    status = run();  // warm-up; also validates the arguments
+    if (status != GMM_OK) break;
+    if ((e = cudaEventRecord(t0, s)) != cudaSuccess) break;
+    for (int i = 0; i < iterations && status == GMM_OK; ++i) status = run();
+    if (status != GMM_OK) break;
+    if ((e = cudaEventRecord(t1, s)) != cudaSuccess || (e = cudaEventSynchronize(t1)) != cudaSuccess) break;
+    float elapsed = 0.f;
+    if ((e = cudaEventElapsedTime(&elapsed, t0, t1)) != cudaSuccess) break;
+    elapsed /= float(iterations);
+    if (best < 0.f || elapsed < best) {
+      best = elapsed;
+      chosen = c;
+    }
+  }
+  cudaEventDestroy(t0);
+  cudaEventDestroy(t1);
+  if (status != GMM_OK) return status;
+  if (e != cudaSuccess) return cuda_fail(e);
+  gmmk::tuning_store(gmmk::tuning_rows_log2(m, num_total_groups), k, n, num_total_groups, transpose_rhs != 0,
+                     out_dtype, chosen.kernel, chosen.raster);
+  *kernel = chosen.kernel;
+  *raster = chosen.raster;
+  *ms = best;
+  return GMM_OK;
 }
 
 int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,

@@ -91,4 +91,13 @@ cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, i
 cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
                                  cudaStream_t stream);
 
+// Per-shape kernel table (tuning.cu).  kernel: a GMM_KERNEL_* id; raster 0 =
+// the default super-column width.
+int32_t tuning_rows_log2(int64_t m, int32_t num_total_groups);
+bool tuning_lookup(int32_t rows_log2, int64_t k, int64_t n, int32_t groups, int32_t transpose, int32_t out_dtype,
+                   int32_t* kernel, int32_t* raster);
+void tuning_store(int32_t rows_log2, int64_t k, int64_t n, int32_t groups, int32_t transpose, int32_t out_dtype,
+                  int32_t kernel, int32_t raster);
+bool tuning_valid(int32_t kernel, int32_t raster);
+
 }  // namespace gmmk

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
@@ -29,7 +30,8 @@ def lib():
 def test_header_declares_the_expected_calls():
     assert declared_functions() == sorted(
         ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error",
-         "gmm_noalloc", "gmm_into", "tgmm_local", "gmm_device_offset"])
+         "gmm_noalloc", "gmm_into", "tgmm_local", "gmm_device_offset", "gmm_tuning_set", "gmm_tuning_get",
+         "gmm_tuning_clear", "gmm_tuning_save", "gmm_tuning_load", "gmm_tune"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -40,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert lib.gmm_status_string(0) == b"ok"
-    for code in range(1, 9):
+    for code in range(1, 10):
         assert lib.gmm_status_string(code) != b"unknown status"
     assert lib.gmm_workspace_bytes() >= 4
 
@@ -99,3 +101,46 @@ def test_tgmm_local_host_validation(lib):
     assert t(go=5) == 5
     assert t(go=-1) == 5
     assert t(out=ctypes.c_void_p((1 << 20) + 4)) == 4
+
+
+# ------------------------------------------------------------------ tiling table (host only)
+def test_tiling_table_set_get_save_load(lib, tmp_path):
+    G.tuning_clear()
+    assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_AUTO, 0)
+    G.tuning_set(7, 4096, 28672, 8, True, torch.bfloat16, G.KERNEL_SINGLE, 16)
+    G.tuning_set(3, 2048, 2048, 128, False, torch.float32, G.KERNEL_SWAP)
+    assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_SINGLE, 16)
+    assert G.tuning_get(7, 4096, 28672, 8, False, torch.bfloat16) == (G.KERNEL_AUTO, 0)
+    path = tmp_path / "table.txt"
+    G.tuning_save(str(path))
+    lines = path.read_text().splitlines()
+    assert lines[0] == "# libgmm tiling table 1"
+    assert sorted(lines[1:]) == sorted(["7 4096 28672 8 1 0 4 16", "3 2048 2048 128 0 1 3 0"])
+    G.tuning_clear()
+    assert G.tuning_get(3, 2048, 2048, 128, False, torch.float32) == (G.KERNEL_AUTO, 0)
+    G.tuning_load(str(path))
+    assert G.tuning_get(3, 2048, 2048, 128, False, torch.float32) == (G.KERNEL_SWAP, 0)
+    assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_SINGLE, 16)
+    G.tuning_clear()
+
+
+@pytest.mark.parametrize("body", ["7 4096 28672 8 1 0 9 0\n", "7 4096 28672 8 1 0 1\n", "7 4096 x 8 1 0 1 0\n",
+                                  "7 4096 28672 8 1 0 1 65\n", "7 4096 28672 8 1 0 1 0 extra\n"])
+def test_tiling_table_rejects_malformed_files(lib, tmp_path, body):
+    G.tuning_clear()
+    good = "3 2048 2048 128 0 1 3 0\n"
+    path = tmp_path / "bad.txt"
+    path.write_text("# libgmm tiling table 1\n" + good + body)
+    assert lib.gmm_tuning_load(str(path).encode()) == 9
+    assert G.tuning_get(3, 2048, 2048, 128, False, torch.float32) == (G.KERNEL_AUTO, 0), "nothing added"
+    path.write_text("no header\n" + good)
+    assert lib.gmm_tuning_load(str(path).encode()) == 9
+    assert lib.gmm_tuning_load(str(tmp_path / "missing.txt").encode()) == 9
+
+
+def test_tiling_table_rejects_bad_entries(lib):
+    assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 0, 0) == 3   # AUTO is not an entry
+    assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 5, 0) == 3
+    assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 1, 99) == 3
+    assert lib.gmm_tuning_set(-1, 4096, 4096, 8, 1, 0, 1, 0) == 3
+    assert G.tuning_rows_log2(16384, 8) == 11 and G.tuning_rows_log2(5, 8) == 0 and G.tuning_rows_log2(32768, 128) == 8
