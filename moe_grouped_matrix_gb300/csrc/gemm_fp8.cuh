@@ -731,11 +731,10 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
           for (int h = 0; h < hq; ++h) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int c = 4 * h + i;
               uint32_t x[4];
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                           : "r"(src + (uint32_t(c ^ (r & 7)) << 4)));
+                           : "r"(src + (uint32_t((4 * h + i) ^ (r & 7)) << 4)));
               uint32_t o[8];
 #pragma unroll
               for (int u = 0; u < 4; ++u) nibble8_to_e4m3<F>(x[u], o[2 * u], o[2 * u + 1]);
@@ -745,15 +744,18 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
             }
           }
         } else {
+          // int8: the row's 8 raw chunks are loaded first, so that their latencies overlap
+          uint32_t x[8][4];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x[c][0]), "=r"(x[c][1]), "=r"(x[c][2]), "=r"(x[c][3])
+                         : "r"(src + (uint32_t(c ^ (r & 7)) << 4)));
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint32_t x[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                         : "r"(src + (uint32_t(c ^ (r & 7)) << 4)));
             uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) int8x4_to_e4m3(x[u], hi[u], lo[u]);
+            for (int u = 0; u < 4; ++u) int8x4_to_e4m3(x[c][u], hi[u], lo[u]);
             const uint32_t pos = uint32_t(c ^ (r & 7)) << 4;
             st_shared_v4(dst + pos, hi[0], hi[1], hi[2], hi[3]);
             st_shared_v4(dst + A_SUB + pos, lo[0], lo[1], lo[2], lo[3]);
