@@ -14,7 +14,8 @@
 //
 // Roles, per CTA (192 threads):
 //   warp 0     TMA producer (both CTAs): this CTA's 128 weight rows and its
-//              N/2 chunk rows per 64-wide k step; bytes of both CTAs' copies
+//              N/2 chunk rows per 128-wide k step (two 64-wide boxes each, 3
+//              stages of 64 KB); bytes of both CTAs' copies
 //              land on the stage's full barrier in the leader CTA
 //   warp 1     TMEM (512 columns, allocated by both CTAs together); in the
 //              leader CTA it also issues the MMAs (M = 256, N, K = 16)
@@ -33,13 +34,16 @@ namespace {
 constexpr int BW = 128;      // weight rows per CTA (its half of the MMA's M = 256)
 constexpr int PAIR_W = 256;  // weight rows (n) per pair tile
 constexpr int CHUNK = 256;   // largest N: rows of a group per item
-constexpr int BK = 64;
-constexpr int STAGES = 6;
+constexpr int BK = 128;      // k per stage: two 64-wide boxes, adjacent in k, per operand
+constexpr int KH = BK / 64;
+constexpr int STAGES = 3;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 1024;
-constexpr uint32_t A_BYTES = BW * BK * 2;              // this CTA's weight rows
-constexpr uint32_t B_BYTES = (CHUNK / 2) * BK * 2;     // up to half a chunk of rows
-constexpr uint32_t TBOX_BYTES = 64 * BK * 2;           // one 64-row box of rows
+constexpr uint32_t A_HALF = BW * 64 * 2;               // this CTA's weight rows over 64 k
+constexpr uint32_t A_BYTES = KH * A_HALF;
+constexpr uint32_t B_HALF = (CHUNK / 2) * 64 * 2;      // up to half a chunk of rows over 64 k
+constexpr uint32_t B_BYTES = KH * B_HALF;
+constexpr uint32_t TBOX_BYTES = 64 * 64 * 2;           // one {64 k, 64 rows} box of rows
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * CHUNK;
 
@@ -157,18 +161,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (A_BYTES + uint32_t(nbox) * TBOX_BYTES));
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * (A_BYTES + uint32_t(KH * nbox) * TBOX_BYTES));
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const uint32_t a_dst = sbase + OFF_A + stage * A_BYTES;
           const uint32_t b_dst = sbase + OFF_B + stage * B_BYTES;
-          if constexpr (kNT) {
-            tma_load_3d_pair(a_dst, &tm_rhs, fb, kb * BK, wrow, t.local_group);
-          } else {
 #pragma unroll
-            for (int j = 0; j < BW / 64; ++j)
-              tma_load_3d_pair(a_dst + j * 8192u, &tm_rhs, fb, wrow + 64 * j, kb * BK, t.local_group);
+          for (int kh = 0; kh < KH; ++kh) {
+            const int32_t kc = kb * BK + 64 * kh;  // past k the boxes are zero-filled
+            if constexpr (kNT) {
+              tma_load_3d_pair(a_dst + kh * A_HALF, &tm_rhs, fb, kc, wrow, t.local_group);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BW / 64; ++j)
+                tma_load_3d_pair(a_dst + kh * A_HALF + j * 8192u, &tm_rhs, fb, wrow + 64 * j, kc, t.local_group);
+            }
+            for (int32_t j = 0; j < nbox; ++j)
+              tma_load_2d_pair(b_dst + kh * B_HALF + j * TBOX_BYTES, &tm_lhs, fb, kc, trow + 64 * j);
           }
-          for (int32_t j = 0; j < nbox; ++j) tma_load_2d_pair(b_dst + j * TBOX_BYTES, &tm_lhs, fb, kb * BK, trow + 64 * j);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -206,9 +215,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t b0 = sbase + OFF_B + stage * B_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t ah = a0 + (kk / 4) * A_HALF, bh = b0 + (kk / 4) * B_HALF;
+              const int kq = kk % 4;
               const uint64_t ad =
-                  kNT ? sw128_desc(a0 + kk * 32, 16, 1024) : sw128_desc(a0 + kk * 2048, 8192, 1024);
-              const uint64_t bd = sw128_desc(b0 + kk * 32, 16, 1024);
+                  kNT ? sw128_desc(ah + kq * 32, 16, 1024) : sw128_desc(ah + kq * 2048, 8192, 1024);
+              const uint64_t bd = sw128_desc(bh + kq * 32, 16, 1024);
               mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             }
             mma_commit_pair(empty_bar(stage), 0x3);
