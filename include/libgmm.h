@@ -189,6 +189,10 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *   lhs    [m, k] BF16;  dout [m, n] BF16;  out [num_groups, k, n] F32 or BF16.
  *   group_sizes device int32 [num_groups], 1 <= num_groups <= GMM_MAX_GROUPS.
  *   Sizes: m >= 0, k % 8 == 0, n % 8 == 0, k, n >= 8; pointers 16-byte aligned.
+ *   Two kernels give the same results within the bound: one SM per 128 x 256
+ *   output tile (default) and SM pairs on 256 x 256 tiles; the environment
+ *   variable GMM_TGMM_KERNEL = single | pair | auto selects one (any other value:
+ *   GMM_ERR_SHAPE).
  *   For an NT weight [G, n, k] the matching gradient is tgmm(dout, x): pass the
  *   forward output gradient as `lhs` and the forward input as `dout`.
  */

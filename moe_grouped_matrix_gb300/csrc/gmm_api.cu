@@ -493,7 +493,18 @@ int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype,
   L.k = int32_t(k);
   L.out = out;
   L.err = static_cast<uint32_t*>(workspace);
-  cudaError_t e = gmmk::launch_tgmm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s);
+  // One SM per tile by default; GMM_TGMM_KERNEL = pair selects the SM-pair
+  // kernel (256 x 256 tiles; as fast on the 128-expert workload, kept for
+  // comparison).
+  bool pair = false;
+  if (const char* env = std::getenv("GMM_TGMM_KERNEL")) {
+    if (std::strcmp(env, "pair") == 0)
+      pair = true;
+    else if (std::strcmp(env, "single") != 0 && std::strcmp(env, "auto") != 0 && env[0] != '\0')
+      return GMM_ERR_SHAPE;
+  }
+  cudaError_t e = pair ? gmmk::launch_tgmm_2sm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s)
+                       : gmmk::launch_tgmm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
 }

@@ -54,6 +54,8 @@ struct TgmmLaunch {
 };
 
 cudaError_t launch_tgmm(const TgmmLaunch& p, bool out_f32, int grid, cudaStream_t stream);
+// The same on SM pairs (256 x 256 output tiles, tcgen05.mma.cta_group::2).
+cudaError_t launch_tgmm_2sm(const TgmmLaunch& p, bool out_f32, int max_ctas, cudaStream_t stream);
 
 // Block-scaled grouped matmul for small groups (decode): rhs e4m3 or bf16
 // [L, n, k], per-(group, k-block, n) fp32 scale, optional bias.

@@ -288,6 +288,35 @@ __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t
   return done;
 }
 
+// Non-blocking test of the same (no suspension: for per-stage handshakes whose
+// arrivals come from another CTA).
+__device__ __forceinline__ uint32_t mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done;
+}
+
+// Bounded spin on mbar_test_wait_cluster.
+__device__ __forceinline__ bool spin_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                 uint32_t* err) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1u;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // Bounded wait for arrivals that come from other CTAs of the cluster.
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                  uint32_t* err) {
@@ -355,6 +384,18 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
+}
+
+// 16-byte store into the shared memory of a CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy writes to the shared memory of any CTA of
+// the cluster before its later async-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ misc

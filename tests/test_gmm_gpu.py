@@ -159,6 +159,13 @@ def test_stream_ordering_on_side_stream():
 
 
 # ------------------------------------------------------------------------ tgmm
+@pytest.fixture(params=["pair", "single"])
+def tgmm_kernel(request, monkeypatch):
+    """Runs the test on the one-SM tgmm kernel (default) and the SM-pair kernel (GMM_TGMM_KERNEL)."""
+    monkeypatch.setenv("GMM_TGMM_KERNEL", request.param)
+    return request.param
+
+
 def _tgmm_case(m, k, n, sizes, out_dtype=torch.float32, seed=0):
     sizes = np.asarray(sizes, np.int32)
     lhs = W.normal((m, k), 1.0, seed + 1, DEV)
@@ -172,21 +179,21 @@ def _tgmm_case(m, k, n, sizes, out_dtype=torch.float32, seed=0):
 
 
 @pytest.mark.parametrize("out_dtype", ODT)
-def test_tgmm_ragged(out_dtype):
+def test_tgmm_ragged(out_dtype, tgmm_kernel):
     # group rows 100 (tail 36), 0, 333, 64 (exactly one chunk), 3; rows 500..599 unused
     _tgmm_case(600, 200, 264, [100, 0, 333, 64, 3], out_dtype=out_dtype)
 
 
-def test_tgmm_group_edges_straddle_chunks():
+def test_tgmm_group_edges_straddle_chunks(tgmm_kernel):
     _tgmm_case(1000, 128, 256, [65, 63, 1, 128, 129, 0, 614], seed=7)
 
 
-def test_tgmm_all_empty_is_zero():
+def test_tgmm_all_empty_is_zero(tgmm_kernel):
     out = _tgmm_case(64, 128, 256, [0, 0])
     assert (out == 0).all()
 
 
-def test_tgmm_sums_to_dense_when_groups_cover_all_rows():
+def test_tgmm_sums_to_dense_when_groups_cover_all_rows(tgmm_kernel):
     m, k, n = 384, 128, 256
     sizes = np.array([100, 84, 200], np.int32)
     lhs = W.normal((m, k), 1.0, 51, DEV)
@@ -194,6 +201,22 @@ def test_tgmm_sums_to_dense_when_groups_cover_all_rows():
     out = G.tgmm(lhs, dout, _gs(sizes))
     dense = lhs.double().T @ dout.double()
     assert torch.allclose(out.double().sum(0), dense, rtol=1e-4, atol=1e-3)
+
+
+def test_tgmm_pair_matches_single_sm_kernel(monkeypatch):
+    # k = 392 (one full 256-wide pair tile, then 136: the second CTA holds 8 columns), n = 136
+    sizes = np.array([130, 0, 1, 257, 64, 48], np.int32)
+    lhs = W.normal((520, 392), 1.0, 61, DEV)
+    dout = W.normal((520, 136), 1.0, 62, DEV)
+    outs = {}
+    for kern in ("pair", "single"):
+        monkeypatch.setenv("GMM_TGMM_KERNEL", kern)
+        outs[kern] = G.tgmm(lhs, dout, _gs(sizes))
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = oracle_tgmm(lhs, dout, sizes)
+    for kern, out in outs.items():
+        check_close(out, ref, mag, f"tgmm {kern}")
 
 
 # ------------------------------------------------ SM-pair kernel (>= 192 rows per group on average)
