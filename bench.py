@@ -405,6 +405,13 @@ def _ncu_fp8_decode(torch, G, W, dev):
     return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"])
 
 
+def _ncu_decode_int4(torch, G, W, dev):
+    fd = W.fp8_decode(dev, fmt="int4")
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
+    return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"],
+                         rhs_format="int4")
+
+
 def _ncu_moe128_wi(torch, G, W, dev):
     mo = W.moe128(dev, which=("lhs", "wi"))
     gs = torch.tensor(mo["group_sizes"], dtype=torch.int32, device=dev)
@@ -413,7 +420,7 @@ def _ncu_moe128_wi(torch, G, W, dev):
 
 
 NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode,
-             "moe128_wi": _ncu_moe128_wi}
+             "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4}
 
 
 def run_ncu_case(name):

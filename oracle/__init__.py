@@ -27,7 +27,7 @@ import threading
 
 import numpy as np
 
-BF16, F32, E4M3, E5M2, INT8, INT4, UINT4, E2M1 = 0, 1, 2, 3, 4, 5, 6, 7
+BF16, F32, E4M3, E5M2, INT8, INT4, UINT4, E2M1, E8M0 = 0, 1, 2, 3, 4, 5, 6, 7, 8
 PACKED = (INT4, UINT4, E2M1)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +56,11 @@ def _load():
             lib.oracle_gmm.argtypes = [P, I, I64, I64, P, I, I32, I64, I, P, I32, I32, P, I32, P, I,
                                        P, I64, P, P, I]
             lib.oracle_gmm.restype = I
+            lib.oracle_gmm_ex.argtypes = [P, I, I64, I64, P, I, I32, I64, I, P, I32, I32, P, I, I32, P, I32, P, I,
+                                          P, I64, P, P, I]
+            lib.oracle_gmm_ex.restype = I
+            lib.oracle_quantize_e4m3.argtypes = [P, I64, I64, I64, P, P]
+            lib.oracle_quantize_e4m3.restype = I
             lib.oracle_tgmm.argtypes = [P, I, I64, I64, P, I, I64, P, I32, P, I64, P, P, I]
             lib.oracle_tgmm.restype = I
             lib.oracle_group_offsets.argtypes = [P, I32, I64, P]
@@ -102,11 +107,21 @@ def group_offsets(group_sizes: np.ndarray, m: int) -> np.ndarray:
 
 
 def gmm(lhs, rhs, group_sizes, *, transpose_rhs=True, group_offset=0, rhs_scale=None,
-        rhs_bias=None, rows=None, lhs_dtype=None, rhs_dtype=None, bias_dtype=None, threads=0):
-    """Forward grouped matmul in fp64.  Returns (ref, mag), each [rows, n]."""
+        rhs_bias=None, rows=None, lhs_dtype=None, rhs_dtype=None, bias_dtype=None, lhs_scale=None,
+        threads=0):
+    """Forward grouped matmul in fp64.  Returns (ref, mag), each [rows, n].
+
+    rhs_scale: f32 [L, nb, 1, n], or uint8 E8M0 codes of that shape.  lhs_scale: None or f32
+    [m, num_lhs_blocks] (per-token-group activation scales)."""
     lhs, rhs, bias = _c(lhs), _c(rhs), _c(rhs_bias)
     gs = np.ascontiguousarray(group_sizes, dtype=np.int32)
-    scale = None if rhs_scale is None else np.ascontiguousarray(rhs_scale, dtype=np.float32)
+    scale_code = F32
+    if rhs_scale is not None and np.asarray(rhs_scale).dtype == np.uint8:
+        scale = np.ascontiguousarray(rhs_scale)
+        scale_code = E8M0
+    else:
+        scale = None if rhs_scale is None else np.ascontiguousarray(rhs_scale, dtype=np.float32)
+    lscale = None if lhs_scale is None else np.ascontiguousarray(lhs_scale, dtype=np.float32)
     m, k = lhs.shape
     L = rhs.shape[0]
     rcode = _dtype_code(rhs, rhs_dtype)
@@ -116,9 +131,10 @@ def gmm(lhs, rhs, group_sizes, *, transpose_rhs=True, group_offset=0, rhs_scale=
     count = m if rows_arr is None else rows_arr.shape[0]
     ref = np.zeros((count, n), dtype=np.float64)
     mag = np.zeros((count, n), dtype=np.float64)
-    rc = _load().oracle_gmm(
+    rc = _load().oracle_gmm_ex(
         _ptr(lhs), _dtype_code(lhs, lhs_dtype), m, k, _ptr(rhs), rcode, L, n,
-        int(bool(transpose_rhs)), _ptr(gs), gs.shape[0], int(group_offset), _ptr(scale), nb,
+        int(bool(transpose_rhs)), _ptr(gs), gs.shape[0], int(group_offset), _ptr(scale), scale_code, nb,
+        _ptr(lscale), 0 if lscale is None else lscale.shape[1],
         _ptr(bias), 0 if bias is None else _dtype_code(bias, bias_dtype), _ptr(rows_arr), count,
         _ptr(ref), _ptr(mag), int(threads))
     if rc != 0:
@@ -142,6 +158,18 @@ def tgmm(lhs, dout, group_sizes, *, k_rows=None, lhs_dtype=None, dout_dtype=None
     if rc != 0:
         raise ValueError("oracle_tgmm rejected its arguments")
     return ref, mag
+
+
+def quantize_e4m3(x_bf16_bits: np.ndarray, group: int = 128):
+    """Per-token-group e4m3 quantisation of bf16 activations [m, k] (stored bits, uint16).
+    Returns (codes uint8 [m, k], scales f32 [m, k / group])."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    m, k = x.shape
+    q = np.zeros((m, k), np.uint8)
+    sc = np.zeros((m, k // group), np.float32)
+    if _load().oracle_quantize_e4m3(_ptr(x), m, k, group, _ptr(q), _ptr(sc)) != 0:
+        raise ValueError("bad quantisation arguments")
+    return q, sc
 
 
 def decode(stored: np.ndarray, dtype: int | None = None) -> np.ndarray:

@@ -54,7 +54,8 @@ namespace {
 // Stored formats.  The 4-bit ones hold two values per byte, the even-indexed
 // value in the low nibble; element i of such an array is nibble i % 2 of byte
 // i / 2.
-enum { DT_BF16 = 0, DT_F32 = 1, DT_E4M3 = 2, DT_E5M2 = 3, DT_INT8 = 4, DT_INT4 = 5, DT_UINT4 = 6, DT_E2M1 = 7 };
+enum { DT_BF16 = 0, DT_F32 = 1, DT_E4M3 = 2, DT_E5M2 = 3, DT_INT8 = 4, DT_INT4 = 5, DT_UINT4 = 6, DT_E2M1 = 7,
+       DT_E8M0 = 8 /* scales only */ };
 
 // bfloat16: the top 16 bits of an IEEE binary32.
 double decode_bf16(uint16_t bits) {
@@ -131,6 +132,36 @@ double load(const void* base, int dtype, int64_t idx) {
 
 bool valid_dtype(int d) { return d >= DT_BF16 && d <= DT_E2M1; }
 
+// E8M0 block scale (page "gemm_quant.rs", widen_block_scale_f32): byte e is
+// 2^(e - 127), except that 255 is 0.
+double decode_e8m0(uint8_t e) { return e == 255 ? 0.0 : std::ldexp(1.0, int(e) - 127); }
+
+// A scale value stored as f32 or E8M0.
+double load_scale(const void* base, int dtype, int64_t idx) {
+  if (dtype == DT_E8M0) return decode_e8m0(static_cast<const uint8_t*>(base)[idx]);
+  return double(static_cast<const float*>(base)[idx]);
+}
+
+// Nearest e4m3fn value to y with ties to the even code, saturating at +-448
+// (|y| above 448 gives 448); NaN gives the NaN code.  Found by comparing y with
+// every finite magnitude of the format (format definition above).
+uint8_t encode_e4m3_rne_sat(double y) {
+  if (std::isnan(y)) return 0x7F;
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  const double a = std::fabs(y);
+  uint8_t best = 0;
+  double best_d = HUGE_VAL;
+  for (int code = 0; code <= 0x7E; ++code) {
+    const double v = decode_e4m3fn(uint8_t(code));
+    const double d = std::fabs(a - v);
+    if (d < best_d || (d == best_d && (code & 1) == 0)) {
+      best = uint8_t(code);
+      best_d = d;
+    }
+  }
+  return sign | best;
+}
+
 int resolve_threads(int threads) {
   if (threads > 0) return threads;
   unsigned hc = std::thread::hardware_concurrency();
@@ -194,18 +225,29 @@ void oracle_group_offsets(const int32_t* group_sizes, int32_t num_groups, int64_
 //   rows       NULL: compute every row 0..m-1; else the listed row indices
 //   ref, mag   [num_rows, n] fp64 outputs (num_rows = m when rows is NULL)
 // Returns 0, or -1 on an argument it cannot interpret.
-int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
-               int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
-               int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_blocks,
-               const void* rhs_bias, int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref,
-               double* mag, int threads) {
+// The same with activation scales and a choice of weight-scale storage (page
+// "gemm_quant.rs": the W8A8 GEMM multiplies each 128-wide K-group's products by
+// a_scale[m, g], and block scales may be stored as E8M0):
+//   lhs_scale        NULL or f32 [m, num_lhs_blocks]; lhs block j covers
+//                    k in [j*k/num_lhs_blocks, (j+1)*k/num_lhs_blocks), and
+//                    lhs[r, kk] counts as lhs_scale[r, j] * lhs[r, kk]
+//   rhs_scale_dtype  DT_F32 or DT_E8M0 for rhs_scale
+int oracle_gmm_ex(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                  int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                  int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int rhs_scale_dtype,
+                  int32_t num_blocks, const float* lhs_scale, int32_t num_lhs_blocks, const void* rhs_bias,
+                  int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref, double* mag, int threads) {
   if (!valid_dtype(lhs_dtype) || !valid_dtype(rhs_dtype)) return -1;
   if (rhs_bias && !valid_dtype(bias_dtype)) return -1;
+  if (rhs_scale && rhs_scale_dtype != DT_F32 && rhs_scale_dtype != DT_E8M0) return -1;
   if (m < 0 || k < 0 || n < 0 || num_local_groups < 0 || num_total_groups < 0) return -1;
   if (group_offset < 0 || group_offset + num_local_groups > num_total_groups) return -1;
   const int32_t nb = rhs_scale ? num_blocks : 1;
   if (nb <= 0 || (k % nb) != 0) return -1;
   const int64_t block = nb ? k / nb : k;
+  const int32_t nlb = lhs_scale ? num_lhs_blocks : 1;
+  if (nlb <= 0 || (k % nlb) != 0) return -1;
+  const int64_t lblock = k / nlb;
 
   std::vector<int64_t> offs;
   group_offsets(group_sizes, num_total_groups, m, offs);
@@ -222,7 +264,10 @@ int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void*
     }
     const int64_t gl = g - group_offset;  // index into the local rhs slice
     std::vector<double> a(static_cast<size_t>(k));
-    for (int64_t kk = 0; kk < k; ++kk) a[kk] = load(lhs, lhs_dtype, r * k + kk);
+    for (int64_t kk = 0; kk < k; ++kk) {
+      a[kk] = load(lhs, lhs_dtype, r * k + kk);
+      if (lhs_scale) a[kk] *= double(lhs_scale[r * nlb + kk / lblock]);
+    }
     for (int64_t c = 0; c < n; ++c) {
       double acc = 0.0, acc_abs = 0.0;
       for (int32_t b = 0; b < nb; ++b) {
@@ -233,7 +278,7 @@ int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void*
           part += a[kk] * w;
           part_abs += std::fabs(a[kk] * w);
         }
-        const double s = rhs_scale ? double(rhs_scale[(gl * nb + b) * n + c]) : 1.0;
+        const double s = rhs_scale ? load_scale(rhs_scale, rhs_scale_dtype, (gl * nb + b) * n + c) : 1.0;
         acc += s * part;
         acc_abs += std::fabs(s) * part_abs;
       }
@@ -246,6 +291,51 @@ int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void*
       mag_row[c] = acc_abs;
     }
   });
+  return 0;
+}
+
+int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+               int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+               int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_blocks,
+               const void* rhs_bias, int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref,
+               double* mag, int threads) {
+  return oracle_gmm_ex(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                       num_total_groups, group_offset, rhs_scale, DT_F32, num_blocks, nullptr, 0, rhs_bias,
+                       bias_dtype, rows, num_rows, ref, mag, threads);
+}
+
+// Per-token-group activation quantisation (page "gemm_quant.rs",
+// per_token_group_quant_fp8: A_fp8 [M, K] e4m3 and a_scale [M, K/128] f32 from
+// bf16 activations).  The page prints no formula; the reading taken here: for
+// each row r and each group j of `group` consecutive k,
+//   amax = max |x|  (NaN if any x is NaN),
+//   scale[r, j] = amax / 448 in fp32 (448 is e4m3fn's largest value), or 1 when
+//                 amax is 0,
+//   q[r, kk] = e4m3fn nearest to x / scale[r, j] (the quotient formed in fp32),
+//              ties to even, saturating at +-448.
+// The fp32 steps are IEEE single-precision operations, as the kernel's are: the
+// codes are fixed by those fp32 values.
+int oracle_quantize_e4m3(const uint16_t* x, int64_t m, int64_t k, int64_t group, uint8_t* q, float* scale) {
+  if (m < 0 || k < 0 || group <= 0 || (k % group) != 0) return -1;
+  const int64_t ng = k / group;
+  for (int64_t r = 0; r < m; ++r) {
+    for (int64_t j = 0; j < ng; ++j) {
+      float amax = 0.f;
+      bool nan = false;
+      for (int64_t kk = j * group; kk < (j + 1) * group; ++kk) {
+        const float v = float(decode_bf16(x[r * k + kk]));
+        if (std::isnan(v)) nan = true;
+        amax = std::max(amax, std::fabs(v));
+      }
+      if (nan) amax = std::nanf("");
+      const float s = amax == 0.f ? 1.f : amax / 448.f;
+      scale[r * ng + j] = s;
+      for (int64_t kk = j * group; kk < (j + 1) * group; ++kk) {
+        const float y = float(decode_bf16(x[r * k + kk])) / s;
+        q[r * k + kk] = encode_e4m3_rne_sat(double(y));
+      }
+    }
+  }
   return 0;
 }
 
@@ -284,6 +374,10 @@ int oracle_tgmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void
 
 // Decodes `count` stored values of `dtype` into fp64 (used by the format pins).
 int oracle_decode(const void* src, int dtype, int64_t count, double* dst) {
+  if (dtype == DT_E8M0) {
+    for (int64_t i = 0; i < count; ++i) dst[i] = decode_e8m0(static_cast<const uint8_t*>(src)[i]);
+    return 0;
+  }
   if (!valid_dtype(dtype)) return -1;
   for (int64_t i = 0; i < count; ++i) dst[i] = load(src, dtype, i);
   return 0;

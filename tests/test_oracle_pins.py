@@ -406,3 +406,70 @@ def test_rejects_bad_arguments():
         oracle.gmm(lhs, w, sizes, group_offset=3)  # 3 + 5 local groups > 5 total
     with pytest.raises(ValueError):
         oracle.gmm(lhs, w, sizes, rhs_scale=np.ones((5, 3, 1, 16), np.float32))  # k=32 not divisible by 3
+
+
+# ------------------------------------------------------------------ W8A8 pieces
+def test_e8m0_scale_codes():
+    codes = np.array([0, 1, 126, 127, 128, 200, 254, 255], np.uint8)
+    got = oracle.decode(codes, oracle.E8M0)
+    expect = [2.0 ** -127, 2.0 ** -126, 0.5, 1.0, 2.0, 2.0 ** 73, 2.0 ** 127, 0.0]
+    np.testing.assert_array_equal(got, expect)
+
+
+def test_lhs_scale_and_e8m0_rhs_scale_against_brute_force():
+    rng = np.random.default_rng(13)
+    m, k, n, G, nb, nlb = 12, 256, 8, 2, 2, 2
+    sizes = [5, 7]
+    codes = rng.integers(0, 256, (m, k)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    lhs_v = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    a_scale = rng.uniform(0.001, 0.01, (m, nlb)).astype(np.float32)
+    w = rand_bf16(rng, (G, n, k), 0.5)
+    e8 = rng.integers(120, 135, (G, nb, 1, n)).astype(np.uint8)
+    e8[0, 0, 0, 3] = 255  # decodes to 0
+    s_v = np.where(e8 == 255, 0.0, 2.0 ** (e8.astype(np.float64) - 127))
+    ref, _ = oracle.gmm(codes, w, np.array(sizes), rhs_scale=e8, lhs_scale=a_scale, lhs_dtype=oracle.E4M3)
+    scaled_lhs = lhs_v * np.repeat(a_scale.astype(np.float64), k // nlb, axis=1)
+    exp = brute_force_gmm(scaled_lhs, bf16_values(w), sizes, True, scale=s_v)
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-12)
+
+
+def _bf16_bits(values):
+    return torch.tensor(values, dtype=torch.float32).to(torch.bfloat16).view(torch.uint16).numpy()
+
+
+def test_quantize_ties_to_even_and_saturation():
+    # amax 448 makes the scale exactly 1, so x / scale = x: 1.0625 lies between 1 and 1.125 (even: 1.0),
+    # 1.1875 between 1.125 and 1.25 (even: 1.25), 248 between 240 and 256 (even: 256)
+    x = _bf16_bits([[448.0, 1.0625, 1.1875, -1.0625, 248.0, 0.0, -448.0, 3.0]])
+    q, s = oracle.quantize_e4m3(x, group=8)
+    assert s.tolist() == [[1.0]]
+    assert q.tolist() == [[0x7E, 0x38, 0x3A, 0xB8, 0x78, 0x00, 0xFE, 0x44]]
+
+
+def test_quantize_matches_torch_rounding_and_error_bound():
+    rng = np.random.default_rng(14)
+    m, k = 16, 512
+    x = (rng.standard_normal((m, k)) * np.exp2(rng.integers(-6, 7, (m, 1)))).astype(np.float32)
+    x[3, 128:256] = 0.0                                  # an all-zero group
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.uint16).numpy()
+    q, s = oracle.quantize_e4m3(bits, group=128)
+    xv = bf16_values(bits)
+    assert s[3, 1] == 1.0 and (q[3, 128:256] == 0).all()
+    # the scale is amax / 448 in fp32; the largest element of each group maps to +-448
+    amax = np.abs(xv).reshape(m, 4, 128).max(axis=2).astype(np.float32)
+    np.testing.assert_array_equal(s[amax > 0], (amax / np.float32(448.0))[amax > 0])
+    y = (xv.astype(np.float32) / np.repeat(s, 128, axis=1)).astype(np.float32)
+    ok = np.abs(y) <= 448.0
+    lib = torch.from_numpy(y[ok]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(q[ok], lib)
+    qv = oracle.decode(q).astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1)
+    bound = np.maximum(np.abs(xv) * 2.0 ** -4, np.repeat(s.astype(np.float64), 128, axis=1) * 2.0 ** -10)
+    assert (np.abs(qv - xv) <= bound * (1 + 1e-9)).all()
+
+
+def test_quantize_nan_group():
+    x = _bf16_bits([[1.0, float("nan"), 2.0, 3.0, 1.0, 2.0, 3.0, 4.0]])
+    q, s = oracle.quantize_e4m3(x, group=4)
+    assert np.isnan(s[0, 0]) and s[0, 1] == np.float32(4.0) / np.float32(448.0)
+    assert (q[0, :4] & 0x7F == 0x7F).all()
