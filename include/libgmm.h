@@ -48,7 +48,9 @@ enum {
   /* 4-bit formats: two values per byte, the even-indexed value in the low nibble */
   GMM_DTYPE_INT4 = 5,  /* two's complement, -8 .. 7 */
   GMM_DTYPE_UINT4 = 6, /* 0 .. 15 */
-  GMM_DTYPE_E2M1 = 7   /* float4_e2m1fn: values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives */
+  GMM_DTYPE_E2M1 = 7,  /* float4_e2m1fn: values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives */
+  /* block scales only (gmm_ex rhs_scale): byte e is 2^(e - 127), 0 is 2^-127, 255 is 0 */
+  GMM_DTYPE_E8M0 = 8
 };
 
 /* Status codes returned by every entry point. */
@@ -179,6 +181,44 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
                       int keep_other_rows, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gmm_ex: gmm(), gmm_into() and gmm_device_offset() in one call, plus the W8A8
+ * form (page "gemm_quant.rs", fp8_gemm_t_blockscaled: C = bf16(sum over 128-wide
+ * K-groups g of the e4m3 MMA over g times a_scale[row, g] times the weight's
+ * block scale)) and E8M0 weight scales (page "gemm_quant.rs",
+ * widen_block_scale_f32).
+ *
+ *   out[r, c] = sum_b s[g', b, c] * sum_{kk in block b} a(r, kk) * W(g', c, kk) + bias[g', c]
+ *   with a(r, kk) = lhs[r, kk] for bf16 lhs, and lhs_scale[r, j] * lhs[r, kk] (j the lhs
+ *   block holding kk; lhs_scale NULL counts as 1) for e4m3 lhs.
+ *
+ *   lhs_dtype        GMM_DTYPE_BF16, or GMM_DTYPE_E4M3 with rhs_dtype one of the 8- and 4-bit
+ *                    weight formats (bf16 weights: GMM_ERR_DTYPE).
+ *   lhs_scale        e4m3 lhs only (else GMM_ERR_DTYPE): NULL or device f32 [m, num_lhs_blocks],
+ *                    4-byte aligned; lhs block j covers kk in [j*k/nlb, (j+1)*k/nlb) and
+ *                    (k / num_lhs_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  The pages' layout is
+ *                    num_lhs_blocks = k / 128 (gmm_quantize_e4m3 with group 128).
+ *   group_offset_dev NULL: group_offset is used as in gmm(); else read from device memory as in
+ *                    gmm_device_offset() (group_offset ignored).
+ *   rhs_scale        NULL or device [num_local_groups, num_quant_blocks, 1, n] of
+ *                    rhs_scale_dtype: GMM_DTYPE_F32, or GMM_DTYPE_E8M0 (one byte each; 8- and
+ *                    4-bit weights only, else GMM_ERR_DTYPE); 16-byte aligned.  A weight scale of
+ *                    the pages' [n / 128, k / 128] layout for one group is s[b, 0, c] =
+ *                    b_scale[c / 128, b].
+ *   keep_other_rows  0: rows outside the local groups are set to 0 (gmm); 1: they keep the
+ *                    caller's contents (gmm_into).
+ *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k
+ *   sub-tile is one e4m3 MMA per token row (exact products, fp32 sums), folded in fp32 as
+ *   acc += s[g', b, c] * lhs_scale[r, j] * D.  GMM_E4M3_KERNEL = decode with e4m3 lhs or
+ *   E8M0 scales: GMM_ERR_DTYPE.
+ */
+int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_lhs_blocks, int64_t m, int64_t k,
+           const void* rhs, int rhs_dtype, int32_t num_local_groups, int64_t n, int transpose_rhs,
+           const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
+           const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
+           const void* rhs_bias, int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/*
  * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS
  * gmm_v2 kernel ...", Context section; gmm.py make_group_metadata docstring on
  * visiting empty groups so that their output is zeroed).
@@ -255,6 +295,24 @@ int gmm_noalloc(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void
                 int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
                 int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
                 const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* stream);
+
+/*
+ * Per-token-group e4m3 quantisation of bf16 activations, the activation side of
+ * the W8A8 path (page "gemm_quant.rs", per_token_group_quant_fp8: A_fp8 [M, K]
+ * e4m3 and a_scale [M, K/128] f32).  The page prints no formula; this library's
+ * reading, for each row r and group j of `group` consecutive k:
+ *   scale[r, j] = max |x| / 448 (fp32 IEEE division; 1 when the maximum is 0;
+ *                 NaN when a value is NaN),
+ *   q[r, kk]    = e4m3fn nearest to x / scale[r, j] (the quotient an fp32 IEEE
+ *                 division), ties to even, saturating at +-448.
+ *   x      device bf16 [m, k] (x_dtype GMM_DTYPE_BF16), 16-byte aligned
+ *   q      device e4m3fn [m, k], 16-byte aligned
+ *   scale  device f32 [m, k / group], 4-byte aligned
+ *   group  64, 128 or 256; k % group == 0 (else GMM_ERR_SHAPE)
+ * Asynchronous on `stream`.
+ */
+int gmm_quantize_e4m3(const void* x, int x_dtype, int64_t m, int64_t k, int64_t group, void* q, float* scale,
+                      void* stream);
 
 /* ------------------------------------------------------------------ tiling table
  * The pages let `tiling` be a callable that looks the problem dimensions up in a

@@ -22,13 +22,13 @@ import threading
 
 import torch
 
-__all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "tune", "tuning_set", "tuning_get", "tuning_clear",
+__all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "quantize_e4m3", "tune", "tuning_set", "tuning_get", "tuning_clear",
            "tuning_save", "tuning_load", "tuning_rows_log2", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
            "DEVERR_NEGATIVE_GROUP_SIZE", "DEVERR_GROUP_SIZES_EXCEED_M", "DEVERR_TIMEOUT"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
 
-DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1 = range(8)
+DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1, DTYPE_E8M0 = range(9)
 # Packed 4-bit weight formats (uint8 tensors [L, n, k / 2], even k in the low nibble), by name.
 PACKED_FORMATS = {"int4": DTYPE_INT4, "uint4": DTYPE_UINT4, "e2m1": DTYPE_E2M1}
 # bf16 forward kernels, as the tiling table names them.
@@ -55,6 +55,9 @@ SIGNATURES = {
                            _SZ, _P], _I),
     "tgmm_local": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
+    "gmm_quantize_e4m3": ([_P, _I, _I64, _I64, _I64, _P, _P, _P], _I),
+    "gmm_ex": ([_P, _I, _P, _I32, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _P, _I, _I32, _P, _I, _P, _I,
+                _I, _P, _SZ, _P], _I),
     "gmm_tuning_set": ([_I32, _I64, _I64, _I32, _I, _I, _I, _I], _I),
     "gmm_tuning_get": ([_I32, _I64, _I64, _I32, _I, _I, _IP, _IP], _I),
     "gmm_tuning_clear": ([], _I),
@@ -127,7 +130,7 @@ def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out, out_dtype,
-              workspace, stream, rhs_format):
+              workspace, stream, rhs_format, lhs_scale=None):
     lib = load_library()
     _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
     if group_sizes.dtype != torch.int32:
@@ -155,6 +158,29 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
         nb = rhs_scale.shape[1]
     if rhs_bias is not None:
         _dev(rhs_bias, "rhs_bias")
+    e8m0 = rhs_scale is not None and rhs_scale.dtype == torch.uint8
+    if lhs.dtype == torch.float8_e4m3fn or lhs_scale is not None or e8m0:
+        # e4m3 activations with their scales, or E8M0 weight scales: gmm_ex
+        if lhs_scale is not None:
+            _dev(lhs_scale, "lhs_scale")
+            if lhs_scale.dtype != torch.float32 or lhs_scale.dim() != 2 or lhs_scale.shape[0] != m:
+                raise ValueError("lhs_scale must be float32 [m, num_lhs_blocks]")
+        dev_off = isinstance(group_offset, torch.Tensor)
+        if dev_off:
+            _dev(group_offset, "group_offset")
+            if group_offset.dtype != torch.int32 or group_offset.numel() != 1:
+                raise TypeError("a tensor group_offset must be one int32 on the device")
+        rc = lib.gmm_ex(lhs.data_ptr(), _code(lhs), None if lhs_scale is None else lhs_scale.data_ptr(),
+                        0 if lhs_scale is None else lhs_scale.shape[1], m, k, rhs.data_ptr(), rcode, rhs.shape[0], n,
+                        int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0],
+                        0 if dev_off else int(group_offset), group_offset.data_ptr() if dev_off else None,
+                        None if rhs_scale is None else rhs_scale.data_ptr(), DTYPE_E8M0 if e8m0 else DTYPE_F32, nb,
+                        None if rhs_bias is None else rhs_bias.data_ptr(),
+                        0 if rhs_bias is None else _code(rhs_bias), out.data_ptr(), _code(out),
+                        int(fn == "gmm_into"), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+        if rc != 0:
+            raise GmmError("gmm_ex", rc)
+        return out
     head = (lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), rcode, rhs.shape[0], n, int(bool(transpose_rhs)),
             group_sizes.data_ptr(), group_sizes.shape[0])
     tail = (None if rhs_scale is None else rhs_scale.data_ptr(), nb,
@@ -176,24 +202,26 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
 
 
 def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
-        out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None):
+        out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None, lhs_scale=None):
     """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
     for each row r of local group g; all other rows of out are zero.  group_offset is an int, or a
     one-element int32 CUDA tensor that the kernel reads when it runs.  rhs is bf16, float8_e4m3fn,
     float8_e5m2 or int8, or a uint8 tensor [G_local, n, k / 2] of packed 4-bit weights with
-    rhs_format = "int4", "uint4" or "e2m1"."""
+    rhs_format = "int4", "uint4" or "e2m1".  rhs_scale is float32 [G_local, nb, 1, n], or uint8
+    E8M0 codes of that shape.  lhs may be float8_e4m3fn (W8A8) with lhs_scale float32
+    [m, num_lhs_blocks] (quantize_e4m3's scales)."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out_dtype, workspace, stream, rhs_format)
+                     out_dtype, workspace, stream, rhs_format, lhs_scale)
 
 
 def gmm_into(lhs, rhs, group_sizes, out, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0,
-             workspace=None, stream=None, rhs_format=None):
+             workspace=None, stream=None, rhs_format=None, lhs_scale=None):
     """As gmm, but only the local groups' rows of `out` are written; every other row keeps the
     caller's contents (the existing-output mode)."""
     if out is None:
         raise ValueError("gmm_into needs an output tensor")
     return _gmm_call("gmm_into", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out.dtype, workspace, stream, rhs_format)
+                     out.dtype, workspace, stream, rhs_format, lhs_scale)
 
 
 def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, out=None, out_dtype=torch.float32,
@@ -244,6 +272,19 @@ def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=No
     if rc != 0:
         raise GmmError("tgmm", rc)
     return out
+
+
+def quantize_e4m3(x, group=128, out=None, scale=None, stream=None):
+    """Per-token-group e4m3 quantisation of bf16 activations [m, k]: returns (q float8_e4m3fn
+    [m, k], scale f32 [m, k / group])."""
+    _dev(x, "x")
+    m, k = x.shape
+    q = out if out is not None else torch.empty((m, k), dtype=torch.float8_e4m3fn, device=x.device)
+    sc = scale if scale is not None else torch.empty((m, k // group), dtype=torch.float32, device=x.device)
+    _dev(q, "out"), _dev(sc, "scale")
+    _check("gmm_quantize_e4m3", load_library().gmm_quantize_e4m3(x.data_ptr(), _code(x), m, k, group, q.data_ptr(),
+                                                                 sc.data_ptr(), _stream(x.device, stream)))
+    return q, sc
 
 
 def tuning_rows_log2(m: int, num_total_groups: int) -> int:

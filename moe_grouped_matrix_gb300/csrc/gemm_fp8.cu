@@ -5,9 +5,10 @@
 namespace gmmk {
 
 cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream) {
+  if (p.lhs_e4m3) return launch_fp8_a8(p, weight_format, out_f32, grid, stream);
   switch (weight_format) {
-    case kWeightE4M3: return fp8::launch_format<fp8::WFmt::kE4M3>(p, out_f32, grid, stream);
-    case kWeightE5M2: return fp8::launch_format<fp8::WFmt::kE5M2>(p, out_f32, grid, stream);
+    case kWeightE4M3: return fp8::launch_format<fp8::WFmt::kE4M3, false>(p, out_f32, grid, stream);
+    case kWeightE5M2: return fp8::launch_format<fp8::WFmt::kE5M2, false>(p, out_f32, grid, stream);
     default: return launch_fp8_converted(p, weight_format, out_f32, grid, stream);
   }
 }

@@ -74,7 +74,7 @@ constexpr uint32_t RT_STRIP = BT * 128;  // 64 k of bf16 for 32 token rows
 constexpr uint32_t RT_BOX = 16 * 128;    // one {64 k, 16 rows} box
 constexpr uint32_t B_SUB = 2 * BT * KQ;  // e4m3 operand sub-tile: 64 rows x 128 bytes
 
-template <WFmt F>
+template <WFmt F, bool kA8>
 struct Cfg {
   static constexpr bool kNibble = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
   static constexpr bool kConv = kNibble || F == WFmt::kInt8;  // weights rewritten in shared memory
@@ -88,8 +88,11 @@ struct Cfg {
   static constexpr int RAWST = 4;
   static constexpr int CST = kConv ? 2 : 0;
   static constexpr uint32_t CONV_BYTES = QPS * PASSES * A_SUB;
-  static constexpr int RTS = 2, BST = 2, NSC = 8;
   static constexpr int NACC = QPS == 2 ? 4 : 8;  // TMEM accumulator slots, one per step
+  // e4m3 activations (kA8) come by TMA straight into the operand ring, which is
+  // then freed through the step-done ring; bf16 ones pass the token split.
+  static constexpr int RTS = kA8 ? 0 : 2, BST = kA8 ? 4 : 2, NSC = 8;
+  static constexpr int SC_PER = kA8 ? QPS * BT : BT;  // token scales per step: per sub-tile with kA8
   static constexpr int SLOT_COLS = QPS * 2 * BT;  // sub-tile h: [slot * SLOT_COLS + 64 h, + 2 T8)
   // One barrier per step records that the step's MMAs have completed (a single
   // tcgen05.commit): it frees the step's A stage (raw for e4m3 / e5m2,
@@ -97,8 +100,9 @@ struct Cfg {
   // the epilogue; step j uses index j % NDONE.
   static constexpr int NDONE = NACC;
   static constexpr uint32_t RT_BYTES = (KS / 64) * RT_STRIP;
-  static constexpr uint32_t B_BYTES = QPS * B_SUB;
-  static constexpr int kConvWarps = 4;                 // token split
+  static constexpr uint32_t B_SUBT = kA8 ? BT * KQ : B_SUB;  // operand sub-tile: 32 or 64 rows
+  static constexpr uint32_t B_BYTES = QPS * B_SUBT;
+  static constexpr int kConvWarps = kA8 ? 1 : 4;       // token split, or the token-scale warp
   static constexpr int kWConvWarps = kConv ? 4 : 0;    // weight rewrite
   static constexpr int kThreads = 192 + 32 * (kConvWarps + kWConvWarps);
 
@@ -107,7 +111,7 @@ struct Cfg {
   static constexpr uint32_t OFF_RT = OFF_CONV + CST * CONV_BYTES;
   static constexpr uint32_t OFF_B = OFF_RT + RTS * RT_BYTES;
   static constexpr uint32_t OFF_SC = OFF_B + BST * B_BYTES;
-  static constexpr uint32_t OFF_CTRL = OFF_SC + NSC * BT * 4;
+  static constexpr uint32_t OFF_CTRL = OFF_SC + NSC * SC_PER * 4;
   static constexpr uint32_t OFF_RAWFULL = OFF_CTRL;
   static constexpr uint32_t OFF_RAWEMPTY = OFF_RAWFULL + 8 * RAWST;
   static constexpr uint32_t OFF_CONVFULL = OFF_RAWEMPTY + 8 * RAWST;
@@ -131,14 +135,15 @@ struct Cfg {
   static_assert(BST <= NDONE && CST <= NDONE, "step-done ring indexing");
   static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(OFF_CONV % 1024 == 0 && OFF_RT % 1024 == 0 && OFF_B % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+  static_assert(OFF_CONV % 1024 == 0 && OFF_RT % 1024 == 0 && OFF_B % 1024 == 0 && B_SUBT % 1024 == 0,
+                "swizzle atoms are 1024-byte aligned");
 };
 
 struct Params {
   const int32_t* group_sizes;
   int32_t num_total_groups, group_offset, num_local_groups;
   int32_t m, n, k;
-  const float* scale;
+  const void* scale;  // f32, or E8M0 bytes when scale_e8m0
   int32_t num_blocks;
   const void* bias;
   int32_t bias_f32;
@@ -146,7 +151,16 @@ struct Params {
   uint32_t* err;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
+  int32_t scale_e8m0;
+  const float* lhs_scale;  // e4m3 activations: NULL or f32 [m, num_lhs_blocks]
+  int32_t num_lhs_blocks;
 };
+
+// An E8M0 block scale as fp32 (page "gemm_quant.rs", widen_block_scale_f32):
+// byte e is 2^(e - 127), the bits e << 23, except that 0 is 2^-127 and 255 is 0.
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+  return e == 255u ? 0.f : __uint_as_float(e == 0u ? 0x00400000u : e << 23);
+}
 
 // Operand rows per half for a chunk of t token rows.
 __device__ __forceinline__ int t8_of(int32_t t) { return t <= 8 ? 8 : (t <= 16 ? 16 : 32); }
@@ -270,11 +284,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&f)[N]) {
   }
 }
 
-template <WFmt F, bool kOutF32>
-__global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
+template <WFmt F, bool kA8, bool kOutF32>
+__global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_rhs,
                     const Params p) {
-  using C = Cfg<F>;
+  using C = Cfg<F, kA8>;
   constexpr int QPS = C::QPS, NACC = C::NACC, NDONE = C::NDONE, NSC = C::NSC;
   int32_t go;
   if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
@@ -311,7 +325,7 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
       mbar_init(rfull_bar(s), 1);
       mbar_init(rempty_bar(s), C::kConvWarps);
     }
-    for (int s = 0; s < C::BST; ++s) mbar_init(bfull_bar(s), C::kConvWarps);
+    for (int s = 0; s < C::BST; ++s) mbar_init(bfull_bar(s), kA8 ? 1 : C::kConvWarps);
     for (int s = 0; s < NSC; ++s) {
       mbar_init(sfull_bar(s), C::kConvWarps);
       mbar_init(sempty_bar(s), 4);
@@ -357,8 +371,11 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // The token ring: bf16 rows for the split (RTS deep), or e4m3 operand rows (BST deep).
+      constexpr int TR = kA8 ? C::BST : C::RTS;
       uint32_t as = 0, aph = 0, rs = 0, rph = 0, apend = 0, rpend = 0;
-      uint32_t apar[C::RAWST], rpar[C::RTS];
+      uint32_t apar[C::RAWST], rpar[TR];
+      uint32_t j = 0;  // steps loaded so far
       bool ok = true;
       for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const GemmTile t = item_of(w);
@@ -389,28 +406,43 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
             as = 0;
             aph ^= 1u;
           }
-          if (!wait_bar(rempty_bar(rs), rph ^ 1u, abort_flag, p.err)) {
-            ok = false;
-            break;
+          if constexpr (kA8) {
+            // e4m3 token rows, one {128 k, 16 rows} box per sub-tile and 16 rows,
+            // straight into operand stage rs once step j - BST's MMAs are done.
+            if (!wait_step_done(j, C::BST)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bfull_bar(rs), uint32_t(rboxes * hq) * RT_BOX);
+            for (int h = 0; h < hq; ++h)
+              for (int rb = 0; rb < rboxes; ++rb)
+                tma_load_2d(sbase + C::OFF_B + rs * C::B_BYTES + h * C::B_SUBT + rb * RT_BOX, &tm_lhs,
+                            bfull_bar(rs), (QPS * ks + h) * KQ, t.row0 + 16 * rb);
+          } else {
+            if (!wait_bar(rempty_bar(rs), rph ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(rfull_bar(rs), uint32_t(rboxes * 2 * hq) * RT_BOX);
+            for (int st = 0; st < 2 * hq; ++st)
+              for (int rb = 0; rb < rboxes; ++rb)
+                tma_load_2d(sbase + C::OFF_RT + rs * C::RT_BYTES + st * RT_STRIP + rb * RT_BOX, &tm_lhs,
+                            rfull_bar(rs), ks * C::KS + 64 * st, t.row0 + 16 * rb);
           }
-          mbar_arrive_expect_tx(rfull_bar(rs), uint32_t(rboxes * 2 * hq) * RT_BOX);
-          for (int st = 0; st < 2 * hq; ++st)
-            for (int rb = 0; rb < rboxes; ++rb)
-              tma_load_2d(sbase + C::OFF_RT + rs * C::RT_BYTES + st * RT_STRIP + rb * RT_BOX, &tm_lhs,
-                          rfull_bar(rs), ks * C::KS + 64 * st, t.row0 + 16 * rb);
           rpar[rs] = rph;
           rpend |= 1u << rs;
-          if (++rs == C::RTS) {
+          if (++rs == TR) {
             rs = 0;
             rph ^= 1u;
           }
+          ++j;
         }
       }
       if (!ok) {
         for (int s = 0; s < C::RAWST; ++s)
           if (apend >> s & 1u) drain_bar(rawfull_bar(s), apar[s]);
-        for (int s = 0; s < C::RTS; ++s)
-          if (rpend >> s & 1u) drain_bar(rfull_bar(s), rpar[s]);
+        for (int s = 0; s < TR; ++s)
+          if (rpend >> s & 1u) drain_bar(kA8 ? bfull_bar(s) : rfull_bar(s), rpar[s]);
       }
     }
   } else if (warp == 1) {
@@ -422,7 +454,8 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
       const int t8 = t8_of(t.row_end - t.row0);
-      const uint32_t idesc = idesc_e4m3(BMW, 2 * t8) | (C::kAType << 7);
+      // N: the h and l rows of the split (2 T8), or the e4m3 token rows (16 or 32).
+      const uint32_t idesc = idesc_e4m3(BMW, kA8 ? max(t8, 16) : 2 * t8) | (C::kAType << 7);
       for (int32_t ks = 0; ks < ksteps; ++ks) {
         const int32_t hq = halves(ks);
         const uint32_t afull = C::kConv ? convfull_bar(as) : rawfull_bar(as);
@@ -434,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           for (int h = 0; h < hq; ++h) {
-            const uint32_t b0 = sbase + C::OFF_B + bs * C::B_BYTES + h * B_SUB;
+            const uint32_t b0 = sbase + C::OFF_B + bs * C::B_BYTES + h * C::B_SUBT;
             const uint32_t d = tmem_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
 #pragma unroll
             for (int pass = 0; pass < C::PASSES; ++pass) {
@@ -483,11 +516,17 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
       const GemmTile t = item_of(w);
       const int32_t col = t.n_tile * BMW + wrow;
       const bool col_ok = col < p.n;
-      const float* srow = p.scale != nullptr ? p.scale + int64_t(t.local_group) * nb * p.n + col : nullptr;
+      const int64_t sidx = int64_t(t.local_group) * nb * p.n + col;  // scale of block 0 for this column
       auto load_scales = [&](int32_t b0, float (&dst)[kPre]) {
 #pragma unroll
-        for (int j = 0; j < kPre; ++j)
-          dst[j] = (srow != nullptr && col_ok && b0 + j < nb) ? __ldg(srow + int64_t(b0 + j) * p.n) : 1.f;
+        for (int j = 0; j < kPre; ++j) {
+          dst[j] = 1.f;
+          if (p.scale != nullptr && col_ok && b0 + j < nb) {
+            const int64_t i = sidx + int64_t(b0 + j) * p.n;
+            dst[j] = p.scale_e8m0 ? e8m0_value(__ldg(static_cast<const uint8_t*>(p.scale) + i))
+                                  : __ldg(static_cast<const float*>(p.scale) + i);
+          }
+        }
       };
       float bias = 0.f;
       if (p.bias != nullptr && col_ok) {
@@ -519,9 +558,15 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
                 }
                 tc_fence_after();
               }
-              const float* ts = tscale + sc * BT;
+              const float* ts = tscale + sc * C::SC_PER + (kA8 ? h * BT : 0);
               const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
-              if constexpr (T8 < 32) {
+              if constexpr (kA8) {
+                // one e4m3 product per token: its T8 columns, times the sub-tile's token scale
+                float d[T8];
+                tmem_ld_cols<T8>(col0, d);
+#pragma unroll
+                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
+              } else if constexpr (T8 < 32) {
                 // h and l columns in one load
                 float d[2 * T8];
                 tmem_ld_cols<2 * T8>(col0, d);
@@ -594,7 +639,42 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
         st_global_v4(static_cast<uint8_t*>(p.out) + byte, 0u, 0u, 0u, 0u);
       }
     }
-  } else if (warp < 10) {
+  } else if (kA8 && warp == 6) {
+    // ---------------------------------------------------------------- token scales
+    // e4m3 activations: per step, the token scale of each of its sub-tiles for
+    // the item's rows (lhs_scale[row, lhs block of the sub-tile], 1 without
+    // lhs_scale, 0 for operand rows past the chunk).
+    const int32_t nlb = p.lhs_scale != nullptr ? p.num_lhs_blocks : 1;
+    const int32_t q_per_lblock = nq / nlb;  // (k / nlb) % 128 == 0 on this path
+    uint32_t sc = 0, scph = 0;
+    bool ok = true;
+    for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const GemmTile t = item_of(w);
+      const int32_t rows = t.row_end - t.row0;
+      for (int32_t ks = 0; ks < ksteps; ++ks) {
+        const int32_t hq = halves(ks);
+        if (!wait_bar(sempty_bar(sc), scph ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        for (int idx = lane; idx < QPS * BT; idx += 32) {
+          const int h = idx / BT, r = idx % BT;
+          float v = 0.f;
+          if (h < hq && r < rows)
+            v = p.lhs_scale != nullptr
+                    ? __ldg(p.lhs_scale + int64_t(t.row0 + r) * nlb + (QPS * ks + h) / q_per_lblock)
+                    : 1.f;
+          tscale[sc * C::SC_PER + idx] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull_bar(sc));
+        if (++sc == NSC) {
+          sc = 0;
+          scph ^= 1u;
+        }
+      }
+    }
+  } else if (!kA8 && warp < 10) {
     // ---------------------------------------------------------------- token split
     // The 128 threads share a step's T8 rows evenly: 128 / T8 adjacent lanes per
     // token row r, each taking the same T8 consecutive k of every sub-tile h of
@@ -714,7 +794,7 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
     // positions.  4-bit: raw chunk 4 h + i (32 codes) of the row becomes A chunks
     // 2 i and 2 i + 1 of sub-tile h.  int8: raw chunk c (16 values) becomes chunk
     // c of the 16 h tile (pass 0) and of the l tile (pass 1).
-    const int r = int(threadIdx.x) - 320;
+    const int r = int(threadIdx.x) - 32 * (6 + C::kConvWarps);
     uint32_t rs = 0, rph = 0, cs = 0;
     uint32_t j = 0;  // steps rewritten so far
     bool ok = true;
@@ -785,21 +865,23 @@ __global__ void __launch_bounds__(Cfg<F>::kThreads, 1)
   }
 }
 
-template <WFmt F, bool kOutF32>
+template <WFmt F, bool kA8, bool kOutF32>
 cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) {
-  auto kern = gemm_fp8_kernel<F, kOutF32>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<F>::SMEM_BYTES));
+  using C = Cfg<F, kA8>;
+  auto kern = gemm_fp8_kernel<F, kA8, kOutF32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
-           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev};
-  kern<<<grid, Cfg<F>::kThreads, Cfg<F>::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
+           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
+           L.lhs_scale, L.num_lhs_blocks};
+  kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }
 
-template <WFmt F>
+// bf16 activations (kA8 false: the exact two-term split) or e4m3 ones (kA8 true).
+template <WFmt F, bool kA8>
 cudaError_t launch_format(const ScaledLaunch& L, bool out_f32, int grid, cudaStream_t stream) {
-  return out_f32 ? launch_format<F, true>(L, grid, stream) : launch_format<F, false>(L, grid, stream);
+  return out_f32 ? launch_format<F, kA8, true>(L, grid, stream) : launch_format<F, kA8, false>(L, grid, stream);
 }
 
 }  // namespace fp8

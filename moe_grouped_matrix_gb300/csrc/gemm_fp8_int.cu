@@ -7,10 +7,10 @@ namespace gmmk {
 cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
                                  cudaStream_t stream) {
   switch (weight_format) {
-    case kWeightInt8: return fp8::launch_format<fp8::WFmt::kInt8>(p, out_f32, grid, stream);
-    case kWeightInt4: return fp8::launch_format<fp8::WFmt::kInt4>(p, out_f32, grid, stream);
-    case kWeightUint4: return fp8::launch_format<fp8::WFmt::kUint4>(p, out_f32, grid, stream);
-    case kWeightE2M1: return fp8::launch_format<fp8::WFmt::kE2M1>(p, out_f32, grid, stream);
+    case kWeightInt8: return fp8::launch_format<fp8::WFmt::kInt8, false>(p, out_f32, grid, stream);
+    case kWeightInt4: return fp8::launch_format<fp8::WFmt::kInt4, false>(p, out_f32, grid, stream);
+    case kWeightUint4: return fp8::launch_format<fp8::WFmt::kUint4, false>(p, out_f32, grid, stream);
+    case kWeightE2M1: return fp8::launch_format<fp8::WFmt::kE2M1, false>(p, out_f32, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

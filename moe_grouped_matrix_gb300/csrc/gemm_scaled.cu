@@ -517,7 +517,8 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
   auto kern = gemm_scaled_kernel<kE4M3, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Layout<kE4M3>::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
+  const auto* scale = static_cast<const float*>(L.scale);
+  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, scale,
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev};
   kern<<<grid, kE4M3 ? 192 + kConvThreads : 192, Layout<kE4M3>::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();

@@ -191,17 +191,31 @@ int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags) {
 
 namespace {
 
+// The arguments only gmm_ex takes: activation scales and the storage of rhs_scale.
+struct ExtArgs {
+  const float* lhs_scale = nullptr;
+  int32_t num_lhs_blocks = 0;
+  int rhs_scale_dtype = GMM_DTYPE_F32;
+};
+
 // Shared body of gmm and gmm_into: zero_rest says whether rows of the
 // groups outside the local slice are written as zero (gmm) or left as the
 // caller filled them (gmm_into).
 int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
              int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
-             int32_t num_total_groups, int32_t group_offset, const float* rhs_scale, int32_t num_quant_blocks,
+             int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int32_t num_quant_blocks,
              const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
              size_t workspace_bytes, void* stream, int32_t zero_rest, const int32_t* group_offset_dev,
-             int forced_kernel = GMM_KERNEL_AUTO, int32_t forced_raster = 0) {
+             int forced_kernel = GMM_KERNEL_AUTO, int32_t forced_raster = 0, const ExtArgs& ext = ExtArgs{}) {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
-  if (lhs_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  // e4m3 activations (W8A8) run on the fp8 kernels only: 8- or 4-bit weights.
+  const bool lhs8 = lhs_dtype == GMM_DTYPE_E4M3;
+  if (lhs_dtype != GMM_DTYPE_BF16 && !lhs8) return GMM_ERR_DTYPE;
+  if (lhs8 && rhs_dtype == GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  if (!lhs8 && ext.lhs_scale != nullptr) return GMM_ERR_DTYPE;
+  const bool scale_e8m0 = ext.rhs_scale_dtype == GMM_DTYPE_E8M0;
+  if (ext.rhs_scale_dtype != GMM_DTYPE_F32 && !scale_e8m0) return GMM_ERR_DTYPE;
+  if (scale_e8m0 && rhs_dtype == GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (rhs_bias != nullptr && bias_dtype != GMM_DTYPE_BF16 && bias_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -220,6 +234,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   const bool scaled_path = quantized || rhs_scale != nullptr;
   if (rhs_scale != nullptr) {
     if (num_quant_blocks < 1 || k % num_quant_blocks != 0) return GMM_ERR_SHAPE;
+  }
+  if (ext.lhs_scale != nullptr) {
+    if (ext.num_lhs_blocks < 1 || k % ext.num_lhs_blocks != 0 || (k / ext.num_lhs_blocks) % 128 != 0)
+      return GMM_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(ext.lhs_scale) % 4 != 0) return GMM_ERR_ALIGN;
   }
   // Block-scaled / e4m3 path: NT layout, k and the quant-block width multiples of 128.
   const int32_t nb = rhs_scale != nullptr ? num_quant_blocks : 1;
@@ -242,10 +261,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     if (items > INT32_MAX) return GMM_ERR_SHAPE;
     gmmk::ScaledLaunch S{};
     {
+      // bf16 rows in {64 k, 16 rows} boxes, e4m3 rows in {128 k, 16 rows} boxes (128 bytes wide either way)
       const uint64_t dims[2] = {uint64_t(k), uint64_t(m)};
-      const uint32_t box[2] = {64, 16};
-      if (int st = make_map(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
+      const uint32_t box[2] = {lhs8 ? 128u : 64u, 16};
+      if (int st = make_map(&S.tm_lhs, lhs8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            lhs8 ? 1 : 2, 2, lhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return st;
     }
     {
@@ -272,6 +292,10 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.err = err;
     S.zero_rest = zero_rest;
     S.group_offset_dev = group_offset_dev;
+    S.scale_e8m0 = scale_e8m0 ? 1 : 0;
+    S.lhs_e4m3 = lhs8 ? 1 : 0;
+    S.lhs_scale = ext.lhs_scale;
+    S.num_lhs_blocks = ext.lhs_scale != nullptr ? ext.num_lhs_blocks : 1;
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     cudaError_t e;
     if (rhs_dtype == GMM_DTYPE_BF16) {
@@ -279,6 +303,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     } else if (rhs_dtype == GMM_DTYPE_E4M3) {
       const int decode = choose_e4m3_decode();
       if (decode < 0) return GMM_ERR_SHAPE;
+      if (decode && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;  // the decoding kernel takes bf16 lhs, f32 scales
       e = decode ? gmmk::launch_scaled(S, true, f32, dev.sms, s) : gmmk::launch_fp8(S, gmmk::kWeightE4M3, f32, dev.sms, s);
     } else {
       const int fmt = rhs_dtype == GMM_DTYPE_E5M2   ? gmmk::kWeightE5M2
@@ -378,6 +403,35 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, 0, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype, workspace,
                   workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset);
+}
+
+int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_lhs_blocks, int64_t m, int64_t k,
+           const void* rhs, int rhs_dtype, int32_t num_local_groups, int64_t n, int transpose_rhs,
+           const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
+           const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
+           const void* rhs_bias, int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  ExtArgs ext;
+  ext.lhs_scale = lhs_scale;
+  ext.num_lhs_blocks = num_lhs_blocks;
+  ext.rhs_scale_dtype = rhs_scale_dtype;
+  return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                  num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype,
+                  workspace, workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset_dev, GMM_KERNEL_AUTO, 0,
+                  ext);
+}
+
+int gmm_quantize_e4m3(const void* x, int x_dtype, int64_t m, int64_t k, int64_t group, void* q, float* scale,
+                      void* stream) {
+  if (x == nullptr || q == nullptr || scale == nullptr) return GMM_ERR_NULL;
+  if (x_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  if (m < 0 || k < 0 || (group != 64 && group != 128 && group != 256) || k % group != 0) return GMM_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || reinterpret_cast<uintptr_t>(scale) % 4 != 0) return GMM_ERR_ALIGN;
+  DeviceInfo dev;
+  if (int st = current_device(&dev)) return st;
+  cudaError_t e = gmmk::launch_quantize_e4m3(x, m, k, group, q, scale, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GMM_OK;
 }
 
 int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,

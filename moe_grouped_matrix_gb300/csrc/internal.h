@@ -60,12 +60,12 @@ cudaError_t launch_tgmm_2sm(const TgmmLaunch& p, bool out_f32, int max_ctas, cud
 // Block-scaled grouped matmul for small groups (decode): rhs e4m3 or bf16
 // [L, n, k], per-(group, k-block, n) fp32 scale, optional bias.
 struct ScaledLaunch {
-  CUtensorMap tm_lhs;  // lhs [m, k] bf16, box {64, 16}
+  CUtensorMap tm_lhs;  // lhs [m, k] bf16, box {64, 16}; e4m3 (lhs_e4m3), box {128, 16}
   CUtensorMap tm_rhs;  // rhs [L, n, k]: e4m3 box {128, 128, 1} / bf16 box {64, 128, 1}
   const int32_t* group_sizes;
   int32_t num_total_groups, group_offset, num_local_groups;
   int32_t m, n, k;
-  const float* scale;  // NULL or [L, nb, 1, n]
+  const void* scale;  // NULL or [L, nb, 1, n], f32 or (scale_e8m0) E8M0 bytes
   int32_t num_blocks;
   const void* bias;
   int32_t bias_f32;
@@ -73,6 +73,10 @@ struct ScaledLaunch {
   uint32_t* err;
   int32_t zero_rest;                // 1: zero rows outside the local groups; 0: leave them as they are
   const int32_t* group_offset_dev;  // NULL, or a device int32 that replaces group_offset
+  int32_t scale_e8m0;               // scale holds E8M0 bytes (fp8 kernels only)
+  int32_t lhs_e4m3;                 // lhs holds e4m3 codes (fp8 kernels only)
+  const float* lhs_scale;           // lhs_e4m3: NULL or f32 [m, num_lhs_blocks]
+  int32_t num_lhs_blocks;
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
@@ -90,7 +94,17 @@ enum WeightFormat : int {
   kWeightE2M1 = 5,
 };
 cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
+// e4m3 activations (lhs_e4m3): the same kernel with the token rows loaded as
+// e4m3 operand tiles and each 128-wide sub-tile scaled by lhs_scale.
+cudaError_t launch_fp8_a8(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
+cudaError_t launch_fp8_a8_packed(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
+                                 cudaStream_t stream);
 cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
+                                 cudaStream_t stream);
+
+// Per-token-group e4m3 quantisation of bf16 activations (quantize.cu); group
+// 64, 128 or 256, k % group == 0.
+cudaError_t launch_quantize_e4m3(const void* x, int64_t m, int64_t k, int64_t group, void* q, float* scale,
                                  cudaStream_t stream);
 
 // Per-shape kernel table (tuning.cu).  kernel: a GMM_KERNEL_* id; raster 0 =

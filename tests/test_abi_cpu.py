@@ -31,7 +31,7 @@ def test_header_declares_the_expected_calls():
     assert declared_functions() == sorted(
         ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error",
          "gmm_noalloc", "gmm_into", "tgmm_local", "gmm_device_offset", "gmm_tuning_set", "gmm_tuning_get",
-         "gmm_tuning_clear", "gmm_tuning_save", "gmm_tuning_load", "gmm_tune"])
+         "gmm_tuning_clear", "gmm_tuning_save", "gmm_tuning_load", "gmm_tune", "gmm_quantize_e4m3", "gmm_ex"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -74,6 +74,41 @@ def call_gmm(lib, fn="gmm", **over):
 @pytest.mark.parametrize("fn", ["gmm", "gmm_into"])
 def test_gmm_host_validation(lib, fn, over, status):
     assert call_gmm(lib, fn, **over) == status
+
+
+def call_gmm_ex(lib, **over):
+    a = dict(lhs=FAKE, lhs_dtype=2, lscale=FAKE, nlb=2, m=256, k=256, rhs=FAKE, rhs_dtype=2, L=4, n=256, trhs=1,
+             gs=FAKE, G=4, go=0, godev=None, scale=FAKE, scale_dtype=8, nb=2, bias=None, bias_dtype=0, out=FAKE,
+             out_dtype=0, keep=0, ws=FAKE, ws_bytes=256, stream=None)
+    a.update(over)
+    return lib.gmm_ex(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(lhs=None), 1), (dict(out=None), 1),
+    (dict(rhs_dtype=0), 2),                         # e4m3 activations need 8- or 4-bit weights
+    (dict(lhs_dtype=0), 2),                         # lhs_scale with bf16 activations
+    (dict(lhs_dtype=1, lscale=None), 2),
+    (dict(scale_dtype=0), 2), (dict(scale_dtype=2), 2),
+    (dict(lhs_dtype=0, lscale=None, rhs_dtype=0), 2),  # E8M0 scales with bf16 weights
+    (dict(trhs=0), 2),
+    (dict(nlb=0), 3), (dict(nlb=3), 3), (dict(nlb=4), 3),  # lhs blocks must be 128-multiples wide
+    (dict(nb=4), 3), (dict(k=200), 3),
+    (dict(lscale=ctypes.c_void_p((1 << 20) + 2)), 4), (dict(godev=ctypes.c_void_p((1 << 20) + 2)), 4),
+    (dict(G=8, go=5), 5),
+    (dict(ws=None), 6),
+])
+def test_gmm_ex_host_validation(lib, over, status):
+    assert call_gmm_ex(lib, **over) == status
+
+
+def test_quantize_host_validation(lib):
+    q = lambda **o: lib.gmm_quantize_e4m3(o.get("x", FAKE), o.get("xd", 0), o.get("m", 4), o.get("k", 256),
+                                          o.get("group", 128), o.get("q", FAKE), o.get("s", FAKE), None)
+    assert q(x=None) == 1 and q(q=None) == 1 and q(s=None) == 1
+    assert q(xd=1) == 2 and q(xd=2) == 2
+    assert q(group=32) == 3 and q(group=96) == 3 and q(k=320) == 3 and q(m=-1) == 3
+    assert q(x=ctypes.c_void_p((1 << 20) + 2)) == 4 and q(s=ctypes.c_void_p((1 << 20) + 2)) == 4
 
 
 def test_tgmm_host_validation(lib):
