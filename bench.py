@@ -378,6 +378,36 @@ def run_suite(dev, peaks):
         record(f"decode_{fmt}_weights", ms, 2 * rows * n * k, bytes_)
         del fd, o
         torch.cuda.empty_cache()
+
+    # W8A8 on the decode workload: per-token-group e4m3 quantisation of the activations
+    # (128-wide groups), then the grouped matmul on e4m3 activations and e4m3 weights, with
+    # f32 and with E8M0 weight scales; each kernel alone and the two in sequence.
+    fd = W.fp8_decode(dev)
+    sizes = fd["group_sizes"]
+    gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    m = fd["lhs"].shape[0]
+    rows = float(sizes.sum())
+    live = int((sizes > 0).sum())
+    q, a_scale = G.quantize_e4m3(fd["lhs"])
+    o = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    ms = _time_call(torch, lambda: G.quantize_e4m3(fd["lhs"], out=q, scale=a_scale))
+    record("w8a8_quantize_e4m3", ms, 0.0, m * k * 2 + m * k + m * (k // 128) * 4)
+    e8 = torch.full(fd["rhs_scale"].shape, 120, dtype=torch.uint8, device=dev)
+    for name, sc, sbytes in (("w8a8_decode_gmm", fd["rhs_scale"], 4), ("w8a8_decode_gmm_e8m0", e8, 1)):
+        ms = _time_call(torch, lambda: G.gmm(q, fd["rhs"], gs, rhs_scale=sc, rhs_bias=fd["rhs_bias"], lhs_scale=a_scale,
+                                             out=o))
+        bytes_ = live * (n * k + nb * n * sbytes + n * 2) + rows * (k + (k // 128) * 4) + m * n * 2
+        record(name, ms, 2 * rows * n * k, bytes_)
+
+    def both():
+        G.quantize_e4m3(fd["lhs"], out=q, scale=a_scale)
+        G.gmm(q, fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"], lhs_scale=a_scale, out=o)
+
+    ms = _time_call(torch, both)
+    bytes_ = live * (n * k + nb * n * 4 + n * 2) + m * k * 2 + m * n * 2
+    record("w8a8_decode_quantize_plus_gmm", ms, 2 * rows * n * k, bytes_)
+    del fd, o, q, a_scale, e8
+    torch.cuda.empty_cache()
     return res
 
 
@@ -412,6 +442,13 @@ def _ncu_decode_int4(torch, G, W, dev):
                          rhs_format="int4")
 
 
+def _ncu_w8a8_decode(torch, G, W, dev):
+    fd = W.fp8_decode(dev)
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
+    q, a_scale = G.quantize_e4m3(fd["lhs"])
+    return lambda: G.gmm(q, fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"], lhs_scale=a_scale)
+
+
 def _ncu_moe128_wi(torch, G, W, dev):
     mo = W.moe128(dev, which=("lhs", "wi"))
     gs = torch.tensor(mo["group_sizes"], dtype=torch.int32, device=dev)
@@ -420,7 +457,7 @@ def _ncu_moe128_wi(torch, G, W, dev):
 
 
 NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode,
-             "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4}
+             "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4, "w8a8_decode": _ncu_w8a8_decode}
 
 
 def run_ncu_case(name):

@@ -517,17 +517,20 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
       const int32_t col = t.n_tile * BMW + wrow;
       const bool col_ok = col < p.n;
       const int64_t sidx = int64_t(t.local_group) * nb * p.n + col;  // scale of block 0 for this column
-      auto load_scales = [&](int32_t b0, float (&dst)[kPre]) {
+      // Prefetched as stored (f32 bits or an E8M0 byte), widened only when used, so
+      // that no instruction waits for the loads before then.
+      auto load_scales = [&](int32_t b0, uint32_t (&dst)[kPre]) {
 #pragma unroll
         for (int j = 0; j < kPre; ++j) {
-          dst[j] = 1.f;
+          dst[j] = p.scale_e8m0 ? 127u : 0x3F800000u;  // 1
           if (p.scale != nullptr && col_ok && b0 + j < nb) {
             const int64_t i = sidx + int64_t(b0 + j) * p.n;
-            dst[j] = p.scale_e8m0 ? e8m0_value(__ldg(static_cast<const uint8_t*>(p.scale) + i))
-                                  : __ldg(static_cast<const float*>(p.scale) + i);
+            dst[j] = p.scale_e8m0 ? uint32_t(__ldg(static_cast<const uint8_t*>(p.scale) + i))
+                                  : __float_as_uint(__ldg(static_cast<const float*>(p.scale) + i));
           }
         }
       };
+      auto widen = [&](uint32_t v) { return p.scale_e8m0 ? e8m0_value(v) : __uint_as_float(v); };
       float bias = 0.f;
       if (p.bias != nullptr && col_ok) {
         const int64_t bi = int64_t(t.local_group) * p.n + col;
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
         float acc[T8];
 #pragma unroll
         for (int i = 0; i < T8; ++i) acc[i] = 0.f;
-        float s_cur[kPre], s_next[kPre];
+        uint32_t s_cur[kPre], s_next[kPre];
         load_scales(0, s_cur);
         int32_t q = 0;
         for (int32_t c0 = 0; c0 < nb && ok; c0 += kPre) {
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
 #pragma unroll
           for (int bi = 0; bi < kPre; ++bi) {
             if (c0 + bi >= nb || !ok) break;
-            const float sw = s_cur[bi];
+            const float sw = widen(s_cur[bi]);
             for (int32_t qq = 0; qq < q_per_block; ++qq) {
               const int h = q % QPS;
               if (h == 0) {
