@@ -106,9 +106,9 @@ size_t gmm_workspace_bytes(void);
  *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  These are built for
  *                decode-sized groups (a few rows each) and stream every weight tile once per
  *                chunk of rows of its group (32 rows for e4m3 weights, 16 for bf16).
- *                8- and 4-bit weights run on the fp8 tensor cores: e4m3 and e5m2 as stored,
- *                the others rewritten exactly as e4m3 (int8 as 16 * high nibble + low nibble,
- *                two e4m3 terms).  Each lhs row is split per k step (256 wide; 128 for int8)
+ *                8- and 4-bit weights run on the fp8 tensor cores: e4m3, e5m2 and e2m1 as
+ *                stored, int8, int4 and uint4 rewritten exactly as e4m3 (int8 as 16 * high
+ *                nibble + low nibble, two e4m3 terms).  Each lhs row is split per k step (256 wide; 128 for int8)
  *                into two e4m3 terms times a power of two, exactly for every value within
  *                2^14 of the step's largest magnitude (smaller ones are off by at most 2^-21
  *                of it); a NaN or infinity in a row makes that output row NaN.
@@ -126,7 +126,8 @@ size_t gmm_workspace_bytes(void);
  *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
  *   out          [m, n] of out_dtype (BF16 or F32).
  *   Sizes: m >= 0, k >= 8, n >= 8, k % 8 == 0, n % 8 == 0 (16-byte rows); lhs, rhs,
- *   out and bias 16-byte aligned.  Row counts and offsets must fit in int32.
+ *   out and bias 16-byte aligned (E2M1 rhs 32-byte aligned).  Row counts and offsets must fit
+ *   in int32.
  *   Returns GMM_OK or an error status above.
  */
 int gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,

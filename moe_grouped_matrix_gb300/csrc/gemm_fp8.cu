@@ -1,5 +1,5 @@
-// e4m3 and e5m2 weights: the fp8 tensor-core kernel reads the TMA tiles as its
-// A operand directly.  Dispatch for every weight format of that kernel.
+// e4m3, e5m2 and e2m1 weights: the fp8 tensor-core kernel reads the TMA tiles
+// as its A operand directly.  Dispatch for every weight format of that kernel.
 #include "gemm_fp8.cuh"
 
 namespace gmmk {
@@ -9,6 +9,7 @@ cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, i
   switch (weight_format) {
     case kWeightE4M3: return fp8::launch_format<fp8::WFmt::kE4M3, false>(p, out_f32, grid, stream);
     case kWeightE5M2: return fp8::launch_format<fp8::WFmt::kE5M2, false>(p, out_f32, grid, stream);
+    case kWeightE2M1: return fp8::launch_format<fp8::WFmt::kE2M1, false>(p, out_f32, grid, stream);
     default: return launch_fp8_converted(p, weight_format, out_f32, grid, stream);
   }
 }

@@ -8,13 +8,14 @@
 //
 // Weights.  tcgen05.mma.kind::f8f6f4 reads a [128 n x 128 k] weight tile from
 // shared memory as its A operand (M = 128 weight rows, K = 32 per instruction).
-// e4m3 and e5m2 tiles are used as TMA copies them.  The other formats are
-// rewritten as e4m3 tiles by 4 weight-converter warps, exactly: every int4,
-// uint4 and e2m1 value is an e4m3 value, and an int8 w is 16 h + l with h its
-// signed high nibble and l its unsigned low nibble, where 16 h and l are e4m3
-// values, so an int8 tile becomes two A tiles whose MMAs add into one
-// accumulator.  The 4-bit formats hold two values per byte, the even k in the
-// low nibble.
+// e4m3, e5m2 and e2m1 tiles are used as TMA copies them (e2m1 through a tensor
+// map that spreads each 16 packed codes over 16 bytes, the 4-bit operand
+// layout of kind::f8f6f4).  int4, uint4 and int8 are rewritten as e4m3 tiles
+// by 4 weight-converter warps, exactly: every int4 and uint4 value is an e4m3
+// value, and an int8 w is 16 h + l with h its signed high nibble and l its
+// unsigned low nibble, where 16 h and l are e4m3 values, so an int8 tile
+// becomes two A tiles whose MMAs add into one accumulator.  The 4-bit formats
+// hold two values per byte, the even k in the low nibble.
 //
 // Activations.  The bf16 lhs rows are brought to e4m3 without losing their
 // value: for each token row and each pipeline step, with M the largest |x| of
@@ -76,12 +77,18 @@ constexpr uint32_t B_SUB = 2 * BT * KQ;  // e4m3 operand sub-tile: 64 rows x 128
 
 template <WFmt F, bool kA8>
 struct Cfg {
-  static constexpr bool kNibble = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
-  static constexpr bool kConv = kNibble || F == WFmt::kInt8;  // weights rewritten in shared memory
+  static constexpr bool kNibble = F == WFmt::kInt4 || F == WFmt::kUint4;  // 4-bit codes rewritten as e4m3
+  static constexpr bool kConv = kNibble || F == WFmt::kInt8;              // weights rewritten in shared memory
   static constexpr int QPS = F == WFmt::kInt8 ? 1 : 2;        // sub-tiles per step
   static constexpr int KS = KQ * QPS;                         // k per step
   static constexpr int PASSES = F == WFmt::kInt8 ? 2 : 1;     // A tiles per sub-tile
-  static constexpr uint32_t kAType = F == WFmt::kE5M2 ? 1u : 0u;  // kind::f8f6f4 type of A
+  // kind::f8f6f4 type of A: e4m3 0, e5m2 1, e2m1 5
+  static constexpr uint32_t kAType = F == WFmt::kE5M2 ? 1u : (F == WFmt::kE2M1 ? 5u : 0u);
+  // Bytes a raw box brings from global memory: e2m1 boxes hold 128 k of packed
+  // codes (64 bytes a row) that the TMA spreads over 128-byte rows, each 8
+  // bytes of codes followed by an 8-byte gap (the layout kind::f8f6f4 reads
+  // 4-bit operands in); the transaction count is the packed bytes.
+  static constexpr uint32_t RAW_TX = F == WFmt::kE2M1 ? RAW_BOX / 2 : RAW_BOX;
   // A raw box holds 128 bytes per row: 128 k of an 8-bit format, 256 k of a 4-bit one.
   static constexpr int RAW_BOXES = kNibble ? 1 : QPS;
   static constexpr uint32_t RAW_BYTES = RAW_BOXES * RAW_BOX;
@@ -223,16 +230,13 @@ __device__ __forceinline__ uint32_t lut4(uint32_t codes) {
 constexpr uint32_t kU0 = 0x44403800u, kU1 = 0x4E4C4A48u, kU2 = 0x53525150u, kU3 = 0x57565554u;
 // int4 codes 8..15 are -8..-1: magnitudes 8, 7, ..., 1 (the sign comes from the mask).
 constexpr uint32_t kI2 = 0x4A4C4E50u, kI3 = 0x38404448u;
-// e2m1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (sign-magnitude codes).
-constexpr uint32_t kF0 = 0x3C383000u, kF1 = 0x4C484440u;
 // 16 times the int4 value: magnitudes 0, 16, ..., 112 and 128, 112, ..., 16.
 constexpr uint32_t kH0 = 0x64605800u, kH1 = 0x6E6C6A68u, kH2 = 0x6A6C6E70u, kH3 = 0x58606468u;
 
 template <WFmt F>
 __device__ __forceinline__ uint32_t nibble4_to_e4m3(uint32_t codes) {
   if constexpr (F == WFmt::kUint4) return lut4<kU0, kU1, kU2, kU3, false>(codes);
-  else if constexpr (F == WFmt::kInt4) return lut4<kU0, kU1, kI2, kI3, true>(codes);
-  else return lut4<kF0, kF1, kF0, kF1, true>(codes);
+  else return lut4<kU0, kU1, kI2, kI3, true>(codes);
 }
 
 // 8 packed 4-bit codes (one word, k order from the low nibble) -> 8 e4m3 bytes.
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
             mbar_arrive_expect_tx(rawfull_bar(as), RAW_BOX);
             tma_load_3d(dst, &tm_rhs, rawfull_bar(as), ks * 128, t.n_tile * BMW, t.local_group);
           } else {
-            mbar_arrive_expect_tx(rawfull_bar(as), uint32_t(hq) * RAW_BOX);
+            mbar_arrive_expect_tx(rawfull_bar(as), uint32_t(hq) * C::RAW_TX);
             for (int h = 0; h < hq; ++h)
               tma_load_3d(dst + h * RAW_BOX, &tm_rhs, rawfull_bar(as), (QPS * ks + h) * KQ, t.n_tile * BMW,
                           t.local_group);

@@ -1,5 +1,5 @@
-// e4m3 activations with 4-bit weights (int4, uint4, e2m1), rewritten as e4m3
-// tiles by the weight-rewrite warps.
+// e4m3 activations with int4 and uint4 weights, rewritten as e4m3 tiles by the
+// weight-rewrite warps.
 #include "gemm_fp8.cuh"
 
 namespace gmmk {
@@ -9,7 +9,6 @@ cudaError_t launch_fp8_a8_packed(const ScaledLaunch& p, int weight_format, bool 
   switch (weight_format) {
     case kWeightInt4: return fp8::launch_format<fp8::WFmt::kInt4, true>(p, out_f32, grid, stream);
     case kWeightUint4: return fp8::launch_format<fp8::WFmt::kUint4, true>(p, out_f32, grid, stream);
-    case kWeightE2M1: return fp8::launch_format<fp8::WFmt::kE2M1, true>(p, out_f32, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -94,6 +94,23 @@ int make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, int rank,
   return GMM_OK;
 }
 
+// e2m1 weights [L, n, k], two codes per byte (even k in the low nibble), in
+// {128 k, 128 rows} boxes that land in shared memory as 128-byte rows, each 8
+// bytes of codes followed by an 8-byte gap (the 4-bit operand layout of
+// tcgen05.mma.kind::f8f6f4).  Needs k % 128 == 0 and a 32-byte-aligned base.
+int make_map_e2m1(CUtensorMap* map, const void* base, int64_t k, int64_t n, int64_t L) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t gdim[3] = {cuuint64_t(k), cuuint64_t(n), cuuint64_t(L)};
+  cuuint64_t gstride[2] = {cuuint64_t(k / 2), cuuint64_t(n) * cuuint64_t(k / 2)};
+  cuuint32_t bdim[3] = {128, 128, 1}, estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), gdim, gstride, bdim, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(int(r));
+  return GMM_OK;
+}
+
 bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 
 // The bf16 forward kernels:
@@ -249,6 +266,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || (rhs_bias && !aligned16(rhs_bias)) ||
       (rhs_scale && !aligned16(rhs_scale)))
     return GMM_ERR_ALIGN;
+  if (rhs_dtype == GMM_DTYPE_E2M1 && (reinterpret_cast<uintptr_t>(rhs) & 31u) != 0) return GMM_ERR_ALIGN;
   if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
   DeviceInfo dev;
   if (int st = current_device(&dev)) return st;
@@ -268,7 +286,9 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
                             lhs8 ? 1 : 2, 2, lhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return st;
     }
-    {
+    if (rhs_dtype == GMM_DTYPE_E2M1) {
+      if (int st = make_map_e2m1(&S.tm_rhs, rhs, k, n, num_local_groups)) return st;
+    } else {
       // Weight rows as bytes: k of an 8-bit format, k / 2 of a 4-bit one; bf16 as elements.
       const uint64_t row = packed4 ? uint64_t(k / 2) : uint64_t(k);
       const uint64_t dims[3] = {row, uint64_t(n), uint64_t(num_local_groups)};

@@ -197,31 +197,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = sbase + OFF_A + stage * A_BYTES;
         const uint32_t b0 = sbase + OFF_B + stage * B_BYTES;
         const int32_t valid = min(BR, rows - c * BR);
-        if (valid < BR) {
-          // Rows [valid, round_up(valid, 16)) belong to the next group (or lie
-          // past m): zero them in all six boxes.  A row is 128 contiguous bytes
-          // (the swizzle permutes 16-byte chunks within the row only).
-          const int32_t zrows = ((valid + 15) & ~15) - valid;
-          const int32_t units = zrows * 6 * 8;
-          for (int32_t u = lane; u < units; u += 32) {
-            const int32_t box = u / (zrows * 8);
-            const int32_t rem = u - box * zrows * 8;
-            const int32_t zr = valid + rem / 8, chunk = rem % 8;
-            const uint32_t base = box < 2 ? a0 + box * BOX_BYTES : b0 + (box - 2) * BOX_BYTES;
-            st_shared_v4(base + zr * 128 + chunk * 16, 0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (lane == 0) {
-          const int32_t ksteps = (valid + 15) / 16;
-          for (int32_t kk = 0; kk < ksteps; ++kk) {
+        const int32_t ksteps = (valid + 15) / 16, kfull = valid / 16;
+        auto issue = [&](int32_t k0, int32_t k1) {
+          for (int32_t kk = k0; kk < k1; ++kk) {
             const uint64_t ad = sw128_desc(a0 + kk * 2048, BOX_BYTES, 1024);
             const uint64_t bd = sw128_desc(b0 + kk * 2048, BOX_BYTES, 1024);
             mma_bf16_ss(d_tmem, ad, bd, kIdesc, (c | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));
+        };
+        // The 16-row blocks that hold only this group's rows go to the tensor
+        // core first; the tail block is fixed up while they run.
+        if (lane == 0) issue(0, kfull);
+        if (kfull < ksteps) {
+          // Rows [valid, 16 ksteps) belong to the next group (or lie past m):
+          // zero them in all six boxes, lanes over (row, 16-byte chunk).  A row
+          // is 128 contiguous bytes (the swizzle permutes chunks within a row).
+          const int32_t zrows = 16 * ksteps - valid;
+          const uint32_t chunk = uint32_t(lane & 7) * 16u;
+#pragma unroll
+          for (int box = 0; box < 6; ++box) {
+            const uint32_t base = box < 2 ? a0 + box * BOX_BYTES : b0 + (box - 2) * BOX_BYTES;
+            for (int32_t zr = lane >> 3; zr < zrows; zr += 4)
+              st_shared_v4(base + uint32_t(valid + zr) * 128u + chunk, 0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) issue(kfull, ksteps);
         }
+        if (lane == 0) mma_commit(empty_bar(stage));
         __syncwarp();
         if (++stage == STAGES) {
           stage = 0;
@@ -284,23 +287,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t(quarter * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += kColsPerBox) {
-        float f[kColsPerBox];
+      // The BN columns in 32-column pieces, two register buffers: the load of
+      // piece q + 1 is in flight while piece q is staged and stored.
+      constexpr int kPieces = BN / 32, kPerBox = kColsPerBox / 32;
+      uint32_t buf[2][32];
+      tmem_ld_32cols_async(tbase, buf[0]);
+      tmem_wait_ld(buf[0]);
+      float f[kColsPerBox];
 #pragma unroll
-        for (int h = 0; h < kColsPerBox / 32; ++h) {
-          uint32_t v[32];
-          tmem_ld_32cols(tbase + c + 32 * h, v);
+      for (int q = 0; q < kPieces; ++q) {
+        if (q + 1 < kPieces) tmem_ld_32cols_async(tbase + 32 * (q + 1), buf[(q + 1) & 1]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[32 * h + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) f[32 * (q % kPerBox) + i] = __uint_as_float(buf[q & 1][i]);
+        if ((q + 1) % kPerBox == 0) {
+          const int c = (q + 1 - kPerBox) * 32;
+          if (nt * BN + c < p.n && krow0 < p.k) {
+            stage_row<kOutF32>(acquire_slice(), lane, f);
+            release_slice(nt * BN + c, krow0, g);
+          }
         }
-        if (c + kColsPerBox == BN) {
+        if (q + 1 < kPieces) tmem_wait_ld(buf[(q + 1) & 1]);
+        if (q + 2 == kPieces) {
+          // every column is in registers: the accumulator can take the next tile
           tc_fence_before();
           mbar_arrive(acce_bar(acc));
-        }
-        if (nt * BN + c < p.n && krow0 < p.k) {
-          stage_row<kOutF32>(acquire_slice(), lane, f);
-          release_slice(nt * BN + c, krow0, g);
         }
       }
       if (++acc == 2) {
