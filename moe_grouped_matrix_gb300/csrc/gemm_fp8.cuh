@@ -110,7 +110,10 @@ struct Cfg {
   static constexpr uint32_t B_SUBT = kA8 ? BT * KQ : B_SUB;  // operand sub-tile: 32 or 64 rows
   static constexpr uint32_t B_BYTES = QPS * B_SUBT;
   static constexpr int kConvWarps = kA8 ? 1 : 4;       // token split, or the token-scale warp
-  static constexpr int kWConvWarps = kConv ? 4 : 0;    // weight rewrite
+  // weight rewrite: 4 warps (one thread per weight row), or 8 (two threads per
+  // row) with e4m3 activations, whose single token warp leaves room
+  static constexpr int kWConvWarps = kConv ? (kA8 ? 8 : 4) : 0;
+  static constexpr int kRowParts = kWConvWarps / 4;
   static constexpr int kThreads = 192 + 32 * (kConvWarps + kWConvWarps);
 
   static constexpr uint32_t OFF_RAW = 0;
@@ -795,13 +798,16 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
     }
   } else if constexpr (C::kConv) {
     // ---------------------------------------------------------------- weight rewrite
-    // Thread r rewrites weight row r of every sub-tile of the step.  Raw rows
-    // and A-tile rows are 128 bytes, 128-byte swizzled (chunk j of row r at
-    // position j ^ (r % 8)), so the 8 rows of a quarter-warp hit 8 different
-    // positions.  4-bit: raw chunk 4 h + i (32 codes) of the row becomes A chunks
-    // 2 i and 2 i + 1 of sub-tile h.  int8: raw chunk c (16 values) becomes chunk
-    // c of the 16 h tile (pass 0) and of the l tile (pass 1).
-    const int r = int(threadIdx.x) - 32 * (6 + C::kConvWarps);
+    // Thread t rewrites part t / 128 (of kRowParts) of weight row r = t % 128 of
+    // every sub-tile of the step.  Raw rows and A-tile rows are 128 bytes,
+    // 128-byte swizzled (chunk j of row r at position j ^ (r % 8)), so the 8
+    // rows of a quarter-warp hit 8 different positions.  4-bit: raw chunk 4 h + i
+    // (32 codes) of the row becomes A chunks 2 i and 2 i + 1 of sub-tile h.
+    // int8: raw chunk c (16 values) becomes chunk c of the 16 h tile (pass 0)
+    // and of the l tile (pass 1).
+    constexpr int kParts = C::kRowParts;
+    const int tw = int(threadIdx.x) - 32 * (6 + C::kConvWarps);
+    const int r = tw & 127, part = tw >> 7;
     uint32_t rs = 0, rph = 0, cs = 0;
     uint32_t j = 0;  // steps rewritten so far
     bool ok = true;
@@ -817,7 +823,8 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
         if constexpr (C::kNibble) {
           for (int h = 0; h < hq; ++h) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int ii = 0; ii < 4 / kParts; ++ii) {
+              const int i = part * (4 / kParts) + ii;
               uint32_t x[4];
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
@@ -831,18 +838,23 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
             }
           }
         } else {
-          // int8: the row's 8 raw chunks are loaded first, so that their latencies overlap
-          uint32_t x[8][4];
+          // int8: this thread's raw chunks of the row are loaded first, so that
+          // their latencies overlap
+          constexpr int kChunks = 8 / kParts;
+          uint32_t x[kChunks][4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
+          for (int cc = 0; cc < kChunks; ++cc) {
+            const int c = part * kChunks + cc;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x[c][0]), "=r"(x[c][1]), "=r"(x[c][2]), "=r"(x[c][3])
+                         : "=r"(x[cc][0]), "=r"(x[cc][1]), "=r"(x[cc][2]), "=r"(x[cc][3])
                          : "r"(src + (uint32_t(c ^ (r & 7)) << 4)));
+          }
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int cc = 0; cc < kChunks; ++cc) {
+            const int c = part * kChunks + cc;
             uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) int8x4_to_e4m3(x[c][u], hi[u], lo[u]);
+            for (int u = 0; u < 4; ++u) int8x4_to_e4m3(x[cc][u], hi[u], lo[u]);
             const uint32_t pos = uint32_t(c ^ (r & 7)) << 4;
             st_shared_v4(dst + pos, hi[0], hi[1], hi[2], hi[3]);
             st_shared_v4(dst + A_SUB + pos, lo[0], lo[1], lo[2], lo[3]);
