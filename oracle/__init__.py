@@ -59,6 +59,9 @@ def _load():
             lib.oracle_gmm_ex.argtypes = [P, I, I64, I64, P, I, I32, I64, I, P, I32, I32, P, I, I32, P, I32, P, I,
                                           P, I64, P, P, I]
             lib.oracle_gmm_ex.restype = I
+            lib.oracle_gmm_ex2.argtypes = [P, I, I64, I64, P, I, I32, I64, I, P, I32, I32, P, I, I32, P, I32, P, I,
+                                           I32, P, I, P, I64, P, P, I]
+            lib.oracle_gmm_ex2.restype = I
             lib.oracle_quantize_e4m3.argtypes = [P, I64, I64, I64, P, P]
             lib.oracle_quantize_e4m3.restype = I
             lib.oracle_tgmm.argtypes = [P, I, I64, I64, P, I, I64, P, I32, P, I64, P, P, I]
@@ -108,11 +111,13 @@ def group_offsets(group_sizes: np.ndarray, m: int) -> np.ndarray:
 
 def gmm(lhs, rhs, group_sizes, *, transpose_rhs=True, group_offset=0, rhs_scale=None,
         rhs_bias=None, rows=None, lhs_dtype=None, rhs_dtype=None, bias_dtype=None, lhs_scale=None,
-        threads=0):
+        rhs_block_scale=None, rhs_block_scale_dtype=None, threads=0):
     """Forward grouped matmul in fp64.  Returns (ref, mag), each [rows, n].
 
     rhs_scale: f32 [L, nb, 1, n], or uint8 E8M0 codes of that shape.  lhs_scale: None or f32
-    [m, num_lhs_blocks] (per-token-group activation scales)."""
+    [m, num_lhs_blocks] (per-token-group activation scales).  rhs_block_scale: None or
+    [L, n, k / block] per-element weight block scales, stored as rhs_block_scale_dtype (E8M0,
+    E4M3 or F32; uint8 arrays default to E8M0, float32 to F32)."""
     lhs, rhs, bias = _c(lhs), _c(rhs), _c(rhs_bias)
     gs = np.ascontiguousarray(group_sizes, dtype=np.int32)
     scale_code = F32
@@ -131,10 +136,16 @@ def gmm(lhs, rhs, group_sizes, *, transpose_rhs=True, group_offset=0, rhs_scale=
     count = m if rows_arr is None else rows_arr.shape[0]
     ref = np.zeros((count, n), dtype=np.float64)
     mag = np.zeros((count, n), dtype=np.float64)
-    rc = _load().oracle_gmm_ex(
+    bscale, bcode, bsize = None, 0, 0
+    if rhs_block_scale is not None:
+        bscale = np.ascontiguousarray(rhs_block_scale)
+        bcode = rhs_block_scale_dtype if rhs_block_scale_dtype is not None else (
+            E8M0 if bscale.dtype == np.uint8 else F32)
+        bsize = k // bscale.shape[-1]
+    rc = _load().oracle_gmm_ex2(
         _ptr(lhs), _dtype_code(lhs, lhs_dtype), m, k, _ptr(rhs), rcode, L, n,
         int(bool(transpose_rhs)), _ptr(gs), gs.shape[0], int(group_offset), _ptr(scale), scale_code, nb,
-        _ptr(lscale), 0 if lscale is None else lscale.shape[1],
+        _ptr(lscale), 0 if lscale is None else lscale.shape[1], _ptr(bscale), bcode, bsize,
         _ptr(bias), 0 if bias is None else _dtype_code(bias, bias_dtype), _ptr(rows_arr), count,
         _ptr(ref), _ptr(mag), int(threads))
     if rc != 0:

@@ -136,9 +136,10 @@ bool valid_dtype(int d) { return d >= DT_BF16 && d <= DT_E2M1; }
 // 2^(e - 127), except that 255 is 0.
 double decode_e8m0(uint8_t e) { return e == 255 ? 0.0 : std::ldexp(1.0, int(e) - 127); }
 
-// A scale value stored as f32 or E8M0.
+// A scale value stored as f32, E8M0 or e4m3fn.
 double load_scale(const void* base, int dtype, int64_t idx) {
   if (dtype == DT_E8M0) return decode_e8m0(static_cast<const uint8_t*>(base)[idx]);
+  if (dtype == DT_E4M3) return decode_e4m3fn(static_cast<const uint8_t*>(base)[idx]);
   return double(static_cast<const float*>(base)[idx]);
 }
 
@@ -232,14 +233,28 @@ void oracle_group_offsets(const int32_t* group_sizes, int32_t num_groups, int64_
 //                    k in [j*k/num_lhs_blocks, (j+1)*k/num_lhs_blocks), and
 //                    lhs[r, kk] counts as lhs_scale[r, j] * lhs[r, kk]
 //   rhs_scale_dtype  DT_F32 or DT_E8M0 for rhs_scale
-int oracle_gmm_ex(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
-                  int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
-                  int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int rhs_scale_dtype,
-                  int32_t num_blocks, const float* lhs_scale, int32_t num_lhs_blocks, const void* rhs_bias,
-                  int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref, double* mag, int threads) {
+// and with per-element block scales of the weights, the microscaling layout
+// (MXFP8: e4m3 weights with an E8M0 scale per 32 consecutive k of a weight
+// row; NVFP4: e2m1 weights with an e4m3 scale per 16):
+//   rhs_block_scale  NULL or [L, n, k / block_size] of rhs_block_scale_dtype
+//                    (DT_E8M0, DT_E4M3 or DT_F32), transpose_rhs only; the
+//                    weight W(g, c, kk) counts as
+//                    rhs_block_scale[g, c, kk / block_size] * W(g, c, kk)
+int oracle_gmm_ex2(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                   int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                   int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int rhs_scale_dtype,
+                   int32_t num_blocks, const float* lhs_scale, int32_t num_lhs_blocks, const void* rhs_block_scale,
+                   int rhs_block_scale_dtype, int32_t block_size, const void* rhs_bias, int bias_dtype,
+                   const int64_t* rows, int64_t num_rows, double* ref, double* mag, int threads) {
   if (!valid_dtype(lhs_dtype) || !valid_dtype(rhs_dtype)) return -1;
   if (rhs_bias && !valid_dtype(bias_dtype)) return -1;
   if (rhs_scale && rhs_scale_dtype != DT_F32 && rhs_scale_dtype != DT_E8M0) return -1;
+  if (rhs_block_scale) {
+    if (rhs_block_scale_dtype != DT_F32 && rhs_block_scale_dtype != DT_E8M0 && rhs_block_scale_dtype != DT_E4M3)
+      return -1;
+    if (!transpose_rhs || block_size <= 0 || k % block_size != 0) return -1;
+  }
+  const int64_t bpr = rhs_block_scale ? k / block_size : 0;  // block scales per weight row
   if (m < 0 || k < 0 || n < 0 || num_local_groups < 0 || num_total_groups < 0) return -1;
   if (group_offset < 0 || group_offset + num_local_groups > num_total_groups) return -1;
   const int32_t nb = rhs_scale ? num_blocks : 1;
@@ -274,7 +289,9 @@ int oracle_gmm_ex(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const vo
         double part = 0.0, part_abs = 0.0;
         for (int64_t kk = b * block; kk < (b + 1) * block; ++kk) {
           const int64_t widx = transpose_rhs ? (gl * n + c) * k + kk : (gl * k + kk) * n + c;
-          const double w = load(rhs, rhs_dtype, widx);
+          double w = load(rhs, rhs_dtype, widx);
+          if (rhs_block_scale)
+            w *= load_scale(rhs_block_scale, rhs_block_scale_dtype, (gl * n + c) * bpr + kk / block_size);
           part += a[kk] * w;
           part_abs += std::fabs(a[kk] * w);
         }
@@ -292,6 +309,16 @@ int oracle_gmm_ex(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const vo
     }
   });
   return 0;
+}
+
+int oracle_gmm_ex(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
+                  int32_t num_local_groups, int64_t n, int transpose_rhs, const int32_t* group_sizes,
+                  int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int rhs_scale_dtype,
+                  int32_t num_blocks, const float* lhs_scale, int32_t num_lhs_blocks, const void* rhs_bias,
+                  int bias_dtype, const int64_t* rows, int64_t num_rows, double* ref, double* mag, int threads) {
+  return oracle_gmm_ex2(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
+                        num_total_groups, group_offset, rhs_scale, rhs_scale_dtype, num_blocks, lhs_scale,
+                        num_lhs_blocks, nullptr, 0, 0, rhs_bias, bias_dtype, rows, num_rows, ref, mag, threads);
 }
 
 int oracle_gmm(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,

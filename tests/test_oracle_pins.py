@@ -473,3 +473,54 @@ def test_quantize_nan_group():
     q, s = oracle.quantize_e4m3(x, group=4)
     assert np.isnan(s[0, 0]) and s[0, 1] == np.float32(4.0) / np.float32(448.0)
     assert (q[0, :4] & 0x7F == 0x7F).all()
+
+
+# ------------------------------------------------------------------ microscaling block scales
+def test_mxfp8_block_scales_against_brute_force():
+    # e4m3 weights with one E8M0 scale per 32 consecutive k of each weight row (MXFP8)
+    rng = np.random.default_rng(21)
+    m, k, n, G = 14, 128, 6, 2
+    sizes = [6, 8]
+    lhs = rand_bf16(rng, (m, k))
+    codes = rng.integers(0, 256, (G, n, k)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x40
+    e8 = rng.integers(118, 136, (G, n, k // 32)).astype(np.uint8)
+    e8[0, 1, 2] = 255   # a zero block
+    e8[1, 4, 0] = 0     # 2^-127
+    w_v = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    s_v = np.where(e8 == 255, 0.0, 2.0 ** (e8.astype(np.float64) - 127))
+    ref, _ = oracle.gmm(lhs, codes, np.array(sizes), rhs_dtype=oracle.E4M3, rhs_block_scale=e8)
+    exp = brute_force_gmm(bf16_values(lhs), w_v * np.repeat(s_v, 32, axis=2), sizes, True)
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-300)
+
+
+def test_nvfp4_block_scales_with_tensor_scale_against_brute_force():
+    # e2m1 weights (packed, low nibble first) with one e4m3 scale per 16 k and an fp32 scale per
+    # expert and column (NVFP4's second level, here the per-block rhs_scale with one block)
+    rng = np.random.default_rng(22)
+    m, k, n, G = 10, 64, 5, 2
+    sizes = [4, 6]
+    lhs = rand_bf16(rng, (m, k))
+    packed = rng.integers(0, 256, (G, n, k // 2)).astype(np.uint8)
+    s8 = rng.integers(0x20, 0x60, (G, n, k // 16)).astype(np.uint8)  # positive finite e4m3 codes
+    tensor_scale = rng.uniform(0.5, 2.0, (G, 1, 1, n)).astype(np.float32)
+    w_v = unpack_nibbles(packed, E2M1_TABLE)
+    s_v = torch.from_numpy(s8.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ref, _ = oracle.gmm(lhs, packed, np.array(sizes), rhs_dtype=oracle.E2M1, rhs_block_scale=s8,
+                        rhs_block_scale_dtype=oracle.E4M3, rhs_scale=tensor_scale)
+    exp = brute_force_gmm(bf16_values(lhs), w_v * np.repeat(s_v, 16, axis=2), sizes, True,
+                          scale=tensor_scale.astype(np.float64))
+    np.testing.assert_allclose(ref, exp, rtol=1e-12, atol=1e-300)
+
+
+def test_one_block_per_row_equals_the_per_column_scale():
+    # a block scale whose block is the whole row is the per-(expert, column) scale with one quant block
+    rng = np.random.default_rng(23)
+    m, k, n, G = 9, 64, 7, 3
+    sizes = [2, 4, 3]
+    lhs = rand_bf16(rng, (m, k))
+    w = rand_bf16(rng, (G, n, k))
+    s = rng.uniform(0.25, 4.0, (G, n, 1)).astype(np.float32)
+    a, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_block_scale=s)
+    b, _ = oracle.gmm(lhs, w, np.array(sizes), rhs_scale=s.reshape(G, n).reshape(G, 1, 1, n))
+    np.testing.assert_allclose(a, b, rtol=1e-14, atol=0)
