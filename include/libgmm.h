@@ -205,6 +205,14 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *                    4-bit weights only, else GMM_ERR_DTYPE); 16-byte aligned.  A weight scale of
  *                    the pages' [n / 128, k / 128] layout for one group is s[b, 0, c] =
  *                    b_scale[c / 128, b].
+ *   rhs_block_scale  NULL, or microscaling block scales of the weights, device
+ *                    [num_local_groups, n, k / block_size] of rhs_block_scale_dtype: every weight
+ *                    W(g, c, kk) counts as rhs_block_scale[g, c, kk / block_size] * W(g, c, kk).
+ *                    Supported: MXFP8, i.e. E4M3 rhs with GMM_DTYPE_E8M0 scales and block_size 32
+ *                    (else GMM_ERR_DTYPE / GMM_ERR_SHAPE), bf16 lhs, F32 rhs_scale (or none) on
+ *                    top.  It runs on the decoding kernel: the decoders multiply each decoded
+ *                    bf16 weight by its block's power of two, exactly while the product stays in
+ *                    bf16's normal range.  No alignment requirement.
  *   keep_other_rows  0: rows outside the local groups are set to 0 (gmm); 1: they keep the
  *                    caller's contents (gmm_into).
  *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k
@@ -216,8 +224,9 @@ int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_l
            const void* rhs, int rhs_dtype, int32_t num_local_groups, int64_t n, int transpose_rhs,
            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
            const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
-           const void* rhs_bias, int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace,
-           size_t workspace_bytes, void* stream);
+           const void* rhs_block_scale, int rhs_block_scale_dtype, int32_t block_size, const void* rhs_bias,
+           int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace, size_t workspace_bytes,
+           void* stream);
 
 /*
  * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS

@@ -56,8 +56,8 @@ SIGNATURES = {
     "tgmm_local": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
     "gmm_quantize_e4m3": ([_P, _I, _I64, _I64, _I64, _P, _P, _P], _I),
-    "gmm_ex": ([_P, _I, _P, _I32, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _P, _I, _I32, _P, _I, _P, _I,
-                _I, _P, _SZ, _P], _I),
+    "gmm_ex": ([_P, _I, _P, _I32, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _P, _I, _I32, _P, _I, _I32, _P,
+                _I, _P, _I, _I, _P, _SZ, _P], _I),
     "gmm_tuning_set": ([_I32, _I64, _I64, _I32, _I, _I, _I, _I], _I),
     "gmm_tuning_get": ([_I32, _I64, _I64, _I32, _I, _I, _IP, _IP], _I),
     "gmm_tuning_clear": ([], _I),
@@ -130,7 +130,7 @@ def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out, out_dtype,
-              workspace, stream, rhs_format, lhs_scale=None):
+              workspace, stream, rhs_format, lhs_scale=None, rhs_block_scale=None):
     lib = load_library()
     _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
     if group_sizes.dtype != torch.int32:
@@ -159,7 +159,11 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
     if rhs_bias is not None:
         _dev(rhs_bias, "rhs_bias")
     e8m0 = rhs_scale is not None and rhs_scale.dtype == torch.uint8
-    if lhs.dtype == torch.float8_e4m3fn or lhs_scale is not None or e8m0:
+    if rhs_block_scale is not None:
+        _dev(rhs_block_scale, "rhs_block_scale")
+        if rhs_block_scale.dim() != 3 or k % rhs_block_scale.shape[2] != 0:
+            raise ValueError("rhs_block_scale must be [G_local, n, k / block_size]")
+    if lhs.dtype == torch.float8_e4m3fn or lhs_scale is not None or e8m0 or rhs_block_scale is not None:
         # e4m3 activations with their scales, or E8M0 weight scales: gmm_ex
         if lhs_scale is not None:
             _dev(lhs_scale, "lhs_scale")
@@ -175,6 +179,10 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
                         int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0],
                         0 if dev_off else int(group_offset), group_offset.data_ptr() if dev_off else None,
                         None if rhs_scale is None else rhs_scale.data_ptr(), DTYPE_E8M0 if e8m0 else DTYPE_F32, nb,
+                        None if rhs_block_scale is None else rhs_block_scale.data_ptr(),
+                        DTYPE_E8M0 if rhs_block_scale is None or rhs_block_scale.dtype == torch.uint8 else
+                        _code(rhs_block_scale),
+                        0 if rhs_block_scale is None else k // rhs_block_scale.shape[2],
                         None if rhs_bias is None else rhs_bias.data_ptr(),
                         0 if rhs_bias is None else _code(rhs_bias), out.data_ptr(), _code(out),
                         int(fn == "gmm_into"), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
@@ -202,26 +210,28 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
 
 
 def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
-        out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None, lhs_scale=None):
+        out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None, lhs_scale=None,
+        rhs_block_scale=None):
     """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
     for each row r of local group g; all other rows of out are zero.  group_offset is an int, or a
     one-element int32 CUDA tensor that the kernel reads when it runs.  rhs is bf16, float8_e4m3fn,
     float8_e5m2 or int8, or a uint8 tensor [G_local, n, k / 2] of packed 4-bit weights with
     rhs_format = "int4", "uint4" or "e2m1".  rhs_scale is float32 [G_local, nb, 1, n], or uint8
     E8M0 codes of that shape.  lhs may be float8_e4m3fn (W8A8) with lhs_scale float32
-    [m, num_lhs_blocks] (quantize_e4m3's scales)."""
+    [m, num_lhs_blocks] (quantize_e4m3's scales).  rhs_block_scale: uint8 E8M0 [G_local, n, k / 32]
+    microscaling scales of float8_e4m3fn weights (MXFP8)."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out_dtype, workspace, stream, rhs_format, lhs_scale)
+                     out_dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale)
 
 
 def gmm_into(lhs, rhs, group_sizes, out, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0,
-             workspace=None, stream=None, rhs_format=None, lhs_scale=None):
+             workspace=None, stream=None, rhs_format=None, lhs_scale=None, rhs_block_scale=None):
     """As gmm, but only the local groups' rows of `out` are written; every other row keeps the
     caller's contents (the existing-output mode)."""
     if out is None:
         raise ValueError("gmm_into needs an output tensor")
     return _gmm_call("gmm_into", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out.dtype, workspace, stream, rhs_format, lhs_scale)
+                     out.dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale)
 
 
 def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, out=None, out_dtype=torch.float32,

@@ -33,6 +33,12 @@
 // places the 7 exponent/mantissa bits of the code at bf16 bits 4..10 (giving
 // the bf16 number 2^-120 times the code's value, subnormals included) and
 // multiplies by 2^120; the two NaN codes (0x7F, 0xFF) are mapped to NaN.
+//
+// Microscaling (MXFP8): with an E8M0 scale per 32 consecutive k of a weight
+// row, each decoder thread's 32 values of a step are one scale block, and the
+// decoded bf16 values are multiplied by the block's power of two, exactly
+// while the product stays within bf16's normal range (|w| 2^(e-127) between
+// 2^-126 and 2^128).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -100,7 +106,15 @@ struct Params {
   uint32_t* err;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
+  const uint8_t* mx_scale;          // NULL, or E8M0 [L, n, k / 32]: one scale per 32 k of a weight row
 };
+
+// bf16x2 holding 2^(e - 127) twice, the value of an E8M0 byte (page
+// "gemm_quant.rs", widen_block_scale_f32: e = 0 is 2^-127, e = 255 is 0).
+__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
+  const uint32_t b = e == 255u ? 0u : (e == 0u ? 0x0040u : e << 7);
+  return b | (b << 16);
+}
 
 // 16 e4m3fn codes (one 16-byte chunk, lowest k first) -> 16 bf16 (8 words).
 // Per 4 codes, magnitudes (low 7 bits) and signs are split once; per pair of
@@ -460,10 +474,20 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
     const int row = quarter * 32 + lane;
     const int c0 = 2 * (dw >> 2);
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const int32_t mx_per_row = p.k / 32;
     uint32_t rs = 0, rphase = 0, os = 0, ophase = 0;
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      // this thread's weight row in the group's rhs, for its MX scales
+      const uint8_t* mx_row = nullptr;
+      if (p.mx_scale != nullptr) {
+        const GemmTile t = item_of(w);
+        const int32_t wr = t.n_tile * BMW + row;
+        if (wr < p.n) mx_row = p.mx_scale + (int64_t(t.local_group) * p.n + wr) * mx_per_row + c0 / 2;
+      }
       for (int32_t ks = 0; ks < ksteps; ++ks) {
+        // block (4 ks + c0 / 2) of the row: the scale of this thread's 32 values
+        const uint32_t mx = mx_row != nullptr ? uint32_t(__ldg(mx_row + 4 * ks)) : 127u;
         if (!wait_bar(rfull_bar(rs), rphase, abort_flag, p.err) ||
             !wait_bar(oempty_bar(os), ophase ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -484,6 +508,12 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
         for (int i = 0; i < 2; ++i) {
           uint32_t o[8];
           decode16(raw[i], o);
+          if (p.mx_scale != nullptr) {
+            const uint32_t s2 = e8m0_bf16x2(mx);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(o[j]) : "r"(o[j]), "r"(s2), "r"(0x80008000u));
+          }
           tmem_st_8cols(tcol + uint32_t(c0 + i) * 8u, o);
         }
         __syncwarp();
@@ -519,7 +549,7 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const auto* scale = static_cast<const float*>(L.scale);
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, scale,
-           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev};
+           L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.mx_scale};
   kern<<<grid, kE4M3 ? 192 + kConvThreads : 192, Layout<kE4M3>::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

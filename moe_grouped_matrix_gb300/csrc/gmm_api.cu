@@ -213,6 +213,9 @@ struct ExtArgs {
   const float* lhs_scale = nullptr;
   int32_t num_lhs_blocks = 0;
   int rhs_scale_dtype = GMM_DTYPE_F32;
+  const void* rhs_block_scale = nullptr;  // microscaling: [L, n, k / block_size]
+  int rhs_block_scale_dtype = GMM_DTYPE_E8M0;
+  int32_t block_size = 0;
 };
 
 // Shared body of gmm and gmm_into: zero_rest says whether rows of the
@@ -233,6 +236,14 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   const bool scale_e8m0 = ext.rhs_scale_dtype == GMM_DTYPE_E8M0;
   if (ext.rhs_scale_dtype != GMM_DTYPE_F32 && !scale_e8m0) return GMM_ERR_DTYPE;
   if (scale_e8m0 && rhs_dtype == GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
+  // Microscaling (MXFP8): e4m3 weights with an E8M0 scale per 32 k of a weight
+  // row, bf16 activations, on the decoding kernel.
+  const bool mx = ext.rhs_block_scale != nullptr;
+  if (mx) {
+    if (rhs_dtype != GMM_DTYPE_E4M3 || ext.rhs_block_scale_dtype != GMM_DTYPE_E8M0 || lhs8 || !transpose_rhs)
+      return GMM_ERR_DTYPE;
+    if (ext.block_size != 32) return GMM_ERR_SHAPE;
+  }
   if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (rhs_bias != nullptr && bias_dtype != GMM_DTYPE_BF16 && bias_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -316,14 +327,19 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.lhs_e4m3 = lhs8 ? 1 : 0;
     S.lhs_scale = ext.lhs_scale;
     S.num_lhs_blocks = ext.lhs_scale != nullptr ? ext.num_lhs_blocks : 1;
+    S.mx_scale = static_cast<const uint8_t*>(ext.rhs_block_scale);
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     cudaError_t e;
     if (rhs_dtype == GMM_DTYPE_BF16) {
       e = gmmk::launch_scaled(S, false, f32, dev.sms, s);
     } else if (rhs_dtype == GMM_DTYPE_E4M3) {
-      const int decode = choose_e4m3_decode();
+      int decode = choose_e4m3_decode();
       if (decode < 0) return GMM_ERR_SHAPE;
       if (decode && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;  // the decoding kernel takes bf16 lhs, f32 scales
+      if (mx) {
+        if (scale_e8m0) return GMM_ERR_DTYPE;
+        decode = 1;  // per-32 scales are applied as the weights are decoded
+      }
       e = decode ? gmmk::launch_scaled(S, true, f32, dev.sms, s) : gmmk::launch_fp8(S, gmmk::kWeightE4M3, f32, dev.sms, s);
     } else {
       const int fmt = rhs_dtype == GMM_DTYPE_E5M2   ? gmmk::kWeightE5M2
@@ -429,12 +445,16 @@ int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_l
            const void* rhs, int rhs_dtype, int32_t num_local_groups, int64_t n, int transpose_rhs,
            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
            const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
-           const void* rhs_bias, int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace,
-           size_t workspace_bytes, void* stream) {
+           const void* rhs_block_scale, int rhs_block_scale_dtype, int32_t block_size, const void* rhs_bias,
+           int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace, size_t workspace_bytes,
+           void* stream) {
   ExtArgs ext;
   ext.lhs_scale = lhs_scale;
   ext.num_lhs_blocks = num_lhs_blocks;
   ext.rhs_scale_dtype = rhs_scale_dtype;
+  ext.rhs_block_scale = rhs_block_scale;
+  ext.rhs_block_scale_dtype = rhs_block_scale_dtype;
+  ext.block_size = block_size;
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype,
                   workspace, workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset_dev, GMM_KERNEL_AUTO, 0,

@@ -77,6 +77,7 @@ struct ScaledLaunch {
   int32_t lhs_e4m3;                 // lhs holds e4m3 codes (fp8 kernels only)
   const float* lhs_scale;           // lhs_e4m3: NULL or f32 [m, num_lhs_blocks]
   int32_t num_lhs_blocks;
+  const uint8_t* mx_scale;          // decoding kernel, e4m3 weights: NULL or E8M0 [L, n, k / 32]
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);

@@ -78,8 +78,8 @@ def test_gmm_host_validation(lib, fn, over, status):
 
 def call_gmm_ex(lib, **over):
     a = dict(lhs=FAKE, lhs_dtype=2, lscale=FAKE, nlb=2, m=256, k=256, rhs=FAKE, rhs_dtype=2, L=4, n=256, trhs=1,
-             gs=FAKE, G=4, go=0, godev=None, scale=FAKE, scale_dtype=8, nb=2, bias=None, bias_dtype=0, out=FAKE,
-             out_dtype=0, keep=0, ws=FAKE, ws_bytes=256, stream=None)
+             gs=FAKE, G=4, go=0, godev=None, scale=FAKE, scale_dtype=8, nb=2, bscale=None, bscale_dtype=8, bsize=0,
+             bias=None, bias_dtype=0, out=FAKE, out_dtype=0, keep=0, ws=FAKE, ws_bytes=256, stream=None)
     a.update(over)
     return lib.gmm_ex(*a.values())
 
@@ -97,6 +97,11 @@ def call_gmm_ex(lib, **over):
     (dict(lscale=ctypes.c_void_p((1 << 20) + 2)), 4), (dict(godev=ctypes.c_void_p((1 << 20) + 2)), 4),
     (dict(G=8, go=5), 5),
     (dict(ws=None), 6),
+    # microscaling block scales: MXFP8 only (e4m3 weights, E8M0 per 32, bf16 activations)
+    (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=32, rhs_dtype=3), 2),
+    (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=32, bscale_dtype=2), 2),
+    (dict(bscale=FAKE, bsize=32), 2),                                     # e4m3 activations
+    (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=16), 3),
 ])
 def test_gmm_ex_host_validation(lib, over, status):
     assert call_gmm_ex(lib, **over) == status
