@@ -208,11 +208,15 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *   rhs_block_scale  NULL, or microscaling block scales of the weights, device
  *                    [num_local_groups, n, k / block_size] of rhs_block_scale_dtype: every weight
  *                    W(g, c, kk) counts as rhs_block_scale[g, c, kk / block_size] * W(g, c, kk).
- *                    Supported: MXFP8, i.e. E4M3 rhs with GMM_DTYPE_E8M0 scales and block_size 32
- *                    (else GMM_ERR_DTYPE / GMM_ERR_SHAPE), bf16 lhs, F32 rhs_scale (or none) on
- *                    top.  It runs on the decoding kernel: the decoders multiply each decoded
- *                    bf16 weight by its block's power of two, exactly while the product stays in
- *                    bf16's normal range.  No alignment requirement.
+ *                    Supported (else GMM_ERR_DTYPE / GMM_ERR_SHAPE), with bf16 lhs and an F32
+ *                    rhs_scale (or none) on top:
+ *                      MXFP8: E4M3 rhs, GMM_DTYPE_E8M0 scales, block_size 32;
+ *                      NVFP4: E2M1 rhs, GMM_DTYPE_E4M3 scales, block_size 16 (the second-level
+ *                      fp32 scale of NVFP4 is rhs_scale with num_quant_blocks = 1).
+ *                    They run on the decoding kernel: the decoders multiply each decoded bf16
+ *                    weight by its block scale, exactly (MXFP8 while the product stays in bf16's
+ *                    normal range; an e2m1 value times an e4m3 value always fits bf16).  No
+ *                    alignment requirement for the scales.
  *   keep_other_rows  0: rows outside the local groups are set to 0 (gmm); 1: they keep the
  *                    caller's contents (gmm_into).
  *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k

@@ -218,8 +218,9 @@ def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True
     float8_e5m2 or int8, or a uint8 tensor [G_local, n, k / 2] of packed 4-bit weights with
     rhs_format = "int4", "uint4" or "e2m1".  rhs_scale is float32 [G_local, nb, 1, n], or uint8
     E8M0 codes of that shape.  lhs may be float8_e4m3fn (W8A8) with lhs_scale float32
-    [m, num_lhs_blocks] (quantize_e4m3's scales).  rhs_block_scale: uint8 E8M0 [G_local, n, k / 32]
-    microscaling scales of float8_e4m3fn weights (MXFP8)."""
+    [m, num_lhs_blocks] (quantize_e4m3's scales).  rhs_block_scale: microscaling scales, uint8 E8M0
+    [G_local, n, k / 32] of float8_e4m3fn weights (MXFP8) or float8_e4m3fn [G_local, n, k / 16] of
+    packed e2m1 weights (NVFP4)."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
                      out_dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale)
 

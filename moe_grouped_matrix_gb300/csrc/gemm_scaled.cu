@@ -106,7 +106,9 @@ struct Params {
   uint32_t* err;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
-  const uint8_t* mx_scale;          // NULL, or E8M0 [L, n, k / 32]: one scale per 32 k of a weight row
+  // Microscaling block scales [L, n, k / block] of the weights: MXFP8 (e4m3
+  // weights) E8M0 per 32 k, or NULL; NVFP4 (e2m1 weights) e4m3 per 16 k.
+  const uint8_t* mx_scale;
 };
 
 // bf16x2 holding 2^(e - 127) twice, the value of an E8M0 byte (page
@@ -114,6 +116,45 @@ struct Params {
 __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
   const uint32_t b = e == 255u ? 0u : (e == 0u ? 0x0040u : e << 7);
   return b | (b << 16);
+}
+
+// bf16x2 holding an e4m3fn value twice (exact: every e4m3fn value is a bf16 value).
+__device__ __forceinline__ uint32_t e4m3_bf16x2(uint32_t code) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(uint16_t(code)));
+  const float f = __half2float(__ushort_as_half(uint16_t(h)));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  return b | (b << 16);
+}
+
+// 32 e2m1 codes (16 bytes, the even k in the low nibble) -> 32 bf16 (16 words,
+// k order: words 0..7 in lo, 8..15 in hi), the first 16 times s_lo and the
+// last 16 times s_hi (bf16x2 scale factors).  A code's 3 magnitude bits placed at bf16 bits 6..8 under its sign
+// bit give the bf16 number 2^-126 times its value (exponent field = the code's
+// exponent, the mantissa bit as bf16's top mantissa bit; code exponent 0 is
+// then the subnormal 2^-127 = 2^-126 * 0.5).  Two bf16x2 fmas multiply by 2^126
+// and by the block scale, exactly (a product of an e2m1 and an e4m3 value has
+// at most 6 significant bits).
+__device__ __forceinline__ void decode_fp4_32(const uint4 raw, uint32_t s_lo, uint32_t s_hi, uint32_t (&lo)[8],
+                                              uint32_t (&hi)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] & 0x0F0F0F0Fu, v = (w[i] >> 4) & 0x0F0F0F0Fu;  // even-k / odd-k codes per byte
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // byte j's even-k code at bits 0..3, its odd-k code at bits 16..19
+      const uint32_t t = __byte_perm(u, v, uint32_t(j) | (uint32_t(4 + j) << 8));
+      const uint32_t x = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
+      uint32_t y;
+      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(x), "r"(0x7E807E80u), "r"(0x80008000u));
+      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(y), "r"(i < 2 ? s_lo : s_hi), "r"(0x80008000u));
+      if (i < 2)
+        lo[4 * i + j] = y;
+      else
+        hi[4 * (i - 2) + j] = y;
+    }
+  }
 }
 
 // 16 e4m3fn codes (one 16-byte chunk, lowest k first) -> 16 bf16 (8 words).
@@ -157,10 +198,13 @@ __device__ __forceinline__ void decode16(const uint4 raw, uint32_t (&o)[8]) {
   }
 }
 
-template <bool kE4M3, bool kOutF32>
+// kE4M3: weights decoded to bf16 by the decoder warps, e4m3 codes, or (kFp4)
+// e2m1 codes two per byte with an e4m3 scale per 16 k (NVFP4).
+template <bool kE4M3, bool kFp4, bool kOutF32>
 __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
     gemm_scaled_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_rhs,
                        const Params p) {
+  static_assert(kE4M3 || !kFp4, "4-bit weights are decoded");
   using L = Layout<kE4M3>;
   constexpr int OSTAGES = L::kOStages;
   int32_t go;
@@ -251,9 +295,11 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
             break;
           }
           if constexpr (kE4M3) {
+            // e2m1: 64 bytes a row ({64 bytes, 128 rows} box, rows 64 bytes apart)
             const uint32_t fb = rfull_bar(ws);
-            mbar_arrive_expect_tx(fb, RAW_BYTES);
-            tma_load_3d(sbase + L::OFF_RAW + ws * RAW_BYTES, &tm_rhs, fb, ks * KS, t.n_tile * BMW, t.local_group);
+            mbar_arrive_expect_tx(fb, kFp4 ? RAW_BYTES / 2 : RAW_BYTES);
+            tma_load_3d(sbase + L::OFF_RAW + ws * RAW_BYTES, &tm_rhs, fb, kFp4 ? ks * (KS / 2) : ks * KS,
+                        t.n_tile * BMW, t.local_group);
           } else {
             const uint32_t fb = ofull_bar(ws);
             mbar_arrive_expect_tx(fb, A_BYTES);
@@ -474,7 +520,7 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
     const int row = quarter * 32 + lane;
     const int c0 = 2 * (dw >> 2);
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    const int32_t mx_per_row = p.k / 32;
+    const int32_t mx_per_row = p.k / (kFp4 ? 16 : 32);
     uint32_t rs = 0, rphase = 0, os = 0, ophase = 0;
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -483,17 +529,38 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
       if (p.mx_scale != nullptr) {
         const GemmTile t = item_of(w);
         const int32_t wr = t.n_tile * BMW + row;
-        if (wr < p.n) mx_row = p.mx_scale + (int64_t(t.local_group) * p.n + wr) * mx_per_row + c0 / 2;
+        // MXFP8: block 4 ks + c0 / 2 holds this thread's 32 values of step ks;
+        // NVFP4: blocks 8 ks + c0 and + 1 hold them
+        if (wr < p.n) mx_row = p.mx_scale + (int64_t(t.local_group) * p.n + wr) * mx_per_row + (kFp4 ? c0 : c0 / 2);
       }
       for (int32_t ks = 0; ks < ksteps; ++ks) {
-        // block (4 ks + c0 / 2) of the row: the scale of this thread's 32 values
-        const uint32_t mx = mx_row != nullptr ? uint32_t(__ldg(mx_row + 4 * ks)) : 127u;
+        uint32_t mx = 127u, s_lo = 0x3F803F80u, s_hi = 0x3F803F80u;  // scales of 1
+        if constexpr (kFp4) {
+          if (mx_row != nullptr) {
+            s_lo = e4m3_bf16x2(__ldg(mx_row + 8 * ks));
+            s_hi = e4m3_bf16x2(__ldg(mx_row + 8 * ks + 1));
+          }
+        } else {
+          if (mx_row != nullptr) mx = uint32_t(__ldg(mx_row + 4 * ks));
+        }
         if (!wait_bar(rfull_bar(rs), rphase, abort_flag, p.err) ||
             !wait_bar(oempty_bar(os), ophase ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t tcol = tmem_base + lane_base + TMEM_A_BASE + os * TMEM_A_STAGE_COLS;
+        if constexpr (kFp4) {
+          // the row's 16-byte chunk c0 / 2 (k [16 c0, 16 c0 + 32)), unswizzled 64-byte rows
+          uint4 raw;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                       : "r"(sbase + L::OFF_RAW + rs * RAW_BYTES + uint32_t(row) * 64u + uint32_t(c0 / 2) * 16u));
+          uint32_t lo[8], hi[8];
+          decode_fp4_32(raw, s_lo, s_hi, lo, hi);
+          tmem_st_8cols(tcol + uint32_t(c0) * 8u, lo);
+          tmem_st_8cols(tcol + uint32_t(c0 + 1) * 8u, hi);
+        } else {
         const uint32_t raw0 = sbase + L::OFF_RAW + rs * RAW_BYTES + uint32_t(row) * 128u;
         uint4 raw[2];
 #pragma unroll
@@ -503,7 +570,6 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
                        : "=r"(raw[i].x), "=r"(raw[i].y), "=r"(raw[i].z), "=r"(raw[i].w)
                        : "r"(raw0 + (uint32_t(c ^ (row & 7)) << 4)));
         }
-        const uint32_t tcol = tmem_base + lane_base + TMEM_A_BASE + os * TMEM_A_STAGE_COLS;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           uint32_t o[8];
@@ -515,6 +581,7 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
               asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(o[j]) : "r"(o[j]), "r"(s2), "r"(0x80008000u));
           }
           tmem_st_8cols(tcol + uint32_t(c0 + i) * 8u, o);
+        }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(rempty_bar(rs));
@@ -542,9 +609,9 @@ __global__ void __launch_bounds__(kE4M3 ? 192 + kConvThreads : 192, 1)
   }
 }
 
-template <bool kE4M3, bool kOutF32>
+template <bool kE4M3, bool kFp4, bool kOutF32>
 cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
-  auto kern = gemm_scaled_kernel<kE4M3, kOutF32>;
+  auto kern = gemm_scaled_kernel<kE4M3, kFp4, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Layout<kE4M3>::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const auto* scale = static_cast<const float*>(L.scale);
@@ -557,8 +624,13 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream) {
-  if (rhs_e4m3) return out_f32 ? launch_impl<true, true>(p, grid, stream) : launch_impl<true, false>(p, grid, stream);
-  return out_f32 ? launch_impl<false, true>(p, grid, stream) : launch_impl<false, false>(p, grid, stream);
+  if (rhs_e4m3)
+    return out_f32 ? launch_impl<true, false, true>(p, grid, stream) : launch_impl<true, false, false>(p, grid, stream);
+  return out_f32 ? launch_impl<false, false, true>(p, grid, stream) : launch_impl<false, false, false>(p, grid, stream);
+}
+
+cudaError_t launch_scaled_nvfp4(const ScaledLaunch& p, bool out_f32, int grid, cudaStream_t stream) {
+  return out_f32 ? launch_impl<true, true, true>(p, grid, stream) : launch_impl<true, true, false>(p, grid, stream);
 }
 
 }  // namespace gmmk

@@ -236,13 +236,16 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   const bool scale_e8m0 = ext.rhs_scale_dtype == GMM_DTYPE_E8M0;
   if (ext.rhs_scale_dtype != GMM_DTYPE_F32 && !scale_e8m0) return GMM_ERR_DTYPE;
   if (scale_e8m0 && rhs_dtype == GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
-  // Microscaling (MXFP8): e4m3 weights with an E8M0 scale per 32 k of a weight
-  // row, bf16 activations, on the decoding kernel.
+  // Microscaling, on the decoding kernel with bf16 activations: MXFP8 (e4m3
+  // weights, an E8M0 scale per 32 k of a weight row) or NVFP4 (e2m1 weights,
+  // an e4m3 scale per 16 k).
   const bool mx = ext.rhs_block_scale != nullptr;
+  const bool nvfp4 = mx && rhs_dtype == GMM_DTYPE_E2M1;
   if (mx) {
-    if (rhs_dtype != GMM_DTYPE_E4M3 || ext.rhs_block_scale_dtype != GMM_DTYPE_E8M0 || lhs8 || !transpose_rhs)
-      return GMM_ERR_DTYPE;
-    if (ext.block_size != 32) return GMM_ERR_SHAPE;
+    const bool mxfp8 = rhs_dtype == GMM_DTYPE_E4M3 && ext.rhs_block_scale_dtype == GMM_DTYPE_E8M0;
+    const bool fp4 = nvfp4 && ext.rhs_block_scale_dtype == GMM_DTYPE_E4M3;
+    if ((!mxfp8 && !fp4) || lhs8 || !transpose_rhs || scale_e8m0) return GMM_ERR_DTYPE;
+    if (ext.block_size != (fp4 ? 16 : 32)) return GMM_ERR_SHAPE;
   }
   if (rhs_dtype < GMM_DTYPE_BF16 || rhs_dtype > GMM_DTYPE_E2M1 || rhs_dtype == GMM_DTYPE_F32) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -297,7 +300,14 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
                             lhs8 ? 1 : 2, 2, lhs, dims, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return st;
     }
-    if (rhs_dtype == GMM_DTYPE_E2M1) {
+    if (nvfp4) {
+      // packed e2m1 bytes for the decoders: {64 bytes (128 k), 128 rows} boxes, unswizzled
+      const uint64_t dims[3] = {uint64_t(k / 2), uint64_t(n), uint64_t(num_local_groups)};
+      const uint32_t box[3] = {64u, 128u, 1u};
+      if (int st = make_map(&S.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, rhs, dims, box,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return st;
+    } else if (rhs_dtype == GMM_DTYPE_E2M1) {
       if (int st = make_map_e2m1(&S.tm_rhs, rhs, k, n, num_local_groups)) return st;
     } else {
       // Weight rows as bytes: k of an 8-bit format, k / 2 of a 4-bit one; bf16 as elements.
@@ -336,11 +346,10 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       int decode = choose_e4m3_decode();
       if (decode < 0) return GMM_ERR_SHAPE;
       if (decode && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;  // the decoding kernel takes bf16 lhs, f32 scales
-      if (mx) {
-        if (scale_e8m0) return GMM_ERR_DTYPE;
-        decode = 1;  // per-32 scales are applied as the weights are decoded
-      }
+      if (mx) decode = 1;  // per-32 scales are applied as the weights are decoded
       e = decode ? gmmk::launch_scaled(S, true, f32, dev.sms, s) : gmmk::launch_fp8(S, gmmk::kWeightE4M3, f32, dev.sms, s);
+    } else if (nvfp4) {
+      e = gmmk::launch_scaled_nvfp4(S, f32, dev.sms, s);
     } else {
       const int fmt = rhs_dtype == GMM_DTYPE_E5M2   ? gmmk::kWeightE5M2
                       : rhs_dtype == GMM_DTYPE_INT8  ? gmmk::kWeightInt8

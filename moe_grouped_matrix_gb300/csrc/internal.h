@@ -77,10 +77,15 @@ struct ScaledLaunch {
   int32_t lhs_e4m3;                 // lhs holds e4m3 codes (fp8 kernels only)
   const float* lhs_scale;           // lhs_e4m3: NULL or f32 [m, num_lhs_blocks]
   int32_t num_lhs_blocks;
-  const uint8_t* mx_scale;          // decoding kernel, e4m3 weights: NULL or E8M0 [L, n, k / 32]
+  const uint8_t* mx_scale;          // decoding kernel: NULL, E8M0 [L, n, k / 32] (e4m3 weights) or
+                                    // e4m3 [L, n, k / 16] (e2m1 weights)
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
+// NVFP4 on the decoding kernel: e2m1 weights (tm_rhs over the packed bytes
+// [L, n, k / 2], box {64, 128, 1}, no swizzle) with e4m3 block scales per 16 k
+// in mx_scale.
+cudaError_t launch_scaled_nvfp4(const ScaledLaunch& p, bool out_f32, int grid, cudaStream_t stream);
 
 // The same operation for 8- and 4-bit weights on the fp8 tensor cores (the
 // bf16 activations are split exactly into two e4m3 terms; e4m3 / e5m2 weights

@@ -102,6 +102,8 @@ def call_gmm_ex(lib, **over):
     (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=32, bscale_dtype=2), 2),
     (dict(bscale=FAKE, bsize=32), 2),                                     # e4m3 activations
     (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=16), 3),
+    (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=32, rhs_dtype=7, bscale_dtype=2), 3),
+    (dict(lhs_dtype=0, lscale=None, scale_dtype=1, bscale=FAKE, bsize=16, rhs_dtype=7, bscale_dtype=8), 2),
 ])
 def test_gmm_ex_host_validation(lib, over, status):
     assert call_gmm_ex(lib, **over) == status

@@ -108,3 +108,64 @@ def test_mxfp8_decode_workload_sampled_rows():
     rows = np.random.default_rng(6).choice(m, 20, replace=False)
     ref, mag = _oracle(wl["lhs"], wl["rhs"], sizes, mx, rhs_scale=wl["rhs_scale"], bias=wl["rhs_bias"], rows=rows)
     check_close(out[torch.from_numpy(rows).to(DEV)], ref, mag, "MXFP8 decode workload")
+
+
+# ------------------------------------------------------------------ NVFP4
+def _nvfp4_scales(shape, seed):
+    # positive e4m3 block scales spanning 2^-4 .. 2^4, one NaN-free code set
+    return W.uniform(shape, 0.0625, 16.0, seed, DEV).to(torch.float8_e4m3fn)
+
+
+def _oracle_fp4(lhs, rhs, sizes, bs, go=0, rhs_scale=None, bias=None, rows=None):
+    return oracle.gmm(W.stored_bits(lhs), W.stored_bits(rhs), sizes, group_offset=go,
+                      rhs_scale=None if rhs_scale is None else W.stored_bits(rhs_scale),
+                      rhs_bias=None if bias is None else W.stored_bits(bias), rows=rows, rhs_dtype=oracle.E2M1,
+                      rhs_block_scale=W.stored_bits(bs), rhs_block_scale_dtype=oracle.E4M3)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("with_scale", [False, True])
+def test_nvfp4_matches_oracle(with_scale, out_dtype):
+    m, k, n, L = 200, 512, 384, 6
+    lhs = W.normal((m, k), 1.0, 101, DEV)
+    rhs = W.weights("e2m1", (L, n, k), 102, DEV)
+    bs = _nvfp4_scales((L, n, k // 16), 103)
+    tensor_scale = W.uniform((L, 1, 1, n), 0.5, 2.0, 104, DEV) if with_scale else None
+    bias = W.normal((L, 1, n), 1.0, 105, DEV)
+    out = G.gmm(lhs, rhs, torch.tensor(SIZES, device=DEV), rhs_scale=tensor_scale, rhs_bias=bias,
+                rhs_block_scale=bs, rhs_format="e2m1", out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = _oracle_fp4(lhs, rhs, SIZES, bs, rhs_scale=tensor_scale, bias=bias)
+    check_close(out, ref, mag, f"NVFP4 (tensor scale {with_scale})")
+
+
+def test_nvfp4_every_code_and_group_offset():
+    # every e2m1 code in both nibbles of every weight row, exact integer-valued activations
+    m, k, n, L, go = 64, 256, 128, 2, 1
+    lhs = W.integer_valued((m, k), -4, 4, 111, DEV)
+    codes = torch.arange(256, dtype=torch.int32, device=DEV).remainder(256).to(torch.uint8)
+    rhs = codes.repeat(L * n * (k // 2) // 256).reshape(L, n, k // 2)
+    bs = _nvfp4_scales((L, n, k // 16), 112)
+    sizes = np.array([10, 30, 24], np.int32)
+    out = G.gmm(lhs, rhs, torch.tensor(sizes, device=DEV), rhs_block_scale=bs, rhs_format="e2m1",
+                group_offset=go, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = _oracle_fp4(lhs, rhs, sizes, bs, go=go)
+    check_close(out, ref, mag, "NVFP4 every code")
+
+
+def test_nvfp4_decode_workload_sampled_rows():
+    wl = W.fp8_decode(DEV, fmt="e2m1")
+    sizes = wl["group_sizes"]
+    m, k = wl["lhs"].shape
+    L, n = wl["rhs"].shape[0], wl["rhs"].shape[1]
+    bs = _nvfp4_scales((L, n, k // 16), 121)
+    out = G.gmm(wl["lhs"], wl["rhs"], torch.tensor(sizes, device=DEV), rhs_block_scale=bs, rhs_format="e2m1",
+                rhs_bias=wl["rhs_bias"])
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    rows = np.random.default_rng(7).choice(m, 20, replace=False)
+    ref, mag = _oracle_fp4(wl["lhs"], wl["rhs"], sizes, bs, bias=wl["rhs_bias"], rows=rows)
+    check_close(out[torch.from_numpy(rows).to(DEV)], ref, mag, "NVFP4 decode workload")
