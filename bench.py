@@ -408,6 +408,29 @@ def run_suite(dev, peaks):
     record("w8a8_decode_quantize_plus_gmm", ms, 2 * rows * n * k, bytes_)
     del fd, o, q, a_scale, e8
     torch.cuda.empty_cache()
+
+    # Microscaling weights on the decode workload (bf16 activations, the decoding kernel):
+    # MXFP8 (e4m3, an E8M0 scale per 32 k of a weight row) and NVFP4 (e2m1, an e4m3 scale per 16 k).
+    for name, fmt, per in (("decode_mxfp8_weights", "e4m3", 32), ("decode_nvfp4_weights", "e2m1", 16)):
+        fd = W.fp8_decode(dev, fmt=fmt)
+        sizes = fd["group_sizes"]
+        gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+        L_ = fd["rhs"].shape[0]
+        if fmt == "e4m3":
+            bs = torch.full((L_, n, k // per), 127, dtype=torch.uint8, device=dev)
+        else:
+            bs = W.uniform((L_, n, k // per), 0.5, 2.0, 7, dev).to(torch.float8_e4m3fn)
+        o = torch.empty((fd["lhs"].shape[0], n), dtype=torch.bfloat16, device=dev)
+        kw = {"rhs_format": fd["rhs_format"]} if fd["rhs_format"] else {}
+        rows = float(sizes.sum())
+        live = int((sizes > 0).sum())
+        ms = _time_call(torch, lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_block_scale=bs, rhs_bias=fd["rhs_bias"],
+                                             out=o, **kw))
+        wbytes = n * k // 2 if fmt == "e2m1" else n * k
+        bytes_ = live * (wbytes + n * (k // per) + n * 2) + rows * k * 2 + fd["lhs"].shape[0] * n * 2
+        record(name, ms, 2 * rows * n * k, bytes_)
+        del fd, o, bs
+        torch.cuda.empty_cache()
     return res
 
 
