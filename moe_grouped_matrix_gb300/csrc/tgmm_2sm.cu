@@ -102,18 +102,19 @@ __device__ __forceinline__ void stage_row(uint32_t slice, int lane, const float*
 // Zeroes rows [valid, valid rounded up to 16) of this stage's B boxes in both
 // CTAs (the rows belong to the next group or lie past m).  A row is 128
 // contiguous bytes (the swizzle permutes 16-byte chunks within a row only).
-// All 32 lanes of the leader's MMA warp.
+// All 32 lanes of the leader's MMA warp, lanes over (row, 16-byte chunk).
 __device__ __forceinline__ void zero_b_tail(uint32_t b0, int32_t valid, int lane) {
   constexpr int kB = int(B_BYTES / BOX_BYTES);
   const uint32_t b0_peer = mapa_shared(b0, 1);
   const int32_t zrows = ((valid + 15) & ~15) - valid;
-  const int32_t units = zrows * kB * 8;
-  for (int32_t u = lane; u < units; u += 32) {
-    const int32_t box = u / (zrows * 8);
-    const int32_t rem = u - box * zrows * 8;
-    const uint32_t off = uint32_t(box) * BOX_BYTES + uint32_t(valid + rem / 8) * 128u + uint32_t(rem % 8) * 16u;
-    st_shared_v4(b0 + off, 0u, 0u, 0u, 0u);
-    st_shared_cluster_v4(b0_peer + off, 0u, 0u, 0u, 0u);
+  const uint32_t chunk = uint32_t(lane & 7) * 16u;
+#pragma unroll
+  for (int box = 0; box < kB; ++box) {
+    for (int32_t zr = lane >> 3; zr < zrows; zr += 4) {
+      const uint32_t off = uint32_t(box) * BOX_BYTES + uint32_t(valid + zr) * 128u + chunk;
+      st_shared_v4(b0 + off, 0u, 0u, 0u, 0u);
+      st_shared_cluster_v4(b0_peer + off, 0u, 0u, 0u, 0u);
+    }
   }
   fence_proxy_async_smem();
   fence_proxy_async_cluster();
@@ -238,17 +239,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t a0 = sbase + OFF_A + stage * A_BYTES;
           const uint32_t b0 = sbase + OFF_B + stage * B_BYTES;
           const int32_t valid = min(BR, rows - c * BR);
-          if (valid < BR) zero_b_tail(b0, valid, lane);
-          tc_fence_after();
-          if (lane == 0) {
-            const int32_t ksteps = (valid + 15) / 16;
-            for (int32_t kk = 0; kk < ksteps; ++kk) {
+          const int32_t ksteps = (valid + 15) / 16, kfull = valid / 16;
+          auto issue = [&](int32_t k0, int32_t k1) {
+            for (int32_t kk = k0; kk < k1; ++kk) {
               const uint64_t ad = sw128_desc(a0 + kk * 2048, BOX_BYTES, 1024);
               const uint64_t bd = sw128_desc(b0 + kk * 2048, BOX_BYTES, 1024);
               mma_bf16_ss_pair(d_tmem, ad, bd, kIdesc, (c | kk) != 0 ? 1u : 0u);
             }
-            mma_commit_pair(empty_bar(stage), 0x3);
+          };
+          tc_fence_after();
+          // the 16-row blocks of this group's rows only go first; the tail block
+          // is fixed up while they run
+          if (lane == 0) issue(0, kfull);
+          if (kfull < ksteps) {
+            zero_b_tail(b0, valid, lane);
+            tc_fence_after();
+            if (lane == 0) issue(kfull, ksteps);
           }
+          if (lane == 0) mma_commit_pair(empty_bar(stage), 0x3);
           __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
