@@ -37,14 +37,19 @@
 // sub-tiles (2, i.e. 256 k; 1 for int8, whose tiles are twice the MMA work);
 // the last step of an item may hold fewer.  Roles:
 //   warp 0      TMA: the step's raw weight boxes (4-deep ring) and its bf16
-//               token rows ({64 k, 16 rows} boxes, 2-deep ring)
+//               token rows ({64 k, 16 rows} boxes, 2-deep ring); with e4m3
+//               activations the e4m3 token rows ({128 k, 16 rows} boxes)
+//               straight into a 4-deep operand ring
 //   warps 6-9   split the bf16 token rows into e4m3 h / l operand rows (2-deep
 //               ring; all 128 threads share any chunk size) and write each
-//               row's step scale (8-deep ring)
-//   warps 10-13 (converted formats) rewrite raw weight tiles as e4m3 A tiles
-//               (2-deep ring), one weight row per thread
-//   warp 1      TMEM owner; per step 4 MMAs 128 x (2 T8) x 32 per A tile, one
-//               accumulator per sub-tile, and one commit into a step-done ring
+//               row's step scale (8-deep ring); with e4m3 activations warp 6
+//               alone writes each sub-tile's token scales
+//   next 4 or 8 (int8, int4, uint4) rewrite raw weight tiles as e4m3 A tiles
+//               (2-deep ring): one weight row per thread, or half a row with
+//               e4m3 activations (8 warps)
+//   warp 1      TMEM owner; per step 4 MMAs 128 x N x 32 per A tile (N = 2 T8,
+//               or 16 / 32 e4m3 token rows), one accumulator per sub-tile,
+//               and one commit into a step-done ring
 //   warps 2-5   per sub-tile: TMEM -> registers, fold with the token scale and
 //               the sub-tile's weight-block scale into fp32 registers; per item
 //               add the bias, round, store
