@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(&tm_out, slices + slot * SLICE_BYTES, col, krow0, g);
+        tma_store_3d_hint(&tm_out, slices + slot * SLICE_BYTES, col, krow0, g, l2_policy_evict_first());
         tma_store_commit();
       }
       slot ^= 1u;
