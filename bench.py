@@ -362,6 +362,21 @@ def run_suite(dev, peaks):
     del fd, o
     torch.cuda.empty_cache()
 
+    # bf16 weights with the same per-block scales and bias (the decoding kernel's bf16 path).
+    fd = W.fp8_decode(dev)
+    sizes = fd["group_sizes"]
+    gs = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    w16 = fd["rhs"].to(torch.bfloat16)
+    del fd["rhs"]
+    o = torch.empty((fd["lhs"].shape[0], n), dtype=torch.bfloat16, device=dev)
+    rows = float(sizes.sum())
+    live = int((sizes > 0).sum())
+    ms = _time_call(torch, lambda: G.gmm(fd["lhs"], w16, gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"], out=o))
+    bytes_ = live * (n * k * 2 + nb * n * 4 + n * 2) + rows * k * 2 + fd["lhs"].shape[0] * n * 2
+    record("decode_bf16_weights_scaled", ms, 2 * rows * n * k, bytes_)
+    del fd, o, w16
+    torch.cuda.empty_cache()
+
     # The decode workload with the other weight formats of the pages' dtype list (group_offset 0).
     for fmt in ("e5m2", "int8", "int4", "uint4", "e2m1"):
         fd = W.fp8_decode(dev, fmt=fmt)
