@@ -341,7 +341,11 @@ def run_suite(dev, peaks):
     dw = torch.empty((128, 2048, 2048), dtype=torch.float32, device=dev)
     ms = _time_call(torch, lambda: G.tgmm(mo["lhs"], mo["dout"], gs, out=dw))
     record("moe128_tgmm_f32", ms, 2 * rows * 2048 * 2048, rows * 2048 * 2 * 2 + dw.numel() * 4)
-    del mo, dw
+    del dw
+    dwb = torch.empty((128, 2048, 2048), dtype=torch.bfloat16, device=dev)
+    ms = _time_call(torch, lambda: G.tgmm(mo["lhs"], mo["dout"], gs, out=dwb))
+    record("moe128_tgmm_bf16", ms, 2 * rows * 2048 * 2048, rows * 2048 * 2 * 2 + dwb.numel() * 2)
+    del mo, dwb
     torch.cuda.empty_cache()
 
     fd = W.fp8_decode(dev)
