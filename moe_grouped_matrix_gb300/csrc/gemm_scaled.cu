@@ -129,30 +129,43 @@ __device__ __forceinline__ uint32_t e4m3_bf16x2(uint32_t code) {
 
 // 32 e2m1 codes (16 bytes, the even k in the low nibble) -> 32 bf16 (16 words,
 // k order: words 0..7 in lo, 8..15 in hi), the first 16 times s_lo and the
-// last 16 times s_hi (bf16x2 scale factors).  A code's 3 magnitude bits placed at bf16 bits 6..8 under its sign
-// bit give the bf16 number 2^-126 times its value (exponent field = the code's
-// exponent, the mantissa bit as bf16's top mantissa bit; code exponent 0 is
-// then the subnormal 2^-127 = 2^-126 * 0.5).  Two bf16x2 fmas multiply by 2^126
-// and by the block scale, exactly (a product of an e2m1 and an e4m3 value has
-// at most 6 significant bits).
+// last 16 times s_hi (bf16x2 scale factors).  Per 4 codes (16 bits, k order):
+// two byte permutes look the high and low bytes of each code's bf16 value up
+// in 8-entry tables indexed by the code's magnitude bits, a third replicates
+// each code's sign into a mask whose bit 7 per byte is the sign, and two more
+// interleave low and high bytes into two bf16x2 words.  The bf16x2 fma by the
+// block scale is exact (an e2m1 value times an e4m3 value has at most 6
+// significant bits).
 __device__ __forceinline__ void decode_fp4_32(const uint4 raw, uint32_t s_lo, uint32_t s_hi, uint32_t (&lo)[8],
                                               uint32_t (&hi)[8]) {
+  // bf16 of the magnitudes 0, 0.5, 1, 1.5 | 2, 3, 4, 6: high bytes, low bytes
+  constexpr uint32_t kH0 = 0x3F3F3F00u, kH1 = 0x40404040u;
+  constexpr uint32_t kL0 = 0xC0800000u, kL1 = 0xC0804000u;
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t u = w[i] & 0x0F0F0F0Fu, v = (w[i] >> 4) & 0x0F0F0F0Fu;  // even-k / odd-k codes per byte
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // byte j's even-k code at bits 0..3, its odd-k code at bits 16..19
-      const uint32_t t = __byte_perm(u, v, uint32_t(j) | (uint32_t(4 + j) << 8));
-      const uint32_t x = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
-      uint32_t y;
-      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(x), "r"(0x7E807E80u), "r"(0x80008000u));
-      asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(y), "r"(i < 2 ? s_lo : s_hi), "r"(0x80008000u));
-      if (i < 2)
-        lo[4 * i + j] = y;
-      else
-        hi[4 * (i - 2) + j] = y;
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t codes = half == 0 ? w[i] : (w[i] >> 16);
+      const uint32_t idx = codes & 0x7777u;
+      // prmt's default mode: a selector nibble with bit 3 set replicates the
+      // selected byte's sign, giving 0xFF for negative codes and 0x80 otherwise
+      uint32_t rep;
+      asm("prmt.b32 %0, %1, %2, %3;" : "=r"(rep) : "r"(0x80808080u), "r"(0x80808080u), "r"(codes));
+      const uint32_t sign = (rep << 1) & 0x80808080u;
+      const uint32_t hb = __byte_perm(kH0, kH1, idx) | sign;
+      const uint32_t lb = __byte_perm(kL0, kL1, idx);
+      const uint32_t s2 = i < 2 ? s_lo : s_hi;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t y = __byte_perm(lb, hb, j == 0 ? 0x5140u : 0x7362u);
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(y), "r"(s2), "r"(0x80008000u));
+        const int word = 4 * i + 2 * half + j;  // values 2 word, 2 word + 1
+        if (word < 8)
+          lo[word] = y;
+        else
+          hi[word - 8] = y;
+      }
     }
   }
 }
