@@ -277,3 +277,40 @@ def test_unknown_kernel_override_is_rejected(monkeypatch):
     w = W.normal((1, 64, 64), 0.05, 2, DEV)
     with pytest.raises(G.GmmError):
         G.gmm(lhs, w, _gs([64]))
+
+
+# ------------------------------------------------------------------ the largest group count
+def _max_groups_sizes(seed):
+    rng = np.random.default_rng(seed)
+    sizes = rng.integers(0, 4, 1024).astype(np.int32)   # GMM_MAX_GROUPS groups, many empty
+    return sizes
+
+
+def test_max_groups_forward(kernel):
+    sizes = _max_groups_sizes(31)
+    _gmm_case(int(sizes.sum()) + 5, 128, 128, sizes, seed=31)
+
+
+def test_max_groups_tgmm(tgmm_kernel):
+    sizes = _max_groups_sizes(32)
+    m = int(sizes.sum()) + 3
+    lhs = W.normal((m, 128), 1.0, 33, DEV)
+    dout = W.normal((m, 128), 1.0, 34, DEV)
+    dw = G.tgmm(lhs, dout, _gs(sizes))
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = oracle_tgmm(lhs, dout, sizes)
+    check_close(dw, ref, mag, "tgmm with 1024 groups")
+
+
+def test_max_groups_fp8_weights():
+    sizes = _max_groups_sizes(35)
+    m = int(sizes.sum()) + 2
+    lhs = W.normal((m, 128), 1.0, 36, DEV)
+    rhs = W.weights("e4m3", (1024, 128, 128), 37, DEV)
+    scale = W.uniform((1024, 1, 1, 128), 0.5 / 448, 2.0 / 448, 38, DEV)
+    out = G.gmm(lhs, rhs, _gs(sizes), rhs_scale=scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = oracle_gmm(lhs, rhs, sizes, rhs_scale=scale)
+    check_close(out, ref, mag, "fp8 weights with 1024 groups")
