@@ -395,10 +395,17 @@ def run_suite(dev, peaks):
         local = sizes[go:]
         rows = float(local.sum())
         live = int((local > 0).sum())
-        ms = _time_call(torch, lambda: G.gmm(fd["lhs"], rhs, gs, rhs_scale=sc, rhs_bias=bi, group_offset=go, out=o))
+        call = lambda: G.gmm(fd["lhs"], rhs, gs, rhs_scale=sc, rhs_bias=bi, group_offset=go, out=o)
         # weights, scales and bias of non-empty local experts, their lhs rows, the whole output
         bytes_ = live * (n * k + nb * n * 4 + n * 2) + rows * k * 2 + fd["lhs"].shape[0] * n * 2
-        record(f"fp8_decode_go{go}", ms, 2 * rows * n * k, bytes_)
+        # the default: the activation rows split once by a pass, then the fp8 kernel
+        record(f"fp8_decode_go{go}", _time_call(torch, call), 2 * rows * n * k, bytes_)
+        # the same call with the split made inside the kernel for every weight tile
+        os.environ["GMM_FP8_ACT_SPLIT"] = "kernel"
+        try:
+            record(f"fp8_decode_go{go}_split_in_kernel", _time_call(torch, call), 2 * rows * n * k, bytes_)
+        finally:
+            del os.environ["GMM_FP8_ACT_SPLIT"]
     del fd, o
     torch.cuda.empty_cache()
 

@@ -23,9 +23,10 @@
  *    that timed out) set sticky flags in the workspace; the call still
  *    completes, treating negative sizes as 0 and cutting the groups at row m.
  *    Read them with gmm_read_device_errors().
- *  - The workspace is caller-owned device memory of at least
- *    gmm_workspace_bytes() bytes, 256-byte aligned, zero-filled once before
- *    its first use.  Calls that share a workspace must be stream-ordered.
+ *  - The workspace is caller-owned device memory of gmm_workspace_bytes()
+ *    bytes (at least GMM_WORKSPACE_MIN_BYTES), 256-byte aligned, zero-filled
+ *    once before its first use.  Calls that share a workspace must be
+ *    stream-ordered.
  *  - Requires the current device to be compute capability 10.3 (GB300).
  */
 #ifndef LIBGMM_H_
@@ -61,7 +62,7 @@ enum {
   GMM_ERR_SHAPE = 3,        /* inconsistent or unsupported sizes */
   GMM_ERR_ALIGN = 4,        /* a pointer is not 16-byte aligned or a row pitch is not a multiple of 16 bytes */
   GMM_ERR_GROUP_OFFSET = 5, /* group_offset outside [0, num_total_groups - num_local_groups] */
-  GMM_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or smaller than gmm_workspace_bytes() */
+  GMM_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or smaller than GMM_WORKSPACE_MIN_BYTES */
   GMM_ERR_ARCH = 7,         /* current device is not compute capability 10.3 */
   GMM_ERR_CUDA = 8,         /* a CUDA runtime or driver call failed; see gmm_last_cuda_error() */
   GMM_ERR_IO = 9            /* a tiling-table file could not be read, parsed or written */
@@ -76,7 +77,19 @@ enum {
 /* Largest num_total_groups (gmm, tgmm_local) or num_groups (tgmm) accepted. */
 #define GMM_MAX_GROUPS 1024
 
-/* Size in bytes of the workspace every call needs (a small constant). */
+/* Smallest workspace a call accepts: the error flags alone. */
+#define GMM_WORKSPACE_MIN_BYTES 256
+
+/*
+ * Size in bytes of a full workspace (a constant, 16 MiB + 256): the error
+ * flags, then scratch for the 8- and 4-bit weight kernels.  With bf16
+ * activations and e4m3, e5m2 or e2m1 weights, a call whose activations fit
+ * (2 m k + 4 m ceil(k / 256) bytes, rounded, within 16 MiB) first splits each
+ * activation row once into its two exact e4m3 terms there, and the kernel
+ * reads them instead of splitting every row again for each 128-wide weight
+ * tile.  The result is the same, bit for bit.  With a smaller workspace (at
+ * least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
+ */
 size_t gmm_workspace_bytes(void);
 
 /*
@@ -113,7 +126,11 @@ size_t gmm_workspace_bytes(void);
  *                2^14 of the step's largest magnitude (smaller ones are off by at most 2^-21
  *                of it); a NaN or infinity in a row makes that output row NaN.
  *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
- *                value than auto, mma or decode: GMM_ERR_SHAPE).
+ *                value than auto, mma or decode: GMM_ERR_SHAPE).  With a full workspace the
+ *                split of bf16 activations is made once per row (see gmm_workspace_bytes);
+ *                GMM_FP8_ACT_SPLIT = kernel keeps it in the kernel, pre requires the pass
+ *                (GMM_ERR_WORKSPACE if it does not fit; any other value than auto, kernel or
+ *                pre: GMM_ERR_SHAPE).
  *                Without scale, bf16 weights run on one of four kernels chosen from the average
  *                group size m / num_total_groups: SM-pair 256x256 row tiles (>= 1024 rows),
  *                SM-pair tiles of 256 weight rows x up to 256 group rows rounded to 32 (>= 16),

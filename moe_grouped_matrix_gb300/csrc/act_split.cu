@@ -1,0 +1,71 @@
+// The exact two-term e4m3 split of bf16 activation rows, made once per row
+// for the fp8 kernel's split-activation mode (gemm_fp8.cuh, kPS), which would
+// otherwise make it once per row and 128-wide weight tile.  For each row r and
+// each k step s (256 wide; the last one 128 wide when k % 256 == 128), with M
+// the largest |x| of the step and e its biased exponent clamped to [8, 254]:
+//   y = x * 2^(134 - e),  h = rne_e4m3(y),  l = rne_e4m3(16 (y - h)),
+//   planes[0][r, kk] = h,  planes[1][r, kk] = l,
+//   scale[r, s] = 2^(e - 134)   (NaN when M is an infinity or a NaN),
+// so that x = scale * (h + l / 16) (see the exactness argument in
+// gemm_fp8.cuh).  The arithmetic is the kernel's own split_e4m3 and exponent
+// rule, so both modes give the same codes.
+// One warp per (row, step), 8 values per lane.  HBM-bound: 2 bytes read and 2
+// written per value.
+#include <cuda_bf16.h>
+
+#include <climits>
+
+#include "gemm_fp8.cuh"
+
+namespace gmmk {
+namespace {
+
+__global__ void __launch_bounds__(256) act_split_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
+                                                       int32_t ksteps, uint8_t* __restrict__ planes,
+                                                       float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // (row, step)
+  if (w >= m * ksteps) return;
+  const int64_t row = w / ksteps;
+  const int32_t s = int32_t(w - row * ksteps);
+  const int64_t kk = int64_t(s) * 256 + lane * 8;
+  const bool mine = kk < k;  // k % 128 == 0: a 128-wide last step fills lanes 0-15
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (mine) v = *reinterpret_cast<const uint4*>(x + row * k + kk);
+  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) amax = max(amax, max((xw[i] << 16) & 0x7FFFFFFFu, xw[i] & 0x7FFF0000u));
+  amax = __reduce_max_sync(0xffffffffu, amax);
+  const uint32_t e = min(max(amax >> 23, 8u), 254u);
+  const float inv_s = __uint_as_float((261u - e) << 23);
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    y[2 * i] = __uint_as_float(xw[i] << 16) * inv_s;
+    y[2 * i + 1] = __uint_as_float(xw[i] & 0xFFFF0000u) * inv_s;
+  }
+  uint32_t hw[2], lw[2];
+  fp8::split_e4m3<8>(y, hw, lw);
+  if (mine) {
+    *reinterpret_cast<uint2*>(planes + row * k + kk) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(planes + (m + row) * k + kk) = make_uint2(lw[0], lw[1]);
+  }
+  if (lane == 0)
+    scale[row * ksteps + s] = amax < 0x7F800000u ? __uint_as_float((e - 7u) << 23) : __uint_as_float(0x7FC00000u);
+}
+
+}  // namespace
+
+cudaError_t launch_act_split(const void* x, int64_t m, int64_t k, void* planes, float* scale, cudaStream_t stream) {
+  const int64_t ksteps = (k + 255) / 256;
+  const int64_t warps = m * ksteps;
+  if (warps == 0) return cudaSuccess;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  act_split_kernel<<<unsigned(blocks), 256, 0, stream>>>(static_cast<const uint16_t*>(x), m, k, int32_t(ksteps),
+                                                        static_cast<uint8_t*>(planes), scale);
+  return cudaGetLastError();
+}
+
+}  // namespace gmmk

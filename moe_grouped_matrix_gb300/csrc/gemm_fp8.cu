@@ -5,6 +5,7 @@
 namespace gmmk {
 
 cudaError_t launch_fp8(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream) {
+  if (p.lhs_split) return launch_fp8_ps(p, weight_format, out_f32, grid, stream);
   if (p.lhs_e4m3) return launch_fp8_a8(p, weight_format, out_f32, grid, stream);
   switch (weight_format) {
     case kWeightE4M3: return fp8::launch_format<fp8::WFmt::kE4M3, false>(p, out_f32, grid, stream);

@@ -39,7 +39,8 @@
 //   warp 0      TMA: the step's raw weight boxes (4-deep ring) and its bf16
 //               token rows ({64 k, 16 rows} boxes, 2-deep ring); with e4m3
 //               activations the e4m3 token rows ({128 k, 16 rows} boxes)
-//               straight into a 4-deep operand ring
+//               straight into a 4-deep operand ring; with split activations
+//               (below) their h and l rows ({128 k, 8 rows} boxes) likewise
 //   warps 6-9   split the bf16 token rows into e4m3 h / l operand rows (2-deep
 //               ring; all 128 threads share any chunk size) and write each
 //               row's step scale (8-deep ring); with e4m3 activations warp 6
@@ -55,6 +56,14 @@
 //               add the bias, round, store
 // Items are (local group, chunk of up to 32 of its rows, 128-wide n tile); a
 // chunk of t rows uses T8 = 8, 16 or 32 operand rows per half (t rounded up).
+//
+// Split activations (kPS).  The same two-term split of the bf16 rows can be
+// made once per row by act_split.cu, instead of once per row and n tile here:
+// h and l codes of every row in two e4m3 planes and each row's 2^(E-7) per
+// step.  The kernel then loads the chunk's h rows into operand rows [0, T8)
+// and its l rows into [T8, 2 T8), the layout the token split writes, and takes
+// the step scales through the token-scale warp; the MMAs and the fold are
+// those of the bf16 path, so both give the same bits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -80,8 +89,11 @@ constexpr uint32_t RT_STRIP = BT * 128;  // 64 k of bf16 for 32 token rows
 constexpr uint32_t RT_BOX = 16 * 128;    // one {64 k, 16 rows} box
 constexpr uint32_t B_SUB = 2 * BT * KQ;  // e4m3 operand sub-tile: 64 rows x 128 bytes
 
-template <WFmt F, bool kA8>
+// kA8: the token operand comes by TMA (e4m3 activations, or with kPS the
+// split activations) and warp 6 writes its scales.
+template <WFmt F, bool kA8, bool kPS = false>
 struct Cfg {
+  static_assert(kA8 || !kPS, "split activations come by TMA");
   static constexpr bool kNibble = F == WFmt::kInt4 || F == WFmt::kUint4;  // 4-bit codes rewritten as e4m3
   static constexpr bool kConv = kNibble || F == WFmt::kInt8;              // weights rewritten in shared memory
   static constexpr int QPS = F == WFmt::kInt8 ? 1 : 2;        // sub-tiles per step
@@ -112,7 +124,7 @@ struct Cfg {
   // the epilogue; step j uses index j % NDONE.
   static constexpr int NDONE = NACC;
   static constexpr uint32_t RT_BYTES = (KS / 64) * RT_STRIP;
-  static constexpr uint32_t B_SUBT = kA8 ? BT * KQ : B_SUB;  // operand sub-tile: 32 or 64 rows
+  static constexpr uint32_t B_SUBT = kA8 && !kPS ? BT * KQ : B_SUB;  // operand sub-tile: 32 or 64 rows
   static constexpr uint32_t B_BYTES = QPS * B_SUBT;
   static constexpr int kConvWarps = kA8 ? 1 : 4;       // token split, or the token-scale warp
   // weight rewrite: 4 warps (one thread per weight row), or 8 (two threads per
@@ -296,11 +308,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&f)[N]) {
   }
 }
 
-template <WFmt F, bool kA8, bool kOutF32>
-__global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
+template <WFmt F, bool kA8, bool kPS, bool kOutF32>
+__global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_rhs,
                     const Params p) {
-  using C = Cfg<F, kA8>;
+  using C = Cfg<F, kA8, kPS>;
   constexpr int QPS = C::QPS, NACC = C::NACC, NDONE = C::NDONE, NSC = C::NSC;
   int32_t go;
   if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
@@ -418,7 +430,21 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
             as = 0;
             aph ^= 1u;
           }
-          if constexpr (kA8) {
+          if constexpr (kPS) {
+            // h and l rows, {128 k, 8 rows} boxes from planes 0 and 1, into
+            // operand rows [0, T8) and [T8, 2 T8) of each sub-tile
+            if (!wait_step_done(j, C::BST)) {
+              ok = false;
+              break;
+            }
+            const int t8 = t8_of(t.row_end - t.row0);
+            mbar_arrive_expect_tx(bfull_bar(rs), uint32_t(hq * 2 * t8) * 128u);
+            for (int h = 0; h < hq; ++h)
+              for (int z = 0; z < 2; ++z)
+                for (int r8 = 0; r8 < t8; r8 += 8)
+                  tma_load_3d(sbase + C::OFF_B + rs * C::B_BYTES + h * C::B_SUBT + uint32_t(z * t8 + r8) * 128u,
+                              &tm_lhs, bfull_bar(rs), (QPS * ks + h) * KQ, t.row0 + r8, z);
+          } else if constexpr (kA8) {
             // e4m3 token rows, one {128 k, 16 rows} box per sub-tile and 16 rows,
             // straight into operand stage rs once step j - BST's MMAs are done.
             if (!wait_step_done(j, C::BST)) {
@@ -467,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
       const GemmTile t = item_of(w);
       const int t8 = t8_of(t.row_end - t.row0);
       // N: the h and l rows of the split (2 T8), or the e4m3 token rows (16 or 32).
-      const uint32_t idesc = idesc_e4m3(BMW, kA8 ? max(t8, 16) : 2 * t8) | (C::kAType << 7);
+      const uint32_t idesc = idesc_e4m3(BMW, kA8 && !kPS ? max(t8, 16) : 2 * t8) | (C::kAType << 7);
       for (int32_t ks = 0; ks < ksteps; ++ks) {
         const int32_t hq = halves(ks);
         const uint32_t afull = C::kConv ? convfull_bar(as) : rawfull_bar(as);
@@ -575,7 +601,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
               }
               const float* ts = tscale + sc * C::SC_PER + (kA8 ? h * BT : 0);
               const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
-              if constexpr (kA8) {
+              if constexpr (kA8 && !kPS) {
                 // one e4m3 product per token: its T8 columns, times the sub-tile's token scale
                 float d[T8];
                 tmem_ld_cols<T8>(col0, d);
@@ -658,7 +684,8 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
     // ---------------------------------------------------------------- token scales
     // e4m3 activations: per step, the token scale of each of its sub-tiles for
     // the item's rows (lhs_scale[row, lhs block of the sub-tile], 1 without
-    // lhs_scale, 0 for operand rows past the chunk).
+    // lhs_scale, 0 for operand rows past the chunk).  Split activations: the
+    // row's 2^(E-7) for the step (lhs_scale[row, step]) for both sub-tiles.
     const int32_t nlb = p.lhs_scale != nullptr ? p.num_lhs_blocks : 1;
     const int32_t q_per_lblock = nq / nlb;  // (k / nlb) % 128 == 0 on this path
     uint32_t sc = 0, scph = 0;
@@ -677,7 +704,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
           float v = 0.f;
           if (h < hq && r < rows)
             v = p.lhs_scale != nullptr
-                    ? __ldg(p.lhs_scale + int64_t(t.row0 + r) * nlb + (QPS * ks + h) / q_per_lblock)
+                    ? __ldg(p.lhs_scale + int64_t(t.row0 + r) * nlb + (kPS ? ks : (QPS * ks + h) / q_per_lblock))
                     : 1.f;
           tscale[sc * C::SC_PER + idx] = v;
         }
@@ -889,10 +916,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8>::kThreads, 1)
   }
 }
 
-template <WFmt F, bool kA8, bool kOutF32>
+template <WFmt F, bool kA8, bool kPS, bool kOutF32>
 cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) {
-  using C = Cfg<F, kA8>;
-  auto kern = gemm_fp8_kernel<F, kA8, kOutF32>;
+  using C = Cfg<F, kA8, kPS>;
+  auto kern = gemm_fp8_kernel<F, kA8, kPS, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
@@ -902,10 +929,12 @@ cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-// bf16 activations (kA8 false: the exact two-term split) or e4m3 ones (kA8 true).
-template <WFmt F, bool kA8>
+// bf16 activations (kA8 false: the exact two-term split), e4m3 ones (kA8
+// true) or split ones (kA8 and kPS).
+template <WFmt F, bool kA8, bool kPS = false>
 cudaError_t launch_format(const ScaledLaunch& L, bool out_f32, int grid, cudaStream_t stream) {
-  return out_f32 ? launch_format<F, kA8, true>(L, grid, stream) : launch_format<F, kA8, false>(L, grid, stream);
+  return out_f32 ? launch_format<F, kA8, kPS, true>(L, grid, stream)
+                 : launch_format<F, kA8, kPS, false>(L, grid, stream);
 }
 
 }  // namespace fp8

@@ -17,7 +17,13 @@
 
 namespace {
 
-constexpr size_t kWorkspaceBytes = 256;
+// Workspace: [0, 256) the sticky error flags; then, used only when the
+// caller's workspace holds all of it, scratch for the split bf16 activations
+// of the fp8 kernels (h / l planes [2, m, k] and step scales [m, ceil(k / 256)]).
+constexpr size_t kWorkspaceMinBytes = 256;
+constexpr size_t kActOffset = 256;
+constexpr size_t kActScratchBytes = size_t(16) << 20;
+constexpr size_t kWorkspaceBytes = kActOffset + kActScratchBytes;
 thread_local int t_last_cuda_error = 0;
 
 int cuda_fail(int code) {
@@ -170,6 +176,19 @@ int choose_e4m3_decode() {
   return 0;
 }
 
+// GMM_FP8_ACT_SPLIT = kernel keeps the two-term split of bf16 activations inside
+// the fp8 kernel (per row and weight tile) instead of a split pass per row;
+// pre insists on the pass (GMM_ERR_WORKSPACE when the workspace cannot hold
+// it).  1: auto, 0: kernel, 2: pre, -1: unknown value.
+int choose_act_split() {
+  if (const char* env = std::getenv("GMM_FP8_ACT_SPLIT")) {
+    if (std::strcmp(env, "kernel") == 0) return 0;
+    if (std::strcmp(env, "pre") == 0) return 2;
+    if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return -1;
+  }
+  return 1;
+}
+
 }  // namespace
 
 extern "C" {
@@ -281,7 +300,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       (rhs_scale && !aligned16(rhs_scale)))
     return GMM_ERR_ALIGN;
   if (rhs_dtype == GMM_DTYPE_E2M1 && (reinterpret_cast<uintptr_t>(rhs) & 31u) != 0) return GMM_ERR_ALIGN;
-  if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < kWorkspaceMinBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
   DeviceInfo dev;
   if (int st = current_device(&dev)) return st;
   if (m == 0) return GMM_OK;
@@ -339,6 +358,36 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.num_lhs_blocks = ext.lhs_scale != nullptr ? ext.num_lhs_blocks : 1;
     S.mx_scale = static_cast<const uint8_t*>(ext.rhs_block_scale);
     const bool f32 = out_dtype == GMM_DTYPE_F32;
+    const int act_split = choose_act_split();
+    if (act_split < 0) return GMM_ERR_SHAPE;
+    // The fp8 kernels; bf16 activations for e4m3, e5m2 and e2m1 weights are
+    // split once per row into the workspace when it has room (act_split.cu).
+    auto fp8_kernel = [&](int fmt) -> int {
+      const bool splittable =
+          !lhs8 && (fmt == gmmk::kWeightE4M3 || fmt == gmmk::kWeightE5M2 || fmt == gmmk::kWeightE2M1);
+      if (splittable && act_split != 0) {
+        const int64_t ksteps = (k + 255) / 256;
+        const size_t scales_at = (kActOffset + size_t(2 * m * k) + 255) & ~size_t(255);
+        const size_t end = scales_at + size_t(m * ksteps) * sizeof(float);
+        if (workspace_bytes >= kWorkspaceBytes && end <= kWorkspaceBytes) {
+          uint8_t* planes = static_cast<uint8_t*>(workspace) + kActOffset;
+          float* scales = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + scales_at);
+          const uint64_t dims[3] = {uint64_t(k), uint64_t(m), 2};
+          const uint32_t box[3] = {128u, 8u, 1u};
+          if (int st = make_map(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, planes, dims, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return st;
+          S.lhs_split = 1;
+          S.lhs_scale = scales;
+          S.num_lhs_blocks = int32_t(ksteps);
+          if (cudaError_t e1 = gmmk::launch_act_split(lhs, m, k, planes, scales, s)) return cuda_fail(e1);
+        } else if (act_split == 2) {
+          return GMM_ERR_WORKSPACE;
+        }
+      }
+      if (cudaError_t e2 = gmmk::launch_fp8(S, fmt, f32, dev.sms, s)) return cuda_fail(e2);
+      return GMM_OK;
+    };
     cudaError_t e;
     if (rhs_dtype == GMM_DTYPE_BF16) {
       e = gmmk::launch_scaled(S, false, f32, dev.sms, s);
@@ -347,7 +396,8 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       if (decode < 0) return GMM_ERR_SHAPE;
       if (decode && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;  // the decoding kernel takes bf16 lhs, f32 scales
       if (mx) decode = 1;  // per-32 scales are applied as the weights are decoded
-      e = decode ? gmmk::launch_scaled(S, true, f32, dev.sms, s) : gmmk::launch_fp8(S, gmmk::kWeightE4M3, f32, dev.sms, s);
+      if (!decode) return fp8_kernel(gmmk::kWeightE4M3);
+      e = gmmk::launch_scaled(S, true, f32, dev.sms, s);
     } else if (nvfp4) {
       e = gmmk::launch_scaled_nvfp4(S, f32, dev.sms, s);
     } else {
@@ -356,7 +406,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
                       : rhs_dtype == GMM_DTYPE_INT4  ? gmmk::kWeightInt4
                       : rhs_dtype == GMM_DTYPE_UINT4 ? gmmk::kWeightUint4
                                                      : gmmk::kWeightE2M1;
-      e = gmmk::launch_fp8(S, fmt, f32, dev.sms, s);
+      return fp8_kernel(fmt);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return GMM_OK;
@@ -554,7 +604,7 @@ int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype,
     return GMM_ERR_SHAPE;
   if (group_offset < 0 || group_offset > num_total_groups - num_local_groups) return GMM_ERR_GROUP_OFFSET;
   if (!aligned16(lhs) || !aligned16(dout) || !aligned16(out)) return GMM_ERR_ALIGN;
-  if (workspace == nullptr || workspace_bytes < kWorkspaceBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < kWorkspaceMinBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
   const int64_t items = int64_t(num_local_groups) * ((k + 127) / 128) * ((n + 255) / 256);
   if (items > INT32_MAX) return GMM_ERR_SHAPE;
   DeviceInfo dev;

@@ -11,9 +11,10 @@
 // library holds until the process exits.  It calls no cudaMalloc, cudaFree or
 // allocating library routine.
 //
-// The kernels' scratch need does not grow with the problem: it is one 32-bit
-// word of device-side error flags, so any problem size the ABI accepts fits
-// the fixed array below; the size check guards the library's own invariant.
+// The kernels need one 32-bit word of device-side error flags, so any problem
+// size the ABI accepts fits the fixed array below.  The optional scratch of a
+// gmm_workspace_bytes() workspace (split bf16 activations for the fp8
+// kernels) is not provided here: those kernels then split inside.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -56,8 +57,7 @@ extern "C" int gmm_noalloc(const void* lhs, int lhs_dtype, int64_t m, int64_t k,
                            int32_t num_total_groups, int32_t group_offset, const float* rhs_scale,
                            int32_t num_quant_blocks, const void* rhs_bias, int bias_dtype, void* out,
                            int out_dtype, void* stream) {
-  const size_t need = gmm_workspace_bytes();
-  if (need > sizeof(g_noalloc_scratch)) return GMM_ERR_WORKSPACE;
+  static_assert(GMM_NOALLOC_SCRATCH_BYTES >= GMM_WORKSPACE_MIN_BYTES, "scratch below the workspace minimum");
   void* scratch = nullptr;
   if (int st = scratch_for_current_device(&scratch)) return st;
   // The flags must start at zero for this call; the array keeps whatever the

@@ -44,7 +44,8 @@ def test_status_strings(lib):
     assert lib.gmm_status_string(0) == b"ok"
     for code in range(1, 10):
         assert lib.gmm_status_string(code) != b"unknown status"
-    assert lib.gmm_workspace_bytes() >= 4
+    # the error flags (256 bytes, the smallest workspace a call accepts), then scratch
+    assert lib.gmm_workspace_bytes() > 256 and lib.gmm_workspace_bytes() % 256 == 0
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
@@ -69,7 +70,7 @@ def call_gmm(lib, fn="gmm", **over):
     (dict(rhs_dtype=4, trhs=0), 2), (dict(rhs_dtype=7, k=200), 3), (dict(rhs_dtype=3, k=192, scale=FAKE, nb=2), 3),
     (dict(G=8, L=4, go=5), 5), (dict(G=8, L=4, go=-1), 5),
     (dict(lhs=ctypes.c_void_p((1 << 20) + 8)), 4), (dict(out=ctypes.c_void_p((1 << 20) + 4)), 4),
-    (dict(ws=None), 6), (dict(ws_bytes=8), 6),
+    (dict(ws=None), 6), (dict(ws_bytes=8), 6), (dict(ws_bytes=255), 6),
 ])
 @pytest.mark.parametrize("fn", ["gmm", "gmm_into"])
 def test_gmm_host_validation(lib, fn, over, status):

@@ -1,0 +1,164 @@
+"""bf16 activations with e4m3, e5m2 and e2m1 weights: the two-term e4m3 split of each
+activation row, made once per row by a pass into the workspace (the default with a full
+workspace) or inside the fp8 kernel for every weight tile (GMM_FP8_ACT_SPLIT=kernel, or a
+workspace of the minimum size).  Both feed the same operand rows and scales to the same MMAs
+and fold, so their outputs must be the same bits.  They must also match the fp64 oracle,
+with groups whose rows span two chunks, a ragged last k step, an n tail, a group_offset
+slice, rows with infinities and NaN, and activations too large for the scratch."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_grouped_matrix_gb300 as G
+from moe_grouped_matrix_gb300 import build as B
+from moe_grouped_matrix_gb300 import workloads as W
+from parity import ORACLE_FORMAT, bits, check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FORMATS = ["e4m3", "e5m2", "e2m1"]
+# Groups of 0..40 rows: chunks of 8, 16 and 32 rows, two groups spanning two chunks.
+SIZES = np.array([3, 0, 17, 1, 40, 0, 8, 16, 5, 33], np.int32)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    B.build()
+    G.load_library()
+    oracle.build()
+
+
+def _inputs(fmt, m, k, n, L, nb, seed):
+    lhs = W.normal((m, k), 1.0, seed, DEV)
+    rhs = W.weights(fmt, (L, n, k), seed + 1, DEV)
+    top = W.FORMAT_MAX[fmt]
+    scale = W.uniform((L, nb, 1, n), 0.5 / top, 2.0 / top, seed + 2, DEV) if nb else None
+    bias = W.normal((L, 1, n), 1.0, seed + 3, DEV)
+    return lhs, rhs, scale, bias, ({"rhs_format": fmt} if fmt in W.PACKED else {})
+
+
+def _both(monkeypatch, call):
+    """The call's output with the split pass and with the in-kernel split."""
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    pre = call()
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    inside = call()
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    monkeypatch.delenv("GMM_FP8_ACT_SPLIT")
+    return pre, inside
+
+
+def _same_bits(a, b):
+    ia = a.view(torch.int16 if a.element_size() == 2 else torch.int32)
+    ib = b.view(torch.int16 if b.element_size() == 2 else torch.int32)
+    nan = torch.isnan(a)
+    assert torch.equal(nan, torch.isnan(b)), "NaN positions differ"
+    assert torch.equal(ia[~nan], ib[~nan]), f"{int((ia != ib).sum())} elements differ"
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16out", "f32out"])
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_pass_equals_kernel_split_and_oracle(fmt, out_dtype, monkeypatch):
+    # k = 640: two 256-wide steps and a 128-wide one; n = 392 ends 8 columns into a tile
+    m, k, n, nb = int(SIZES.sum()) + 9, 640, 392, 5
+    lhs, rhs, scale, bias, kw = _inputs(fmt, m, k, n, SIZES.size, nb, 80)
+    gs = torch.tensor(SIZES, device=DEV)
+    pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias,
+                                                   out_dtype=out_dtype, **kw))
+    _same_bits(pre, inside)
+    ref, mag = oracle.gmm(bits(lhs), bits(rhs), SIZES, rhs_scale=bits(scale), rhs_bias=bits(bias),
+                          rhs_dtype=ORACLE_FORMAT[fmt])
+    check_close(pre, ref, mag, f"{fmt} split pass")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_group_offset_slice_without_scale(fmt, monkeypatch):
+    sizes = np.array([5, 12, 0, 33, 7, 1, 20], np.int32)
+    go, L = 2, 4
+    m, k, n = int(sizes.sum()), 1024, 256
+    lhs, rhs, _, bias, kw = _inputs(fmt, m, k, n, L, 0, 90)
+    gs = torch.tensor(sizes, device=DEV)
+    pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_bias=bias, group_offset=go,
+                                                   out_dtype=torch.float32, **kw))
+    _same_bits(pre, inside)
+    ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, group_offset=go, rhs_bias=bits(bias),
+                          rhs_dtype=ORACLE_FORMAT[fmt])
+    check_close(pre, ref, mag, f"{fmt} go={go}")
+
+
+def test_wide_range_infinities_and_nan(monkeypatch):
+    # rows whose steps span many binades, a row with an infinity and a row with a NaN: the
+    # step scale is NaN there, so those output rows are NaN in both modes
+    sizes = np.array([6, 10], np.int32)
+    m, k, n = 16, 512, 128
+    x = W.normal((m, k), 1.0, 100)
+    ramp = torch.pow(2.0, torch.linspace(-30, 20, k)).to(torch.bfloat16)
+    x[1] = x[1] * ramp
+    x[3, 17] = float("inf")
+    x[12, 300] = float("nan")
+    lhs = x.to(DEV)
+    rhs = W.weights("e4m3", (2, n, k), 101, DEV)
+    scale = W.uniform((2, 4, 1, n), 0.5 / 448, 2.0 / 448, 102, DEV)
+    gs = torch.tensor(sizes, device=DEV)
+    pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32))
+    _same_bits(pre, inside)
+    assert torch.isnan(pre[3]).all() and torch.isnan(pre[12]).all()
+    finite = [r for r in range(m) if r not in (3, 12)]
+    ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, rhs_scale=bits(scale), rhs_dtype=oracle.E4M3)
+    check_close(pre[finite], ref[finite], mag[finite], "wide range")
+
+
+def test_minimum_workspace_splits_inside(monkeypatch):
+    m, k, n = int(SIZES.sum()), 768, 256
+    lhs, rhs, scale, bias, _ = _inputs("e4m3", m, k, n, SIZES.size, 3, 110)
+    gs = torch.tensor(SIZES, device=DEV)
+    small = torch.zeros(256, dtype=torch.uint8, device=DEV)  # the error flags only
+    full = G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias, out_dtype=torch.float32)
+    minimal = G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias, out_dtype=torch.float32, workspace=small)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0 and G.read_device_errors(workspace=small) == 0
+    _same_bits(full, minimal)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    with pytest.raises(G.GmmError):
+        G.gmm(lhs, rhs, gs, rhs_scale=scale, workspace=small)
+
+
+def test_activations_beyond_the_scratch_split_inside(monkeypatch):
+    # 2 m k = 18.9 MB does not fit the 16 MiB scratch: auto falls back to the in-kernel split
+    m, k, n = 2304, 4096, 128
+    sizes = np.array([1000, 0, 1304], np.int32)
+    lhs, rhs, scale, _, _ = _inputs("e4m3", m, k, n, 3, 32, 120)
+    gs = torch.tensor(sizes, device=DEV)
+    auto = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    inside = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    _same_bits(auto, inside)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    with pytest.raises(G.GmmError):
+        G.gmm(lhs, rhs, gs, rhs_scale=scale)
+    rows = np.array([0, 999, 1000, 2303])
+    ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, rhs_scale=bits(scale), rhs_dtype=oracle.E4M3, rows=rows)
+    check_close(auto[torch.from_numpy(rows).to(DEV)], ref, mag, "beyond the scratch")
+
+
+@pytest.mark.parametrize("go", [0, 32])
+def test_decode_workload_both_modes(go, monkeypatch):
+    fd = W.fp8_decode(torch.device(DEV))
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=DEV)
+    pre, inside = _both(monkeypatch, lambda: G.gmm(fd["lhs"], fd["rhs"][go:], gs, rhs_scale=fd["rhs_scale"][go:],
+                                                   rhs_bias=fd["rhs_bias"][go:], group_offset=go))
+    _same_bits(pre, inside)
+
+
+def test_unknown_setting_is_rejected(monkeypatch):
+    lhs, rhs, scale, _, _ = _inputs("e4m3", 16, 256, 128, 1, 1, 130)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "sometimes")
+    with pytest.raises(G.GmmError):
+        G.gmm(lhs, rhs, torch.tensor([16], dtype=torch.int32, device=DEV), rhs_scale=scale)
