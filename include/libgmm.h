@@ -83,12 +83,12 @@ enum {
 /*
  * Size in bytes of a full workspace (a constant, 16 MiB + 256): the error
  * flags, then scratch for the 8- and 4-bit weight kernels.  With bf16
- * activations and e4m3, e5m2 or e2m1 weights, a call whose activations fit
- * (2 m k + 4 m ceil(k / 256) bytes, rounded, within 16 MiB) first splits each
- * activation row once into its two exact e4m3 terms there, and the kernel
- * reads them instead of splitting every row again for each 128-wide weight
- * tile.  The result is the same, bit for bit.  With a smaller workspace (at
- * least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
+ * activations, a call of those kernels whose activations fit (2 m k + 4 m
+ * ceil(k / 256) bytes, 4 m k / 128 for int8 weights, rounded, within 16 MiB)
+ * first splits each activation row once into its two exact e4m3 terms there,
+ * and the kernel reads them instead of splitting every row again for each
+ * 128-wide weight tile.  The result is the same, bit for bit.  With a smaller
+ * workspace (at least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
  */
 size_t gmm_workspace_bytes(void);
 

@@ -19,7 +19,7 @@ namespace {
 
 // Workspace: [0, 256) the sticky error flags; then, used only when the
 // caller's workspace holds all of it, scratch for the split bf16 activations
-// of the fp8 kernels (h / l planes [2, m, k] and step scales [m, ceil(k / 256)]).
+// of the fp8 kernels (h / l planes [2, m, k] and step scales [m, k steps]).
 constexpr size_t kWorkspaceMinBytes = 256;
 constexpr size_t kActOffset = 256;
 constexpr size_t kActScratchBytes = size_t(16) << 20;
@@ -360,13 +360,12 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     const int act_split = choose_act_split();
     if (act_split < 0) return GMM_ERR_SHAPE;
-    // The fp8 kernels; bf16 activations for e4m3, e5m2 and e2m1 weights are
-    // split once per row into the workspace when it has room (act_split.cu).
+    // The fp8 kernels; bf16 activations are split once per row into the
+    // workspace when it has room (act_split.cu), in the kernel's k steps.
     auto fp8_kernel = [&](int fmt) -> int {
-      const bool splittable =
-          !lhs8 && (fmt == gmmk::kWeightE4M3 || fmt == gmmk::kWeightE5M2 || fmt == gmmk::kWeightE2M1);
-      if (splittable && act_split != 0) {
-        const int64_t ksteps = (k + 255) / 256;
+      if (!lhs8 && act_split != 0) {
+        const int32_t step = fmt == gmmk::kWeightInt8 ? 128 : 256;
+        const int64_t ksteps = (k + step - 1) / step;
         const size_t scales_at = (kActOffset + size_t(2 * m * k) + 255) & ~size_t(255);
         const size_t end = scales_at + size_t(m * ksteps) * sizeof(float);
         if (workspace_bytes >= kWorkspaceBytes && end <= kWorkspaceBytes) {
@@ -380,7 +379,7 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
           S.lhs_split = 1;
           S.lhs_scale = scales;
           S.num_lhs_blocks = int32_t(ksteps);
-          if (cudaError_t e1 = gmmk::launch_act_split(lhs, m, k, planes, scales, s)) return cuda_fail(e1);
+          if (cudaError_t e1 = gmmk::launch_act_split(lhs, m, k, step, planes, scales, s)) return cuda_fail(e1);
         } else if (act_split == 2) {
           return GMM_ERR_WORKSPACE;
         }

@@ -80,7 +80,7 @@ struct ScaledLaunch {
   const uint8_t* mx_scale;          // decoding kernel: NULL, E8M0 [L, n, k / 32] (e4m3 weights) or
                                     // e4m3 [L, n, k / 16] (e2m1 weights)
   int32_t lhs_split;                // fp8 kernels: tm_lhs spans act_split's h / l planes [2, m, k]
-                                    // (box {128, 8, 1}); lhs_scale its [m, ceil(k / 256)] step scales
+                                    // (box {128, 8, 1}); lhs_scale its [m, k steps] step scales
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
@@ -109,11 +109,15 @@ cudaError_t launch_fp8_a8_packed(const ScaledLaunch& p, int weight_format, bool 
                                  cudaStream_t stream);
 cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
                                  cudaStream_t stream);
-// Split activations (lhs_split): e4m3, e5m2 and e2m1 weights.
+// Split activations (lhs_split), every weight format of the fp8 kernel.
 cudaError_t launch_fp8_ps(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
+cudaError_t launch_fp8_ps_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
+                                   cudaStream_t stream);
 // The exact two-term split of bf16 rows [m, k] (k % 128 == 0) into e4m3 h / l
-// planes [2, m, k] and step scales [m, ceil(k / 256)] (act_split.cu).
-cudaError_t launch_act_split(const void* x, int64_t m, int64_t k, void* planes, float* scale, cudaStream_t stream);
+// planes [2, m, k] and step scales [m, ceil(k / step)], step 256 or 128 (the
+// fp8 kernel's k step: 128 for int8 weights) (act_split.cu).
+cudaError_t launch_act_split(const void* x, int64_t m, int64_t k, int32_t step, void* planes, float* scale,
+                             cudaStream_t stream);
 
 // Per-token-group e4m3 quantisation of bf16 activations (quantize.cu); group
 // 64, 128 or 256, k % group == 0.

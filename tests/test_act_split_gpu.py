@@ -1,4 +1,4 @@
-"""bf16 activations with e4m3, e5m2 and e2m1 weights: the two-term e4m3 split of each
+"""bf16 activations with 8- and 4-bit weights: the two-term e4m3 split of each
 activation row, made once per row by a pass into the workspace (the default with a full
 workspace) or inside the fp8 kernel for every weight tile (GMM_FP8_ACT_SPLIT=kernel, or a
 workspace of the minimum size).  Both feed the same operand rows and scales to the same MMAs
@@ -18,7 +18,7 @@ from parity import ORACLE_FORMAT, bits, check_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-FORMATS = ["e4m3", "e5m2", "e2m1"]
+FORMATS = ["e4m3", "e5m2", "e2m1", "int8", "int4", "uint4"]
 # Groups of 0..40 rows: chunks of 8, 16 and 32 rows, two groups spanning two chunks.
 SIZES = np.array([3, 0, 17, 1, 40, 0, 8, 16, 5, 33], np.int32)
 
