@@ -157,6 +157,42 @@ def test_decode_workload_both_modes(go, monkeypatch):
     _same_bits(pre, inside)
 
 
+@pytest.mark.parametrize("fmt,m,k", [("e4m3", 1, 128), ("int8", 1, 128), ("e2m1", 3, 384), ("int4", 9, 256),
+                                     ("uint4", 40, 128)])
+def test_smallest_shapes(fmt, m, k, monkeypatch):
+    # one row; a single 128-wide step (half of a 256-wide one); int8's 128-wide steps
+    sizes = np.array([m], np.int32)
+    lhs, rhs, scale, bias, kw = _inputs(fmt, m, k, 128, 1, 1, 140)
+    gs = torch.tensor(sizes, device=DEV)
+    pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias,
+                                                   out_dtype=torch.float32, **kw))
+    _same_bits(pre, inside)
+    ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, rhs_scale=bits(scale), rhs_bias=bits(bias),
+                          rhs_dtype=ORACLE_FORMAT[fmt])
+    check_close(pre, ref, mag, f"{fmt} m={m} k={k}")
+
+
+@pytest.mark.parametrize("m,fits", [(4064, True), (4080, False)])
+def test_scratch_boundary(m, fits, monkeypatch):
+    # k = 2048: the split rows take 2 m k bytes, then 256-aligned step scales (m * 8 * 4): 4064 rows
+    # fill the 16 MiB scratch but for its last 1 KB, 4080 rows do not fit
+    k, n = 2048, 128
+    sizes = np.array([m // 2, 0, m - m // 2], np.int32)
+    lhs, rhs, scale, _, _ = _inputs("e4m3", m, k, n, 3, 16, 150)
+    gs = torch.tensor(sizes, device=DEV)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    if not fits:
+        with pytest.raises(G.GmmError):
+            G.gmm(lhs, rhs, gs, rhs_scale=scale)
+        return
+    pre = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
+    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    inside = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    _same_bits(pre, inside)
+
+
 def test_unknown_setting_is_rejected(monkeypatch):
     lhs, rhs, scale, _, _ = _inputs("e4m3", 16, 256, 128, 1, 1, 130)
     monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "sometimes")
