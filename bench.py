@@ -274,6 +274,8 @@ def run_gpu(args, rank, world):
         e2e["pipelined"] = True
         e2e["weights"] = "resident on the device (model state); activations and group sizes copied each step"
         e2e["weights_copied_each_step"] = run_e2e(True)
+        if G.read_device_errors(stream=s_mm) != 0:
+            raise RuntimeError("device error flags set during the end-to-end measurement")
         del h_lhs, h_rhs, h_out, d_lhs, d_rhs, d_out
 
     cpu = None

@@ -40,7 +40,7 @@ _TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.fl
 
 _lock = threading.Lock()
 _lib = None
-_workspaces: dict[int, torch.Tensor] = {}
+_workspaces: dict[tuple[int, int], torch.Tensor] = {}
 
 # Every function the header declares, with its ctypes signature.
 _P, _I, _I32, _I64, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
@@ -96,16 +96,24 @@ def load_library() -> ctypes.CDLL:
     return _lib
 
 
-def workspace_for(device: torch.device) -> torch.Tensor:
-    """A zero-filled per-device workspace of gmm_workspace_bytes() bytes (cached)."""
+def workspace_for(device: torch.device, stream=None) -> torch.Tensor:
+    """A zero-filled workspace of gmm_workspace_bytes() bytes for calls on `stream` (default:
+    the device's current stream), cached per (device, stream).  The workspace holds per-call
+    scratch (the split activation rows of the 8- and 4-bit weight kernels) as well as the
+    error flags, so calls on different streams, which may run at the same time, each get
+    their own; calls on one stream are ordered and share it."""
     idx = torch.device(device).index
     if idx is None:
         idx = torch.cuda.current_device()
-    ws = _workspaces.get(idx)
+    dev = torch.device("cuda", idx)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    key = (idx, s.cuda_stream)
+    ws = _workspaces.get(key)
     if ws is None:
         nbytes = int(load_library().gmm_workspace_bytes())
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=torch.device("cuda", idx))
-        _workspaces[idx] = ws
+        with torch.cuda.stream(s):  # zero-filled in order with the stream's calls
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
     return ws
 
 
@@ -151,7 +159,7 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
     _dev(out, "out")
     if tuple(out.shape) != (m, n):
         raise ValueError(f"out must be [{m}, {n}], got {list(out.shape)}")
-    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
     nb = 0
     if rhs_scale is not None:
         _dev(rhs_scale, "rhs_scale")
@@ -254,7 +262,7 @@ def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, ou
     _dev(out, "out")
     if tuple(out.shape) != (L, k, n):
         raise ValueError(f"out must be [{L}, {k}, {n}], got {list(out.shape)}")
-    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
     rc = lib.tgmm_local(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(),
                         G, int(group_offset), L, out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(),
                         _stream(lhs.device, stream))
@@ -277,7 +285,7 @@ def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=No
     if out is None:
         out = torch.empty((G, k, n), dtype=out_dtype, device=lhs.device)
     _dev(out, "out")
-    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
     rc = lib.tgmm(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(), G,
                   out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
     if rc != 0:
@@ -347,7 +355,7 @@ def tune(lhs, rhs, group_sizes, rhs_bias=None, transpose_rhs=True, group_offset=
     if out is None:
         out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
     _dev(out, "out")
-    ws = workspace if workspace is not None else workspace_for(lhs.device)
+    ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
     kern, ras, ms = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_float(0)
     rc = lib.gmm_tune(lhs.data_ptr(), _code(lhs), m, k, rhs.data_ptr(), _code(rhs), rhs.shape[0], n,
                       int(bool(transpose_rhs)), group_sizes.data_ptr(), group_sizes.shape[0], int(group_offset),
@@ -362,7 +370,7 @@ def read_device_errors(device=None, workspace=None, stream=None) -> int:
     """Synchronises the stream and returns (and clears) the sticky device error flags."""
     lib = load_library()
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    ws = workspace if workspace is not None else workspace_for(dev)
+    ws = workspace if workspace is not None else workspace_for(dev, stream)
     flags = ctypes.c_uint32(0)
     rc = lib.gmm_read_device_errors(ws.data_ptr(), _stream(dev, stream), ctypes.byref(flags))
     if rc != 0:

@@ -193,6 +193,31 @@ def test_scratch_boundary(m, fits, monkeypatch):
     _same_bits(pre, inside)
 
 
+def test_two_streams_at_once_keep_their_own_split_rows():
+    # calls on two streams may overlap; each stream's default workspace holds its own split rows
+    sizes = np.array([30, 0, 41, 57], np.int32)
+    m, k, n = int(sizes.sum()), 2048, 512
+    a = _inputs("e4m3", m, k, n, 4, 4, 160)
+    b = _inputs("e4m3", m, k, n, 4, 4, 170)
+    gs = torch.tensor(sizes, device=DEV)
+    call = lambda t: G.gmm(t[0], t[1], gs, rhs_scale=t[2], rhs_bias=t[3], out_dtype=torch.float32)
+    ref_a, ref_b = call(a), call(b)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            oa = call(a)
+        with torch.cuda.stream(s2):
+            ob = call(b)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    assert G.read_device_errors(stream=s1) == 0 and G.read_device_errors(stream=s2) == 0
+    for oa, ob in outs:
+        _same_bits(oa, ref_a)
+        _same_bits(ob, ref_b)
+
+
 def test_unknown_setting_is_rejected(monkeypatch):
     lhs, rhs, scale, _, _ = _inputs("e4m3", 16, 256, 128, 1, 1, 130)
     monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "sometimes")

@@ -106,14 +106,16 @@ def test_one_cuda_graph_serves_several_offsets():
     gs = _gs(SIZES)
     offset = _dev_offset(0)
     out = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
-    G.gmm(lhs, rhs, gs, group_offset=offset, out=out)  # library, workspace and kernel attributes set up
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # library, the stream's workspace and kernel attributes set up
+        G.gmm(lhs, rhs, gs, group_offset=offset, out=out)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
+    with torch.cuda.graph(graph, stream=s):
         G.gmm(lhs, rhs, gs, group_offset=offset, out=out)
     for go in (0, 4, 2):
         offset.fill_(go)
         graph.replay()
         torch.cuda.synchronize()
-        assert G.read_device_errors() == 0
+        assert G.read_device_errors(stream=s) == 0
         assert torch.equal(out, G.gmm(lhs, rhs, gs, group_offset=go)), f"replay with offset {go}"
