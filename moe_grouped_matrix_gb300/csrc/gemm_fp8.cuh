@@ -238,12 +238,18 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // Four 4-bit codes (bits 0..15 of `codes`, k order) -> four e4m3 bytes (k order).
 template <uint32_t T0, uint32_t T1, uint32_t T2, uint32_t T3, bool kSigned>
 __device__ __forceinline__ uint32_t lut4(uint32_t codes) {
+  if constexpr (!kSigned) {
+    // Every entry is below 0x80, so a selector nibble with bit 3 set gives 0
+    // (the replicated sign bit): codes 8..15 read 0 from the low table, and
+    // with bit 3 flipped, codes 0..7 read 0 from the high one.
+    static_assert(((T0 | T1 | T2 | T3) & 0x80808080u) == 0u, "unsigned tables hold positive codes");
+    return prmt(T0, T1, codes) | prmt(T2, T3, codes ^ 0x8888u);
+  }
+  // signed: magnitudes from the two tables, picked and signed by the mask
   const uint32_t idx = codes & 0x7777u;
   const uint32_t upper = prmt(0x80808080u, 0x80808080u, codes);
-  uint32_t r = prmt(T0, T1, idx);
-  if constexpr (T0 != T2 || T1 != T3) r = (prmt(T2, T3, idx) & upper) | (r & ~upper);
-  if constexpr (kSigned) r |= (upper << 1) & 0x80808080u;
-  return r;
+  const uint32_t r = (prmt(T2, T3, idx) & upper) | (prmt(T0, T1, idx) & ~upper);
+  return r | ((upper << 1) & 0x80808080u);
 }
 
 // e4m3 bytes of 0..15 (the unsigned table, also the low half of int4's).
