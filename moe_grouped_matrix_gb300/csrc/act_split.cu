@@ -11,7 +11,8 @@
 // gemm_fp8.cuh).  The arithmetic is the kernel's own split_e4m3 and exponent
 // rule, so both modes give the same codes.
 // One warp per (row, step), 8 (256-wide steps) or 4 values per lane.
-// HBM-bound: 2 bytes read and 2 written per value.
+// HBM-bound: 2 bytes read and 2 written per value.  The fp8 kernel that
+// follows is launched as its programmatic dependent (gemm_fp8.cuh).
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -70,6 +71,10 @@ __global__ void __launch_bounds__(256) act_split_kernel(const uint16_t* __restri
   }
   if (lane == 0)
     scale[row * ksteps + s] = amax < 0x7F800000u ? __uint_as_float((e - 7u) << 23) : __uint_as_float(0x7FC00000u);
+  // The matmul that reads these rows may start now (it waits for this grid's
+  // completion before its first read of them).  Signalled after the work, so
+  // that its CTAs never hold SMs this grid still needs.
+  griddep_launch_dependents();
 }
 
 }  // namespace

@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
       uint32_t apar[C::RAWST], rpar[TR];
       uint32_t j = 0;  // steps loaded so far
       bool ok = true;
+      bool split_ready = false;  // kPS: the split rows' kernel has completed
       for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const GemmTile t = item_of(w);
         const int32_t rboxes = t.row_end - t.row0 > 16 ? 2 : 1;
@@ -444,6 +445,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
               break;
             }
             const int t8 = t8_of(t.row_end - t.row0);
+            if (!split_ready) {  // weights already stream; the split rows come from the kernel before
+              griddep_wait();
+              split_ready = true;
+            }
             mbar_arrive_expect_tx(bfull_bar(rs), uint32_t(hq * 2 * t8) * 128u);
             for (int h = 0; h < hq; ++h)
               for (int z = 0; z < 2; ++z)
@@ -692,6 +697,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     // the item's rows (lhs_scale[row, lhs block of the sub-tile], 1 without
     // lhs_scale, 0 for operand rows past the chunk).  Split activations: the
     // row's 2^(E-7) for the step (lhs_scale[row, step]) for both sub-tiles.
+    if constexpr (kPS) griddep_wait();  // the step scales come from the kernel before
     const int32_t nlb = p.lhs_scale != nullptr ? p.num_lhs_blocks : 1;
     const int32_t q_per_lblock = nq / nlb;  // (k / nlb) % 128 == 0 on this path
     uint32_t sc = 0, scph = 0;
@@ -931,6 +937,23 @@ cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) 
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
            L.lhs_scale, L.num_lhs_blocks};
+  if constexpr (kPS) {
+    // Launched as the programmatic dependent of the split-rows kernel just
+    // before it in the stream: the prologue and the weight stream overlap that
+    // kernel's end; only the split rows and their scales wait for it.  Every
+    // other input was written before that kernel started.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(unsigned(C::kThreads));
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.tm_lhs, L.tm_rhs, p);
+  }
   kern<<<grid, C::kThreads, C::SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

@@ -87,6 +87,16 @@ __device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity) {
 }
 
 // ------------------------------------------------------------------ fences
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream ends;
+// griddep_wait blocks until that kernel has completed and its writes are
+// visible (a no-op without the launch attribute).  griddep_launch_dependents
+// lets the next kernel start once every CTA has issued it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
