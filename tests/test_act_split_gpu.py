@@ -218,6 +218,37 @@ def test_two_streams_at_once_keep_their_own_split_rows():
         _same_bits(ob, ref_b)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "int4"])
+def test_captured_graph_replays_with_new_activations(fmt):
+    # the split pass and the matmul (its programmatic dependent) captured in one CUDA graph,
+    # replayed with new activations and group sizes copied into the captured buffers
+    sizes1 = np.array([7, 0, 19, 33, 4], np.int32)
+    sizes2 = np.array([0, 30, 1, 8, 24], np.int32)
+    m, k, n = 63, 1024, 384
+    lhs, rhs, scale, bias, kw = _inputs(fmt, m, k, n, 5, 4, 180)
+    lhs1, lhs2 = lhs.clone(), W.normal((m, k), 1.0, 185, DEV)
+    gs = torch.tensor(sizes1, device=DEV)
+    out = torch.empty((m, n), dtype=torch.float32, device=DEV)
+    call = lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias, out=out, **kw)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # the stream's workspace and the kernels' attributes set up
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    for x, sizes in ((lhs2, sizes2), (lhs1, sizes1)):
+        ref = G.gmm(x, rhs, torch.tensor(sizes, device=DEV), rhs_scale=scale, rhs_bias=bias,
+                    out_dtype=torch.float32, **kw)
+        lhs.copy_(x)
+        gs.copy_(torch.from_numpy(sizes))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert G.read_device_errors(stream=s) == 0
+        _same_bits(out, ref)
+
+
 def test_unknown_setting_is_rejected(monkeypatch):
     lhs, rhs, scale, _, _ = _inputs("e4m3", 16, 256, 128, 1, 1, 130)
     monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "sometimes")
