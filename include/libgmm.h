@@ -123,7 +123,7 @@ size_t gmm_workspace_bytes(void);
  *                stored, int8, int4 and uint4 rewritten exactly as e4m3 (int8 as 16 * high
  *                nibble + low nibble, two e4m3 terms).  Each lhs row is split per k step (256 wide; 128 for int8)
  *                into two e4m3 terms times a power of two, exactly for every value within
- *                2^14 of the step's largest magnitude (smaller ones are off by at most 2^-21
+ *                2^13 of the step's largest magnitude (smaller ones are off by at most 2^-21
  *                of it); a NaN or infinity in a row makes that output row NaN.
  *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
  *                value than auto, mma or decode: GMM_ERR_SHAPE).  With a full workspace the

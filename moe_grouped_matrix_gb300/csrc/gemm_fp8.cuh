@@ -25,9 +25,9 @@
 // |x / 2^(E-7)| < 256, so h never saturates.  x has 8 significant bits and h the
 // top 4 of them (rounded), so x / 2^(E-7) - h is a multiple of x's last place
 // below half of h's last place: at most 4 significant bits, and 16 times it lies
-// in e4m3's range.  The split is exact for every x with |x| >= M * 2^-14 (where
-// x / 2^(E-7) is an e4m3 normal); below that, l is rounded to a multiple of 2^-9,
-// an error of at most M * 2^-21 in x.  h and l are B operand rows (a token's h
+// in e4m3's range.  The split is exact for every x with |x| >= 2^(E-13), where
+// x / 2^(E-7) is an e4m3 normal: so for every x within 2^13 of M.  Below that,
+// l is rounded to a multiple of 2^-9, an error of at most M * 2^-21 in x.  h and l are B operand rows (a token's h
 // in row i, its l in row T8 + i); their products with the weights are exact and
 // the tensor core sums them in fp32.  Each 128-wide sub-tile accumulates into
 // its own TMEM columns, and the epilogue folds it as

@@ -15,6 +15,7 @@ import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
 from parity import ORACLE_FORMAT, bits, check_close
+from split_statement import split_statement
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -247,6 +248,33 @@ def test_captured_graph_replays_with_new_activations(fmt):
         torch.cuda.synchronize()
         assert G.read_device_errors(stream=s) == 0
         _same_bits(out, ref)
+
+
+@pytest.mark.parametrize("fmt,step", [("e4m3", 256), ("int8", 128)])
+def test_split_rows_equal_a_host_statement_of_the_split(fmt, step):
+    # the pass's h / l planes and step scales, read back from the workspace, bit for bit
+    m, k, n = 37, 640, 128
+    x = W.normal((m, k), 1.0, 190).float()
+    x[1] = 0.0                                                   # a zero row: e clamps to 8
+    x[2] = -0.0                                                  # negative zeros
+    x[3] = x[3] * 1e-30                                          # tiny values
+    x[4] = x[4] * torch.pow(2.0, torch.linspace(-30, 20, k))     # many binades per step
+    x[5, :8] = torch.tensor([128.0, 1.0625, 1.1875, -1.0625, 3.0, 0.0078125, -0.0, 2.0 ** -20])  # ties
+    x[6] = x[6] * 3e4                                            # large values
+    lhs = x.to(torch.bfloat16).to(DEV)
+    rhs = W.weights(fmt, (1, n, k), 191, DEV)
+    G.gmm(lhs, rhs, torch.tensor([m], dtype=torch.int32, device=DEV), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ws = G.workspace_for(torch.device(DEV))
+    ksteps = -(-k // step)
+    planes = ws[256:256 + 2 * m * k].cpu().numpy().reshape(2, m, k)
+    at = (256 + 2 * m * k + 255) // 256 * 256
+    scales = ws[at:at + 4 * m * ksteps].cpu().numpy().view(np.float32).reshape(m, ksteps)
+    want_planes, want_scales = split_statement(bits(lhs), step)
+    bad = np.argwhere(planes != want_planes)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
+    assert np.array_equal(scales.view(np.uint32), want_scales.view(np.uint32))
 
 
 def test_unknown_setting_is_rejected(monkeypatch):
