@@ -116,15 +116,15 @@ def test_small_values_beside_a_large_value_on_zero_weights(fmt, split):
 
 @pytest.mark.parametrize("fmt", ["e4m3", "int8", "int4"])
 def test_three_magnitudes_in_ragged_groups(fmt, split):
-    """Random rows made of three magnitude clusters 2^25 apart, the largest on zero weights for
-    half of the columns, over ragged groups (chunks of 1 to 16 rows, a group across two
+    """Random rows made of three magnitude clusters 2^25 apart, the largest (the first value of
+    every step) on zero weights for half of the columns, over ragged groups (chunks of 1 to 16 rows, a group across two
     chunks), a group_offset slice and a bf16 output."""
     sizes = np.array([5, 0, 23, 1, 9, 14], np.int32)
     m, k, n = int(sizes.sum()) + 3, 768, 264
     step = _step(fmt)
     g = np.random.Generator(np.random.PCG64(303))
-    cluster = g.integers(0, 3, (m, k))
-    cluster[:, ::step] = 0  # every step holds a large value
+    cluster = g.integers(1, 3, (m, k))
+    cluster[:, ::step] = 0  # every step holds a large value, at its first position only
     mant = g.uniform(1, 2, (m, k)) * np.where(g.random((m, k)) < 0.5, -1, 1)
     x = mant * 2.0 ** (-25.0 * cluster)
     lhs = torch.tensor(x).to(torch.bfloat16).to(DEV)
