@@ -83,12 +83,13 @@ enum {
 /*
  * Size in bytes of a full workspace (a constant, 16 MiB + 256): the error
  * flags, then scratch for the 8- and 4-bit weight kernels.  With bf16
- * activations, a call of those kernels whose activations fit (2 m k + 4 m
- * ceil(k / 256) bytes, 4 m k / 128 for int8 weights, rounded, within 16 MiB)
- * first splits each activation row once into its two exact e4m3 terms there,
- * and the kernel reads them instead of splitting every row again for each
- * 128-wide weight tile.  The result is the same, bit for bit.  With a smaller
- * workspace (at least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
+ * activations, a call of those kernels whose split activations fit the
+ * caller's workspace (256 bytes of flags, then 4 m k bytes of e4m3 terms
+ * rounded up to 256, then 8 m ceil(k / 256) bytes of step scales, 8 m k / 128
+ * for int8 weights) first splits each activation row once there, and the kernel
+ * reads the terms instead of splitting every row again for each 128-wide weight
+ * tile.  The result is the same, bit for bit.  With a smaller workspace (at
+ * least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
  */
 size_t gmm_workspace_bytes(void);
 
@@ -118,13 +119,20 @@ size_t gmm_workspace_bytes(void);
  *                transpose_rhs != 0 (else GMM_ERR_DTYPE), k % 128 == 0 and
  *                (k / num_quant_blocks) % 128 == 0 (else GMM_ERR_SHAPE).  These are built for
  *                decode-sized groups (a few rows each) and stream every weight tile once per
- *                chunk of rows of its group (32 rows for e4m3 weights, 16 for bf16).
+ *                chunk of rows of its group (16 rows; 32 for e4m3 activations in gmm_ex).
  *                8- and 4-bit weights run on the fp8 tensor cores: e4m3, e5m2 and e2m1 as
  *                stored, int8, int4 and uint4 rewritten exactly as e4m3 (int8 as 16 * high
- *                nibble + low nibble, two e4m3 terms).  Each lhs row is split per k step (256 wide; 128 for int8)
- *                into two e4m3 terms times a power of two, exactly for every value within
- *                2^13 of the step's largest magnitude (smaller ones are off by at most 2^-21
- *                of it); a NaN or infinity in a row makes that output row NaN.
+ *                nibble + low nibble, two e4m3 terms).  Each bf16 lhs row is split per k step (256 wide;
+ *                128 for int8) into e4m3 terms at two powers of two, which hold every value of
+ *                the step exactly when its magnitudes fall within two ranges of 2^13 (the
+ *                largest value's and the largest of what that leaves): so the products with
+ *                the weights are exact and the tensor cores sum them in fp32, as the pages'
+ *                dot_general does.  A row with a step that the two levels do not hold, or
+ *                that holds an infinity or a NaN, is summed again by the same kernel from the
+ *                stored bf16 values and weights (exact products, fp32 sums, IEEE infinities
+ *                and NaNs); realistic activations almost never need it.  Infinite e5m2
+ *                weights give +-inf or NaN in the columns they touch (the split's terms can
+ *                be zero: inf * 0 is NaN).
  *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
  *                value than auto, mma or decode: GMM_ERR_SHAPE).  With a full workspace the
  *                split of bf16 activations is made once per row (see gmm_workspace_bytes);

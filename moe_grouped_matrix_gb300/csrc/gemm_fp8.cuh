@@ -17,21 +17,30 @@
 // becomes two A tiles whose MMAs add into one accumulator.  The 4-bit formats
 // hold two values per byte, the even k in the low nibble.
 //
-// Activations.  The bf16 lhs rows are brought to e4m3 without losing their
-// value: for each token row and each pipeline step, with M the largest |x| of
-// the row's step and E = floor(log2 M),
-//   x = 2^(E-7) * (h + l / 16),   h = rne_e4m3(x / 2^(E-7)),
-//                                 l = rne_e4m3(16 * (x / 2^(E-7) - h)).
-// |x / 2^(E-7)| < 256, so h never saturates.  x has 8 significant bits and h the
-// top 4 of them (rounded), so x / 2^(E-7) - h is a multiple of x's last place
+// Activations.  The pages multiply bf16 activations by the weights with exact
+// products and fp32 sums (gmm.py, _accum: dot_general with an f32 result).
+// Here each bf16 row is brought to e4m3 without losing its value, per token row
+// and pipeline step (split_step): with M1 the largest |x| of the row's step and
+// E1 = floor(log2 M1),
+//   x = 2^(E1-7) * (h + l / 16) + r,   h = rne_e4m3(x / 2^(E1-7)),
+//                                      l = rne_e4m3(16 * (x / 2^(E1-7) - h)).
+// |x / 2^(E1-7)| < 256, so h never saturates.  x has 8 significant bits and h the
+// top 4 of them (rounded), so x / 2^(E1-7) - h is a multiple of x's last place
 // below half of h's last place: at most 4 significant bits, and 16 times it lies
-// in e4m3's range.  The split is exact for every x with |x| >= 2^(E-13), where
-// x / 2^(E-7) is an e4m3 normal: so for every x within 2^13 of M.  Below that,
-// l is rounded to a multiple of 2^-9, an error of at most M * 2^-21 in x.  h and l are B operand rows (a token's h
-// in row i, its l in row T8 + i); their products with the weights are exact and
-// the tensor core sums them in fp32.  Each 128-wide sub-tile accumulates into
-// its own TMEM columns, and the epilogue folds it as
-//   acc[i] += s[g, b, c] * 2^(E_i-7) * (D[c, i] + D[c, T8 + i] / 16).
+// in e4m3's range.  So r = 0 for every x with |x| >= 2^(E1-13), where
+// x / 2^(E1-7) is an e4m3 normal: every x within 2^13 of M1.  Smaller values
+// leave a rest r (|r| <= 2^(E1-21)), which a second level splits the same way
+// with its own largest magnitude M2: r = 2^(E2-7) * (h2 + l2 / 16) + r2.  The two
+// levels hold every step whose magnitudes lie within two such ranges (a few
+// large values beside small ones, the case one level gets wrong); a step that
+// leaves r2 != 0, or holds an infinity or a NaN, marks its row, and the last
+// CTA to finish computes that row's outputs again from the stored values
+// (fix_marked_rows).  h, l, h2 and l2 are B operand rows (chunk row 8 b + i in
+// rows 32 b + i, + 8, + 16, + 24); their products with the weights are exact
+// and the tensor core sums them in fp32.  Each 128-wide sub-tile accumulates
+// into its own TMEM columns, and the epilogue folds it as
+//   acc[i] += s[g, b, c] * (s1_i * (D_h + D_l / 16) + s2_i * (D_h2 + D_l2 / 16)),
+// reading the h2 / l2 columns only in steps where some row has a second level.
 //
 // Pipeline (one CTA per SM, persistent over items).  A step covers QPS
 // sub-tiles (2, i.e. 256 k; 1 for int8, whose tiles are twice the MMA work);
@@ -40,30 +49,32 @@
 //               token rows ({64 k, 16 rows} boxes, 2-deep ring); with e4m3
 //               activations the e4m3 token rows ({128 k, 16 rows} boxes)
 //               straight into a 4-deep operand ring; with split activations
-//               (below) their h and l rows ({128 k, 8 rows} boxes) likewise
-//   warps 6-9   split the bf16 token rows into e4m3 h / l operand rows (2-deep
-//               ring; all 128 threads share any chunk size) and write each
-//               row's step scale (8-deep ring); with e4m3 activations warp 6
-//               alone writes each sub-tile's token scales
+//               (below) their h, l, h2 and l2 rows ({128 k, 8 rows, 4 planes}
+//               boxes) likewise
+//   warps 6-9   split the bf16 token rows into e4m3 h / l / h2 / l2 operand
+//               rows (2-deep ring; all 128 threads share any chunk size) and
+//               write each row's step scales (8-deep ring); with e4m3
+//               activations warp 6 alone writes each sub-tile's token scales
 //   next 4 or 8 (int8, int4, uint4) rewrite raw weight tiles as e4m3 A tiles
 //               (2-deep ring): one weight row per thread, or half a row with
 //               e4m3 activations (8 warps)
-//   warp 1      TMEM owner; per step 4 MMAs 128 x N x 32 per A tile (N = 2 T8,
-//               or 16 / 32 e4m3 token rows), one accumulator per sub-tile,
-//               and one commit into a step-done ring
-//   warps 2-5   per sub-tile: TMEM -> registers, fold with the token scale and
+//   warp 1      TMEM owner; per step 4 MMAs 128 x N x 32 per A tile (N = 4 T8
+//               split rows, or 16 / 32 e4m3 token rows), one accumulator per
+//               sub-tile, and one commit into a step-done ring
+//   warps 2-5   per sub-tile: TMEM -> registers, fold with the token scales and
 //               the sub-tile's weight-block scale into fp32 registers; per item
 //               add the bias, round, store
-// Items are (local group, chunk of up to 32 of its rows, 128-wide n tile); a
-// chunk of t rows uses T8 = 8, 16 or 32 operand rows per half (t rounded up).
+// Items are (local group, chunk of up to BT of its rows, 128-wide n tile), BT =
+// 16 with bf16 activations and 32 with e4m3 ones; a chunk of t rows uses T8 =
+// 8, 16 or 32 operand rows per term (t rounded up).
 //
-// Split activations (kPS).  The same two-term split of the bf16 rows can be
-// made once per row by act_split.cu, instead of once per row and n tile here:
-// h and l codes of every row in two e4m3 planes and each row's 2^(E-7) per
-// step.  The kernel then loads the chunk's h rows into operand rows [0, T8)
-// and its l rows into [T8, 2 T8), the layout the token split writes, and takes
-// the step scales through the token-scale warp; the MMAs and the fold are
-// those of the bf16 path, so both give the same bits.
+// Split activations (kPS).  The same split of the bf16 rows can be made once
+// per row by act_split.cu, instead of once per row and n tile here: the h, l,
+// h2 and l2 codes of every row in four e4m3 planes and each row's (s1, s2) per
+// step.  The kernel then loads each 8 chunk rows' four terms with one box into
+// the operand layout the token split writes, and takes the step scales through
+// the token-scale warp; the MMAs and the fold are those of the bf16 path, so
+// both give the same bits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -79,21 +90,24 @@ namespace fp8 {
 enum class WFmt : int { kE4M3 = 0, kE5M2 = 1, kInt8 = 2, kInt4 = 3, kUint4 = 4, kE2M1 = 5 };
 
 constexpr int BMW = 128;  // weight rows (n) per item = MMA M
-constexpr int BT = 32;    // token rows per item at most
 constexpr int KQ = 128;   // k per sub-tile (one e4m3 A tile row is 128 bytes)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t A_SUB = BMW * KQ;     // one e4m3 A tile: 128 rows x 128 bytes
 constexpr uint32_t RAW_BOX = BMW * 128;  // one raw weight box: 128 rows x 128 bytes
-constexpr uint32_t RT_STRIP = BT * 128;  // 64 k of bf16 for 32 token rows
-constexpr uint32_t RT_BOX = 16 * 128;    // one {64 k, 16 rows} box
-constexpr uint32_t B_SUB = 2 * BT * KQ;  // e4m3 operand sub-tile: 64 rows x 128 bytes
+constexpr uint32_t RT_BOX = 16 * 128;    // one {64 k, 16 rows} bf16 or {128 k, 16 rows} e4m3 box
+constexpr int SUB_COLS = 64;             // TMEM columns of one sub-tile's accumulator
 
 // kA8: the token operand comes by TMA (e4m3 activations, or with kPS the
 // split activations) and warp 6 writes its scales.
 template <WFmt F, bool kA8, bool kPS = false>
 struct Cfg {
   static_assert(kA8 || !kPS, "split activations come by TMA");
+  // bf16 activations, split in the kernel or by the split pass: each chunk row
+  // becomes four e4m3 operand rows (h, l, h2, l2)
+  static constexpr bool kSplit = !kA8 || kPS;
+  static constexpr int BT = kSplit ? 16 : 32;  // token rows per item at most
+  static constexpr uint32_t RT_STRIP = BT * 128;  // 64 k of bf16 for BT token rows
   static constexpr bool kNibble = F == WFmt::kInt4 || F == WFmt::kUint4;  // 4-bit codes rewritten as e4m3
   static constexpr bool kConv = kNibble || F == WFmt::kInt8;              // weights rewritten in shared memory
   static constexpr int QPS = F == WFmt::kInt8 ? 1 : 2;        // sub-tiles per step
@@ -116,15 +130,21 @@ struct Cfg {
   // e4m3 activations (kA8) come by TMA straight into the operand ring, which is
   // then freed through the step-done ring; bf16 ones pass the token split.
   static constexpr int RTS = kA8 ? 0 : 2, BST = kA8 ? 4 : 2, NSC = 8;
-  static constexpr int SC_PER = kA8 ? QPS * BT : BT;  // token scales per step: per sub-tile with kA8
-  static constexpr int SLOT_COLS = QPS * 2 * BT;  // sub-tile h: [slot * SLOT_COLS + 64 h, + 2 T8)
+  // token scales per step: (s1, s2) per row with split activations, then four
+  // words that are non-zero when some row of the chunk has a second level in
+  // the step (one per split warp; with split activations only the first);
+  // one scale per sub-tile and row with e4m3 activations
+  static constexpr int SC_PER = kSplit ? 2 * BT + 4 : QPS * BT;
+  static constexpr int SLOT_COLS = QPS * SUB_COLS;  // sub-tile h: [slot * SLOT_COLS + 64 h, + N)
   // One barrier per step records that the step's MMAs have completed (a single
   // tcgen05.commit): it frees the step's A stage (raw for e4m3 / e5m2,
   // converted otherwise) and operand stage and hands its accumulator slot to
   // the epilogue; step j uses index j % NDONE.
   static constexpr int NDONE = NACC;
   static constexpr uint32_t RT_BYTES = (KS / 64) * RT_STRIP;
-  static constexpr uint32_t B_SUBT = kA8 && !kPS ? BT * KQ : B_SUB;  // operand sub-tile: 32 or 64 rows
+  // operand sub-tile: 4 BT = 64 split rows (per 8 chunk rows: 8 h, 8 l, 8 h2, 8 l2
+  // rows), or 32 e4m3 token rows
+  static constexpr uint32_t B_SUBT = (kSplit ? 4 * BT : BT) * KQ;
   static constexpr uint32_t B_BYTES = QPS * B_SUBT;
   static constexpr int kConvWarps = kA8 ? 1 : 4;       // token split, or the token-scale warp
   // weight rewrite: 4 warps (one thread per weight row), or 8 (two threads per
@@ -158,6 +178,8 @@ struct Cfg {
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 
   static_assert(NACC * SLOT_COLS <= int(TMEM_COLS), "TMEM map");
+  // the MMA's N (4 T8 split rows, or up to 32 token rows) fits a sub-tile's columns
+  static_assert((kSplit ? 4 * BT : BT) <= SUB_COLS, "sub-tile accumulator width");
   static_assert(kConv || RAWST == NDONE, "raw stages are freed through the step-done ring");
   static_assert(BST <= NDONE && CST <= NDONE, "step-done ring indexing");
   static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
@@ -175,12 +197,18 @@ struct Params {
   const void* bias;
   int32_t bias_f32;
   void* out;
-  uint32_t* err;
+  uint32_t* err;  // [0] sticky error flags; [1] split marks pending; [2] CTAs done (fix_marked_rows)
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
   int32_t scale_e8m0;
-  const float* lhs_scale;  // e4m3 activations: NULL or f32 [m, num_lhs_blocks]
+  const float* lhs_scale;  // e4m3 activations: NULL or f32 [m, num_lhs_blocks];
+                           // split activations: (s1, s2) pairs [m, num_lhs_blocks = k steps, 2]
   int32_t num_lhs_blocks;
+  // For the rows whose split needs the exact path: the bf16 lhs [m, k] and the
+  // weights as stored, [L, n, w_row_bytes] (k bytes, or k / 2 for 4-bit formats).
+  const uint16_t* x;
+  const uint8_t* w;
+  int64_t w_row_bytes;
 };
 
 // An E8M0 block scale as fp32 (page "gemm_quant.rs", widen_block_scale_f32):
@@ -220,6 +248,140 @@ __device__ __forceinline__ void split_e4m3(const float (&y)[N], uint32_t (&hw)[N
     hw[j] = h01 | (h23 << 16);
     lw[j] = l01 | (l23 << 16);
   }
+}
+
+// Largest value (max) or union (or) over the TPR lanes of a token row; a row's
+// lanes are TPR consecutive lanes starting at a multiple of TPR.  Every lane of
+// the warp must call these together.
+template <int TPR>
+__device__ __forceinline__ uint32_t row_max(uint32_t v) {
+  if constexpr (TPR == 32) {
+    return __reduce_max_sync(0xffffffffu, v);
+  } else {
+#pragma unroll
+    for (int d = 1; d < TPR; d <<= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, d));
+    return v;
+  }
+}
+template <int TPR>
+__device__ __forceinline__ uint32_t row_or(uint32_t v) {
+  if constexpr (TPR == 32) {
+    return __reduce_or_sync(0xffffffffu, v);
+  } else {
+#pragma unroll
+    for (int d = 1; d < TPR; d <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
+  }
+}
+
+// Bits of the scale 2^(E-7) and of its inverse for a largest magnitude with
+// fp32 bits `amax` (sign cleared): E + 127 = amax's exponent field, kept in
+// [8, 254] so that both are fp32 normals.
+__device__ __forceinline__ float split_scale(uint32_t amax) {
+  return __uint_as_float((min(max(amax >> 23, 8u), 254u) - 7u) << 23);
+}
+__device__ __forceinline__ float split_inv_scale(uint32_t amax) {
+  return __uint_as_float((261u - min(max(amax >> 23, 8u), 254u)) << 23);
+}
+
+// x - s (h + l / 16) for the e4m3 codes h, l of two values (low bytes of hw, lw
+// first): what a split level leaves of x.  Exact: s (h + l / 16) is a multiple of
+// s 2^-13 below 2^128 with at most 22 significant bits, and the difference,
+// a multiple of x's last place smaller than x or zero, is an fp32 value.
+__device__ __forceinline__ float2 split_rest(float x0, float x1, uint32_t hw, uint32_t lw, float s) {
+  const float2 h = e4m3x2_value(hw), l = e4m3x2_value(lw);
+  return make_float2(fmaf(-s, fmaf(l.x, 0.0625f, h.x), x0), fmaf(-s, fmaf(l.y, 0.0625f, h.y), x1));
+}
+
+// The two-level split of one token row's k step (a pipeline step of the fp8
+// kernel), of which this lane holds N bf16 values, packed two per word (k order,
+// low half first; lanes past k hold zeros).  With M1 the step's largest |x| and
+// s1 = 2^(E1-7), E1 = floor(log2 M1) (clamped as in split_scale):
+//   x = s1 (h + l / 16) + r,       h = e4m3(x / s1),  l = e4m3(16 (x / s1 - h)),
+// exact (r = 0) for every |x| >= 2^(E1-13); the rest r, an fp32 value, is split
+// the same way with its own largest magnitude M2 and s2 = 2^(E2-7):
+//   r = s2 (h2 + l2 / 16) + r2.
+// When r = 0 for the whole step, s2 = 0 and h2 = l2 = 0.  When r2 != 0 somewhere
+// in the step (the step's magnitudes spread over more than two such ranges), or
+// the step holds an infinity or a NaN, s2 carries a set sign bit (s2 = -|s2|, or
+// -0): the row must then be computed another way, and s1 is NaN for a
+// non-finite step.  Every lane of the warp calls this together.  The rest is
+// only computed when some row of the warp has a non-zero value below 2^(E1-13)
+// (biased exponent below e1 - 13; none can be rounded when e1 <= 14, as x's last
+// place is then no finer than the split's), decided by a vote, so that warps
+// whose rows need no second level skip that work.
+template <int N, int TPR>
+__device__ __forceinline__ void split_step(const uint32_t (&xw)[N / 2], uint32_t (&hw)[N / 4], uint32_t (&lw)[N / 4],
+                                           uint32_t (&hw2)[N / 4], uint32_t (&lw2)[N / 4], float& s1, float& s2) {
+  static_assert(N % 4 == 0, "values per lane");
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) amax = max(amax, max((xw[i] << 16) & 0x7FFFFFFFu, xw[i] & 0x7FFF0000u));
+  amax = row_max<TPR>(amax);
+  s1 = split_scale(amax);
+  {
+    const float inv = split_inv_scale(amax);
+    float y[N];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      y[2 * i] = __uint_as_float(xw[i] << 16) * inv;
+      y[2 * i + 1] = __uint_as_float(xw[i] & 0xFFFF0000u) * inv;
+    }
+    split_e4m3<N>(y, hw, lw);
+  }
+  const bool nonfinite = amax >= 0x7F800000u;
+  const uint32_t e1 = min(max(amax >> 23, 8u), 254u);
+  bool small = false;  // a value of this lane the first level may round
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const uint32_t a = (xw[i] << 16) & 0x7FFFFFFFu, b = xw[i] & 0x7FFF0000u;
+    small |= (a != 0u && (a >> 23) + 13u < e1) || (b != 0u && (b >> 23) + 13u < e1);
+  }
+  bool rest = false;  // the row has values that neither level holds
+  s2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) hw2[j] = lw2[j] = 0u;
+  if (__any_sync(0xffffffffu, small && !nonfinite)) {
+    // what level 1 leaves: r = x - s1 (h + l / 16)
+    float r[N];
+    uint32_t rmax = 0;
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+      const uint32_t x01 = xw[2 * j], x23 = xw[2 * j + 1];
+      const float2 r01 =
+          split_rest(__uint_as_float(x01 << 16), __uint_as_float(x01 & 0xFFFF0000u), hw[j], lw[j], s1);
+      const float2 r23 =
+          split_rest(__uint_as_float(x23 << 16), __uint_as_float(x23 & 0xFFFF0000u), hw[j] >> 16, lw[j] >> 16, s1);
+      r[4 * j] = r01.x, r[4 * j + 1] = r01.y, r[4 * j + 2] = r23.x, r[4 * j + 3] = r23.y;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) rmax = max(rmax, __float_as_uint(r[4 * j + u]) & 0x7FFFFFFFu);
+    }
+    rmax = row_max<TPR>(rmax);
+    if (nonfinite) rmax = 0u;
+    const float inv2 = split_inv_scale(rmax);
+    float y2[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) y2[j] = r[j] * inv2;
+    split_e4m3<N>(y2, hw2, lw2);
+    const float t2 = rmax != 0u ? split_scale(rmax) : 0.f;
+    uint32_t left = 0;  // this lane's values that neither level holds
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+      const float2 a = split_rest(r[4 * j], r[4 * j + 1], hw2[j], lw2[j], t2);
+      const float2 b = split_rest(r[4 * j + 2], r[4 * j + 3], hw2[j] >> 16, lw2[j] >> 16, t2);
+      left |= __float_as_uint(a.x) | __float_as_uint(a.y) | __float_as_uint(b.x) | __float_as_uint(b.y);
+    }
+    if (rmax == 0u) {  // no second level in this row: zero codes, as in warps that skip it
+      left = 0u;
+#pragma unroll
+      for (int j = 0; j < N / 4; ++j) hw2[j] = lw2[j] = 0u;
+    }
+    rest = row_or<TPR>(left & 0x7FFFFFFFu) != 0u;
+    s2 = t2;
+  }
+  const bool flag = rest || nonfinite;
+  if (nonfinite) s1 = __uint_as_float(0x7FC00000u);
+  if (flag) s2 = __uint_as_float(__float_as_uint(s2) | 0x80000000u);
 }
 
 // ------------------------------------------------------------------ weight rewrite
@@ -279,6 +441,202 @@ __device__ __forceinline__ void int8x4_to_e4m3(uint32_t w, uint32_t& hi, uint32_
   const uint32_t l = w & 0x0F0F0F0Fu, h = (w >> 4) & 0x0F0F0F0Fu;
   lo = lut4<kU0, kU1, kU2, kU3, false>(prmt(l | (l >> 4), 0u, 0x0020u));
   hi = lut4<kH0, kH1, kH2, kH3, true>(prmt(h | (h >> 4), 0u, 0x0020u));
+}
+
+// ------------------------------------------------------------------ exact rows
+// The value of a 4-bit code (low nibble of c) of format F.
+template <WFmt F>
+__device__ __forceinline__ float nibble_value(uint32_t c) {
+  c &= 15u;
+  if constexpr (F == WFmt::kUint4) return float(c);
+  if constexpr (F == WFmt::kInt4) return float(int32_t(c << 28) >> 28);
+  // e2m1: sign, 2-bit exponent (bias 1), 1-bit mantissa; exponent 0 is 0 or 0.5
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float v = e == 0u ? 0.5f * float(m) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -v : v;
+}
+
+// Eight stored weights of one row (8 bytes of an 8-bit format, or 4 bytes of a
+// 4-bit one holding 8 codes) as fp32 values, k order.
+template <WFmt F>
+__device__ __forceinline__ void weights8(uint2 raw, float (&v)[8]) {
+  if constexpr (F == WFmt::kE4M3 || F == WFmt::kE5M2) {
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t hh;
+        const uint16_t pair = uint16_t(w[h] >> (16 * q));
+        if constexpr (F == WFmt::kE4M3)
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pair));
+        else
+          asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(hh) : "h"(pair));
+        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&hh));
+        v[4 * h + 2 * q] = f.x;
+        v[4 * h + 2 * q + 1] = f.y;
+      }
+  } else if constexpr (F == WFmt::kInt8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = float(int32_t((i < 4 ? raw.x : raw.y) << (24 - 8 * (i & 3))) >> 24);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = nibble_value<F>(raw.x >> (4 * i));
+  }
+}
+
+// out[row, col] before the bias, summed over k from the stored bf16 activations
+// x (the row, k values) and weights wrow (the column's weight row as stored),
+// without the split: for each quant block b the exact products x * w summed in
+// fp32 (four interleaved partial sums), times the block's scale (scale[s0 + b
+// sn], f32 or E8M0; 1 without scale), added in fp32; IEEE arithmetic
+// throughout, so infinities and NaNs come out as the definition gives them.
+// Used for the rows whose split is not exact, which realistic activations
+// almost never produce; one lane per output column, its weight row read from
+// global memory (k % 128 == 0, and the block width a multiple of 128, on this
+// path).
+template <WFmt F>
+__device__ __forceinline__ float exact_row_sum(const uint16_t* __restrict__ x, const uint8_t* __restrict__ wrow,
+                                               const void* scale, bool scale_e8m0, int64_t s0, int64_t sn,
+                                               int32_t k, int32_t nb) {
+  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
+  const int32_t kb = k / nb;
+  float total = 0.f;
+  for (int32_t b = 0; b < nb; ++b) {
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int32_t k0 = b * kb; k0 < (b + 1) * kb; k0 += 8) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k0));
+      const uint2 raw = k4 ? make_uint2(__ldg(reinterpret_cast<const uint32_t*>(wrow + k0 / 2)), 0u)
+                           : __ldg(reinterpret_cast<const uint2*>(wrow + k0));
+      float wv[8];
+      weights8<F>(raw, wv);
+      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        part[i] = fmaf(__uint_as_float(xs[i] << 16), wv[2 * i], part[i]);
+        part[i] = fmaf(__uint_as_float(xs[i] & 0xFFFF0000u), wv[2 * i + 1], part[i]);
+      }
+    }
+    float s = 1.f;
+    if (scale != nullptr) {
+      const int64_t si = s0 + int64_t(b) * sn;
+      s = scale_e8m0 ? e8m0_value(__ldg(static_cast<const uint8_t*>(scale) + si))
+                     : __ldg(static_cast<const float*>(scale) + si);
+    }
+    total = fmaf((part[0] + part[1]) + (part[2] + part[3]), s, total);
+  }
+  return total;
+}
+
+// Rows whose split a step marked (a second level left a rest, or the step held
+// an infinity or a NaN) are summed again here, from the stored bf16 values and
+// weights (exact_row_sum), and their outputs overwritten.  Called by every
+// thread of every CTA at the end of the kernel with split activations.  With the
+// split pass, which has completed by then, nothing is done unless it marked a
+// row (err[1]).  Otherwise each CTA counts itself in (err[2], wrapping at the
+// grid size) after its stores; the last one sees every other CTA's stores, and
+// if a split marked some row (err[1], set by the split pass or the token split
+// and cleared here) it finds
+// the marked rows of the local groups (from the step scales' sign bits, or by
+// splitting the rows again when the kernel split them itself) and recomputes
+// them, one output column per thread.  Realistic activations almost never mark
+// a row, so the last CTA normally only reads err[1].  `scratch`: shared memory
+// no longer in use, at least 1040 bytes.
+template <WFmt F, bool kPS, bool kOutF32>
+__device__ __noinline__ void fix_marked_rows(const Params& p, int32_t go, const int32_t* offs, uint8_t* scratch,
+                                             int32_t step) {
+  uint32_t* s_todo = reinterpret_cast<uint32_t*>(scratch);
+  uint8_t* mark = scratch + 16;
+  constexpr int32_t RB = 1024;  // rows per block of marks
+  if (threadIdx.x == 0) {
+    uint32_t todo = 1u;
+    if constexpr (kPS) {
+      griddep_wait();  // the split pass has completed: err[1] holds all its marks
+      todo = *reinterpret_cast<volatile uint32_t*>(p.err + 1);
+    }
+    if (todo != 0u) {
+      __threadfence();  // this CTA's outputs are visible before it counts itself in
+      const uint32_t prior = atomicInc(p.err + 2, gridDim.x - 1u);
+      todo = 0u;
+      if (prior == gridDim.x - 1u) {
+        __threadfence();
+        todo = atomicExch(p.err + 1, 0u);
+      }
+    }
+    *s_todo = todo;
+  }
+  __syncthreads();
+  if (*s_todo == 0u) return;
+  const int32_t nb = p.scale != nullptr ? p.num_blocks : 1;
+  const int32_t ksteps = (p.k + step - 1) / step;
+  const int32_t row_lo = offs[go], row_hi = offs[go + p.num_local_groups];
+  const int warps = int(blockDim.x) >> 5, wid = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
+  for (int32_t r0 = row_lo; r0 < row_hi; r0 += RB) {
+    const int32_t nr = min(RB, row_hi - r0);
+    for (int32_t i = threadIdx.x; i < nr; i += blockDim.x) mark[i] = 0;
+    __syncthreads();
+    if constexpr (kPS) {
+      for (int64_t i = threadIdx.x; i < int64_t(nr) * ksteps; i += blockDim.x) {
+        const int64_t at = (int64_t(r0) * ksteps + i) * 2 + 1;  // s2 of (row, step)
+        if (__float_as_uint(p.lhs_scale[at]) >> 31) mark[i / ksteps] = 1;
+      }
+    } else {
+      // the token split's marks, found again with the split pass's lane layout:
+      // one warp per (row, step), step / 32 values per lane
+      for (int64_t u = wid; u < int64_t(nr) * ksteps; u += warps) {
+        const int32_t rr = int32_t(u / ksteps), ks = int32_t(u % ksteps);
+        const uint16_t* x = p.x + int64_t(r0 + rr) * p.k;
+        float s1, s2;
+        if (step == 256) {
+          uint32_t xw[4] = {0u, 0u, 0u, 0u}, hw[2], lw[2], hw2[2], lw2[2];
+          const int32_t kk = ks * 256 + lane * 8;
+          if (kk < p.k) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + kk));
+            xw[0] = v.x, xw[1] = v.y, xw[2] = v.z, xw[3] = v.w;
+          }
+          split_step<8, 32>(xw, hw, lw, hw2, lw2, s1, s2);
+        } else {
+          uint32_t xw[2] = {0u, 0u}, hw[1], lw[1], hw2[1], lw2[1];
+          const int32_t kk = ks * 128 + lane * 4;
+          if (kk < p.k) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + kk));
+            xw[0] = v.x, xw[1] = v.y;
+          }
+          split_step<4, 32>(xw, hw, lw, hw2, lw2, s1, s2);
+        }
+        if (lane == 0 && (__float_as_uint(s2) >> 31)) mark[rr] = 1;
+      }
+    }
+    __syncthreads();
+    for (int32_t rr = 0; rr < nr; ++rr) {
+      if (!mark[rr]) continue;
+      const int32_t row = r0 + rr;
+      int32_t lo = go, hi = go + p.num_local_groups;  // the largest g with offs[g] <= row
+      while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (offs[mid] <= row)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      const int32_t lg = lo - go;
+      const uint16_t* x = p.x + int64_t(row) * p.k;
+      for (int32_t c = threadIdx.x; c < p.n; c += blockDim.x) {
+        float v = exact_row_sum<F>(x, p.w + (int64_t(lg) * p.n + c) * p.w_row_bytes, p.scale, p.scale_e8m0 != 0,
+                                   int64_t(lg) * nb * p.n + c, p.n, p.k, nb);
+        if (p.bias != nullptr) {
+          const int64_t bi = int64_t(lg) * p.n + c;
+          v += p.bias_f32 ? __ldg(static_cast<const float*>(p.bias) + bi)
+                          : __bfloat162float(static_cast<const __nv_bfloat16*>(p.bias)[bi]);
+        }
+        if constexpr (kOutF32)
+          static_cast<float*>(p.out)[int64_t(row) * p.n + c] = v;
+        else
+          static_cast<__nv_bfloat16*>(p.out)[int64_t(row) * p.n + c] = __float2bfloat16_rn(v);
+      }
+    }
+    __syncthreads();
+  }
 }
 
 template <int N>
@@ -342,6 +700,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
   auto sfull_bar = [&](uint32_t s) { return sbase + C::OFF_SFULL + 8 * s; };
   auto sempty_bar = [&](uint32_t s) { return sbase + C::OFF_SEMPTY + 8 * s; };
   auto acce_bar = [&](uint32_t s) { return sbase + C::OFF_ACCE + 8 * s; };
+
   const uint32_t done_bar = sbase + C::OFF_DONE;
 
   if (warp == 0 && lane == 0) {
@@ -373,7 +732,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
   }
   if (warp == 2) {
     build_group_offsets(p.group_sizes, p.num_total_groups, p.m, offs, p.err);
-    build_tile_prefix(offs, go, p.num_local_groups, BT, tiles);
+    build_tile_prefix(offs, go, p.num_local_groups, C::BT, tiles);
   }
   tc_fence_before();
   __syncthreads();
@@ -389,9 +748,12 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
   const int32_t total = t_tiles * n_tiles;
   // Items: row chunks outer, the weight tiles of the chunk's group inner.
   auto item_of = [&](int32_t w) {
-    return decode_gemm_tile(w, t_tiles, n_tiles, n_tiles, tiles, offs, go, p.num_local_groups, BT);
+    return decode_gemm_tile(w, t_tiles, n_tiles, n_tiles, tiles, offs, go, p.num_local_groups, C::BT);
   };
   auto halves = [&](int32_t ks) { return min(QPS, nq - QPS * ks); };
+  // Rows of an item's chunk: row_end is the end of the chunk's group, which can
+  // lie past the chunk's BT rows.
+  auto chunk_rows = [&](const GemmTile& t) { return min(t.row_end - t.row0, int32_t(C::BT)); };
   // Step j's operand / converted stage is reused by step j + depth once step j's MMAs are done.
   auto wait_step_done = [&](uint32_t j, int depth) {
     return j < uint32_t(depth) ||
@@ -410,7 +772,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
       bool split_ready = false;  // kPS: the split rows' kernel has completed
       for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const GemmTile t = item_of(w);
-        const int32_t rboxes = t.row_end - t.row0 > 16 ? 2 : 1;
+        const int32_t rboxes = chunk_rows(t) > 16 ? 2 : 1;
         for (int32_t ks = 0; ks < ksteps; ++ks) {
           const int32_t hq = halves(ks);
           // Raw stage `as` is free once its last reader is done: the MMAs of the
@@ -438,23 +800,22 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
             aph ^= 1u;
           }
           if constexpr (kPS) {
-            // h and l rows, {128 k, 8 rows} boxes from planes 0 and 1, into
-            // operand rows [0, T8) and [T8, 2 T8) of each sub-tile
+            // per 8 chunk rows one {128 k, 8 rows, 4 planes} box: their h, l,
+            // h2 and l2 rows, operand rows [32 b, 32 b + 32) of each sub-tile
             if (!wait_step_done(j, C::BST)) {
               ok = false;
               break;
             }
-            const int t8 = t8_of(t.row_end - t.row0);
+            const int t8 = t8_of(chunk_rows(t));
             if (!split_ready) {  // weights already stream; the split rows come from the kernel before
               griddep_wait();
               split_ready = true;
             }
-            mbar_arrive_expect_tx(bfull_bar(rs), uint32_t(hq * 2 * t8) * 128u);
+            mbar_arrive_expect_tx(bfull_bar(rs), uint32_t(hq * 4 * t8) * 128u);
             for (int h = 0; h < hq; ++h)
-              for (int z = 0; z < 2; ++z)
-                for (int r8 = 0; r8 < t8; r8 += 8)
-                  tma_load_3d(sbase + C::OFF_B + rs * C::B_BYTES + h * C::B_SUBT + uint32_t(z * t8 + r8) * 128u,
-                              &tm_lhs, bfull_bar(rs), (QPS * ks + h) * KQ, t.row0 + r8, z);
+              for (int r8 = 0; r8 < t8; r8 += 8)
+                tma_load_3d(sbase + C::OFF_B + rs * C::B_BYTES + h * C::B_SUBT + uint32_t(4 * r8) * 128u, &tm_lhs,
+                            bfull_bar(rs), (QPS * ks + h) * KQ, t.row0 + r8, 0);
           } else if constexpr (kA8) {
             // e4m3 token rows, one {128 k, 16 rows} box per sub-tile and 16 rows,
             // straight into operand stage rs once step j - BST's MMAs are done.
@@ -475,7 +836,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
             mbar_arrive_expect_tx(rfull_bar(rs), uint32_t(rboxes * 2 * hq) * RT_BOX);
             for (int st = 0; st < 2 * hq; ++st)
               for (int rb = 0; rb < rboxes; ++rb)
-                tma_load_2d(sbase + C::OFF_RT + rs * C::RT_BYTES + st * RT_STRIP + rb * RT_BOX, &tm_lhs,
+                tma_load_2d(sbase + C::OFF_RT + rs * C::RT_BYTES + st * C::RT_STRIP + rb * RT_BOX, &tm_lhs,
                             rfull_bar(rs), ks * C::KS + 64 * st, t.row0 + 16 * rb);
           }
           rpar[rs] = rph;
@@ -502,9 +863,9 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
-      const int t8 = t8_of(t.row_end - t.row0);
-      // N: the h and l rows of the split (2 T8), or the e4m3 token rows (16 or 32).
-      const uint32_t idesc = idesc_e4m3(BMW, kA8 && !kPS ? max(t8, 16) : 2 * t8) | (C::kAType << 7);
+      const int t8 = t8_of(chunk_rows(t));
+      // N: the h, l, h2 and l2 rows of the split (4 T8), or the e4m3 token rows (16 or 32).
+      const uint32_t idesc = idesc_e4m3(BMW, C::kSplit ? 4 * t8 : max(t8, 16)) | (C::kAType << 7);
       for (int32_t ks = 0; ks < ksteps; ++ks) {
         const int32_t hq = halves(ks);
         const uint32_t afull = C::kConv ? convfull_bar(as) : rawfull_bar(as);
@@ -517,7 +878,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
         if (lane == 0) {
           for (int h = 0; h < hq; ++h) {
             const uint32_t b0 = sbase + C::OFF_B + bs * C::B_BYTES + h * C::B_SUBT;
-            const uint32_t d = tmem_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
+            const uint32_t d = tmem_base + slot * C::SLOT_COLS + uint32_t(h) * SUB_COLS;
 #pragma unroll
             for (int pass = 0; pass < C::PASSES; ++pass) {
               const uint32_t a0 = C::kConv ? sbase + C::OFF_CONV + as * C::CONV_BYTES + (h * C::PASSES + pass) * A_SUB
@@ -560,7 +921,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     uint32_t slot = 0, sph = 0, sc = 0, scph = 0;
     bool ok = true;
-    constexpr int kPre = 8;  // weight scales are first-touch DRAM reads: fetched 8 blocks ahead
+    // Weight scales are first-touch DRAM reads: fetched kPre blocks ahead.  The
+    // fold loop is unrolled kPre times; with split activations, whose fold has
+    // the second level's branch, 4 measured faster than 8 (less code to fetch).
+    constexpr int kPre = C::kSplit ? 4 : 8;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
       const int32_t col = t.n_tile * BMW + wrow;
@@ -610,29 +974,39 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
                 }
                 tc_fence_after();
               }
-              const float* ts = tscale + sc * C::SC_PER + (kA8 ? h * BT : 0);
-              const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * (2 * BT);
-              if constexpr (kA8 && !kPS) {
+              const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * SUB_COLS;
+              if constexpr (!C::kSplit) {
                 // one e4m3 product per token: its T8 columns, times the sub-tile's token scale
+                const float* ts = tscale + sc * C::SC_PER + h * C::BT;
                 float d[T8];
                 tmem_ld_cols<T8>(col0, d);
 #pragma unroll
                 for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
-              } else if constexpr (T8 < 32) {
-                // h and l columns in one load
-                float d[2 * T8];
-                tmem_ld_cols<2 * T8>(col0, d);
-#pragma unroll
-                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], fmaf(d[T8 + i], 0.0625f, d[i]), acc[i]);
               } else {
-                // 32 h columns, then 32 l columns (fewer live registers)
-                float d[T8];
-                tmem_ld_cols<T8>(col0, d);
+                // Chunk row 8 b + i has its h, l, h2, l2 products in columns 32 b + i,
+                // + 8, + 16, + 24.  The h2 and l2 columns are read only in steps where
+                // some row of the chunk has a second level (s2 != 0).
+                const float2* ts = reinterpret_cast<const float2*>(tscale + sc * C::SC_PER);
+                const uint4 lv2 = *reinterpret_cast<const uint4*>(tscale + sc * C::SC_PER + 2 * C::BT);
+                const bool two = (lv2.x | lv2.y | lv2.z | lv2.w) != 0u;
 #pragma unroll
-                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
-                tmem_ld_cols<T8>(col0 + T8, d);
+                for (int b = 0; b < T8 / 8; ++b) {
+                  float d[16];
+                  tmem_ld_cols<16>(col0 + 32 * b, d);
 #pragma unroll
-                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i] * 0.0625f, d[i], acc[i]);
+                  for (int i = 0; i < 8; ++i)
+                    acc[8 * b + i] = fmaf(sw * ts[8 * b + i].x, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
+                  if (two) {
+                    tmem_ld_cols<16>(col0 + 32 * b + 16, d);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      // a row without a second level keeps its sum (its h2 / l2 products
+                      // are with zero codes, NaN against an infinite weight)
+                      const float s2 = ts[8 * b + i].y;
+                      if (s2 != 0.f) acc[8 * b + i] = fmaf(sw * s2, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
+                    }
+                  }
+                }
               }
               ++q;
               if (h == QPS - 1 || q == nq) {
@@ -669,13 +1043,13 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           }
         }
       };
-      const int t8 = t8_of(t.row_end - t.row0);
+      const int t8 = t8_of(chunk_rows(t));
       if (t8 == 8)
         run(std::integral_constant<int, 8>{});
-      else if (t8 == 16)
+      else if (C::kSplit || t8 == 16)
         run(std::integral_constant<int, 16>{});
       else
-        run(std::integral_constant<int, 32>{});
+        run(std::integral_constant<int, C::kSplit ? 16 : 32>{});
     }
     // Rows outside [offs[first local], offs[last local + 1]) are zero, unless the
     // caller keeps them (gmm_into).
@@ -696,7 +1070,8 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     // e4m3 activations: per step, the token scale of each of its sub-tiles for
     // the item's rows (lhs_scale[row, lhs block of the sub-tile], 1 without
     // lhs_scale, 0 for operand rows past the chunk).  Split activations: the
-    // row's 2^(E-7) for the step (lhs_scale[row, step]) for both sub-tiles.
+    // row's (s1, s2) for the step (lhs_scale[row, step, 0..1]) for both
+    // sub-tiles, (0, 0) past the chunk.
     if constexpr (kPS) griddep_wait();  // the step scales come from the kernel before
     const int32_t nlb = p.lhs_scale != nullptr ? p.num_lhs_blocks : 1;
     const int32_t q_per_lblock = nq / nlb;  // (k / nlb) % 128 == 0 on this path
@@ -704,21 +1079,32 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
-      const int32_t rows = t.row_end - t.row0;
+      const int32_t rows = chunk_rows(t);
       for (int32_t ks = 0; ks < ksteps; ++ks) {
         const int32_t hq = halves(ks);
         if (!wait_bar(sempty_bar(sc), scph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        for (int idx = lane; idx < QPS * BT; idx += 32) {
-          const int h = idx / BT, r = idx % BT;
-          float v = 0.f;
-          if (h < hq && r < rows)
-            v = p.lhs_scale != nullptr
-                    ? __ldg(p.lhs_scale + int64_t(t.row0 + r) * nlb + (kPS ? ks : (QPS * ks + h) / q_per_lblock))
-                    : 1.f;
-          tscale[sc * C::SC_PER + idx] = v;
+        if constexpr (kPS) {
+          uint32_t two = 0;  // some row of the chunk has a second level in this step
+          for (int idx = lane; idx < 2 * C::BT; idx += 32) {
+            const int r = idx >> 1;
+            const float v = r < rows ? __ldg(p.lhs_scale + (int64_t(t.row0 + r) * nlb + ks) * 2 + (idx & 1)) : 0.f;
+            tscale[sc * C::SC_PER + idx] = v;
+            two |= (idx & 1) ? __float_as_uint(v) : 0u;
+          }
+          two = __any_sync(0xffffffffu, two != 0u) ? 1u : 0u;
+          if (lane < 4) reinterpret_cast<uint32_t*>(tscale)[sc * C::SC_PER + 2 * C::BT + lane] = lane == 0 ? two : 0u;
+        } else {
+          for (int idx = lane; idx < QPS * C::BT; idx += 32) {
+            const int h = idx / C::BT, r = idx % C::BT;
+            float v = 0.f;
+            if (h < hq && r < rows)
+              v = p.lhs_scale != nullptr ? __ldg(p.lhs_scale + int64_t(t.row0 + r) * nlb + (QPS * ks + h) / q_per_lblock)
+                                         : 1.f;
+            tscale[sc * C::SC_PER + idx] = v;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sfull_bar(sc));
@@ -732,20 +1118,23 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     // ---------------------------------------------------------------- token split
     // The 128 threads share a step's T8 rows evenly: 128 / T8 adjacent lanes per
     // token row r, each taking the same T8 consecutive k of every sub-tile h of
-    // the step (T8 / 8 bf16 chunks of 16 bytes per sub-tile from the token tile;
-    // T8 bytes of e4m3 into rows r (h part) and T8 + r (l part) of operand
-    // sub-tile h).  The lanes of a row agree on the row's step maximum by
-    // shuffles.  All tiles are 128-byte swizzled: 16-byte chunk j of row r sits
-    // at position j ^ (r % 8).
+    // the step (T8 / 8 bf16 chunks of 16 bytes per sub-tile from the token tile).
+    // split_step turns them into T8 bytes of each of h, l, h2 and l2, written to
+    // rows 32 (r / 8) + 8 p + r % 8 (p = 0, 1, 2, 3) of operand sub-tile h; the
+    // lanes of a row agree on its maxima by shuffles.  All tiles are 128-byte
+    // swizzled: 16-byte chunk j of row R sits at position j ^ (R % 8), and
+    // R % 8 = r % 8.
     const int ct = int(threadIdx.x) - 192;
     uint32_t rs = 0, rph = 0, bs = 0, sc = 0, scph = 0;
     uint32_t j = 0;  // steps split so far
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
+      const int32_t rows = chunk_rows(t);
       auto run = [&](auto t8c) {
         constexpr int T8 = decltype(t8c)::value;
-        constexpr int TPR = 128 / T8;  // threads per token row: 16, 8 or 4
+        constexpr int TPR = 128 / T8;  // threads per token row: 16 or 8
+        constexpr int NV = QPS * T8;   // values per lane and step
         const int r = ct / TPR, seg = ct % TPR;
         for (int32_t ks = 0; ks < ksteps; ++ks) {
           const int32_t hq = halves(ks);
@@ -756,64 +1145,58 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           }
           // Sub-tile h, k [T8 seg, T8 seg + T8): bf16 chunks c = T8 seg / 8 + i of
           // the sub-tile, in strip 2 h + c / 8 of the token tile at position c % 8.
-          uint32_t xw[QPS][T8 / 2];
-          uint32_t amax = 0;
+          uint32_t xw[NV / 2];
           const uint32_t src = sbase + C::OFF_RT + rs * C::RT_BYTES + uint32_t(r) * 128u;
 #pragma unroll
           for (int h = 0; h < QPS; ++h) {
-            if (h < hq) {
 #pragma unroll
-              for (int i = 0; i < T8 / 8; ++i) {
+            for (int i = 0; i < T8 / 8; ++i) {
+              uint32_t* v = xw + h * (T8 / 2) + 4 * i;
+              v[0] = v[1] = v[2] = v[3] = 0u;
+              if (h < hq) {
                 const int c = seg * (T8 / 8) + i;
                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(xw[h][4 * i]), "=r"(xw[h][4 * i + 1]), "=r"(xw[h][4 * i + 2]),
-                               "=r"(xw[h][4 * i + 3])
-                             : "r"(src + uint32_t(2 * h + (c >> 3)) * RT_STRIP + (uint32_t((c & 7) ^ (r & 7)) << 4)));
+                             : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                             : "r"(src + uint32_t(2 * h + (c >> 3)) * C::RT_STRIP +
+                                   (uint32_t((c & 7) ^ (r & 7)) << 4)));
               }
-#pragma unroll
-              for (int i = 0; i < T8 / 2; ++i)
-                amax = max(amax, max((xw[h][i] << 16) & 0x7FFFFFFFu, xw[h][i] & 0x7FFF0000u));
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(rempty_bar(rs));  // the values are in registers
-#pragma unroll
-          for (int dd = 1; dd < TPR; dd <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, dd));
-          // E + 127 of the step maximum, kept in [8, 254] so that both 2^(E-7)
-          // and 2^(7-E) are fp32 normals; a NaN or infinity gives a NaN scale.
-          const uint32_t e = min(max(amax >> 23, 8u), 254u);
-          const float inv_s = __uint_as_float((261u - e) << 23);
+          uint32_t code[4][NV / 4];
+          float s1, s2;
+          split_step<NV, TPR>(xw, code[0], code[1], code[2], code[3], s1, s2);
 #pragma unroll
           for (int h = 0; h < QPS; ++h) {
             if (h < hq) {
-              float y[T8];
+              // e4m3 bytes [T8 seg, T8 seg + T8) of each of the row's four operand
+              // rows: 16-byte chunk (T8 seg) / 16, at byte (T8 seg) % 16 within it.
+              const uint32_t sub = sbase + C::OFF_B + bs * C::B_BYTES + uint32_t(h) * C::B_SUBT;
 #pragma unroll
-              for (int i = 0; i < T8 / 2; ++i) {
-                y[2 * i] = __uint_as_float(xw[h][i] << 16) * inv_s;
-                y[2 * i + 1] = __uint_as_float(xw[h][i] & 0xFFFF0000u) * inv_s;
-              }
-              uint32_t hw[T8 / 4], lw[T8 / 4];
-              split_e4m3<T8>(y, hw, lw);
-              // e4m3 bytes [T8 seg, T8 seg + T8) of the row: 16-byte chunk
-              // (T8 seg) / 16, at byte (T8 seg) % 16 within it.
-              const uint32_t sub = sbase + C::OFF_B + bs * C::B_BYTES + uint32_t(h) * B_SUB;
-              const uint32_t hrow = sub + uint32_t(r) * 128u, lrow = sub + uint32_t(T8 + r) * 128u;
-              if constexpr (T8 == 8) {
-                const uint32_t pos = (uint32_t((seg >> 1) ^ (r & 7)) << 4) + uint32_t(seg & 1) * 8u;
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(hrow + pos), "r"(hw[0]), "r"(hw[1]));
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(lrow + pos), "r"(lw[0]), "r"(lw[1]));
-              } else {
-#pragma unroll
-                for (int cc = 0; cc < T8 / 16; ++cc) {
-                  const uint32_t pos = uint32_t((seg * (T8 / 16) + cc) ^ (r & 7)) << 4;
-                  st_shared_v4(hrow + pos, hw[4 * cc], hw[4 * cc + 1], hw[4 * cc + 2], hw[4 * cc + 3]);
-                  st_shared_v4(lrow + pos, lw[4 * cc], lw[4 * cc + 1], lw[4 * cc + 2], lw[4 * cc + 3]);
+              for (int pl = 0; pl < 4; ++pl) {
+                const uint32_t prow = sub + uint32_t(32 * (r >> 3) + 8 * pl + (r & 7)) * 128u;
+                const uint32_t* cw = code[pl] + h * (T8 / 4);
+                if constexpr (T8 == 8) {
+                  const uint32_t pos = (uint32_t((seg >> 1) ^ (r & 7)) << 4) + uint32_t(seg & 1) * 8u;
+                  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(prow + pos), "r"(cw[0]), "r"(cw[1]));
+                } else {
+                  st_shared_v4(prow + (uint32_t(seg ^ (r & 7)) << 4), cw[0], cw[1], cw[2], cw[3]);
                 }
               }
             }
           }
-          if (seg == 0)
-            tscale[sc * BT + r] = amax < 0x7F800000u ? __uint_as_float((e - 7u) << 23) : __uint_as_float(0x7FC00000u);
+          const bool live = r < rows;
+          if (seg == 0) {
+            tscale[sc * C::SC_PER + 2 * r] = live ? s1 : 0.f;
+            tscale[sc * C::SC_PER + 2 * r + 1] = live ? s2 : 0.f;
+            // a marked row: the last CTA sums it again (see fix_marked_rows)
+            if (live && (__float_as_uint(s2) >> 31)) atomicOr(p.err + 1, 1u);
+          }
+          // this warp's rows: any second level in the step (read by the epilogue)
+          const bool two = __any_sync(0xffffffffu, seg == 0 && live && __float_as_uint(s2) != 0u);
+          if (lane == 0)
+            reinterpret_cast<uint32_t*>(tscale)[sc * C::SC_PER + 2 * C::BT + (warp - 6)] = two ? 1u : 0u;
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -832,13 +1215,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           ++j;
         }
       };
-      const int t8 = t8_of(t.row_end - t.row0);
-      if (t8 == 8)
+      if (t8_of(rows) == 8)
         run(std::integral_constant<int, 8>{});
-      else if (t8 == 16)
-        run(std::integral_constant<int, 16>{});
       else
-        run(std::integral_constant<int, 32>{});
+        run(std::integral_constant<int, 16>{});
     }
   } else if constexpr (C::kConv) {
     // ---------------------------------------------------------------- weight rewrite
@@ -926,6 +1306,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if constexpr (C::kSplit) fix_marked_rows<F, kPS, kOutF32>(p, go, offs, smem + C::OFF_B, C::KS);
 }
 
 template <WFmt F, bool kA8, bool kPS, bool kOutF32>
@@ -934,9 +1315,11 @@ cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) 
   auto kern = gemm_fp8_kernel<F, kA8, kPS, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
+  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
-           L.lhs_scale, L.num_lhs_blocks};
+           L.lhs_scale, L.num_lhs_blocks, static_cast<const uint16_t*>(L.lhs_raw),
+           static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k)};
   if constexpr (kPS) {
     // Launched as the programmatic dependent of the split-rows kernel just
     // before it in the stream: the prologue and the weight stream overlap that

@@ -17,9 +17,12 @@
 
 namespace {
 
-// Workspace: [0, 256) the sticky error flags; then, used only when the
+// Workspace: [0, 256) word 0 the sticky error flags, word 1 the split marks
+// pending and word 2 the count of finished CTAs of the fp8 kernels (their last
+// CTA sums marked rows again); then, used only when the
 // caller's workspace holds all of it, scratch for the split bf16 activations
-// of the fp8 kernels (h / l planes [2, m, k] and step scales [m, k steps]).
+// of the fp8 kernels (h / l / h2 / l2 planes [4, m, k] and the (s1, s2) step
+// scales [m, k steps, 2]).
 constexpr size_t kWorkspaceMinBytes = 256;
 constexpr size_t kActOffset = 256;
 constexpr size_t kActScratchBytes = size_t(16) << 20;
@@ -357,6 +360,8 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.lhs_scale = ext.lhs_scale;
     S.num_lhs_blocks = ext.lhs_scale != nullptr ? ext.num_lhs_blocks : 1;
     S.mx_scale = static_cast<const uint8_t*>(ext.rhs_block_scale);
+    S.lhs_raw = lhs;
+    S.rhs_raw = rhs;
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     const int act_split = choose_act_split();
     if (act_split < 0) return GMM_ERR_SHAPE;
@@ -366,20 +371,21 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       if (!lhs8 && act_split != 0) {
         const int32_t step = fmt == gmmk::kWeightInt8 ? 128 : 256;
         const int64_t ksteps = (k + step - 1) / step;
-        const size_t scales_at = (kActOffset + size_t(2 * m * k) + 255) & ~size_t(255);
-        const size_t end = scales_at + size_t(m * ksteps) * sizeof(float);
-        if (workspace_bytes >= kWorkspaceBytes && end <= kWorkspaceBytes) {
+        const size_t scales_at = (kActOffset + size_t(4 * m * k) + 255) & ~size_t(255);
+        const size_t end = scales_at + size_t(m * ksteps) * 2 * sizeof(float);
+        if (end <= workspace_bytes) {
           uint8_t* planes = static_cast<uint8_t*>(workspace) + kActOffset;
           float* scales = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + scales_at);
-          const uint64_t dims[3] = {uint64_t(k), uint64_t(m), 2};
-          const uint32_t box[3] = {128u, 8u, 1u};
+          const uint64_t dims[3] = {uint64_t(k), uint64_t(m), 4};
+          const uint32_t box[3] = {128u, 8u, 4u};
           if (int st = make_map(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, planes, dims, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B))
             return st;
           S.lhs_split = 1;
           S.lhs_scale = scales;
           S.num_lhs_blocks = int32_t(ksteps);
-          if (cudaError_t e1 = gmmk::launch_act_split(lhs, m, k, step, planes, scales, s)) return cuda_fail(e1);
+          if (cudaError_t e1 = gmmk::launch_act_split(lhs, m, k, step, planes, scales, err + 1, s))
+            return cuda_fail(e1);
         } else if (act_split == 2) {
           return GMM_ERR_WORKSPACE;
         }

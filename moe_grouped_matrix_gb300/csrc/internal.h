@@ -79,8 +79,11 @@ struct ScaledLaunch {
   int32_t num_lhs_blocks;
   const uint8_t* mx_scale;          // decoding kernel: NULL, E8M0 [L, n, k / 32] (e4m3 weights) or
                                     // e4m3 [L, n, k / 16] (e2m1 weights)
-  int32_t lhs_split;                // fp8 kernels: tm_lhs spans act_split's h / l planes [2, m, k]
-                                    // (box {128, 8, 1}); lhs_scale its [m, k steps] step scales
+  int32_t lhs_split;                // fp8 kernels: tm_lhs spans act_split's h / l / h2 / l2 planes
+                                    // [4, m, k] (box {128, 8, 4}); lhs_scale its (s1, s2) step
+                                    // scales [m, k steps, 2]
+  const void* lhs_raw;              // fp8 kernels with bf16 lhs: the lhs itself, [m, k] bf16
+  const void* rhs_raw;              // fp8 kernels: the weights as stored, [L, n, k or k / 2]
 };
 
 cudaError_t launch_scaled(const ScaledLaunch& p, bool rhs_e4m3, bool out_f32, int grid, cudaStream_t stream);
@@ -113,11 +116,12 @@ cudaError_t launch_fp8_converted(const ScaledLaunch& p, int weight_format, bool 
 cudaError_t launch_fp8_ps(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
 cudaError_t launch_fp8_ps_converted(const ScaledLaunch& p, int weight_format, bool out_f32, int grid,
                                    cudaStream_t stream);
-// The exact two-term split of bf16 rows [m, k] (k % 128 == 0) into e4m3 h / l
-// planes [2, m, k] and step scales [m, ceil(k / step)], step 256 or 128 (the
-// fp8 kernel's k step: 128 for int8 weights) (act_split.cu).
+// The two-level e4m3 split of bf16 rows [m, k] (k % 128 == 0) into e4m3 planes
+// h / l / h2 / l2 [4, m, k] and step scales (s1, s2) [m, ceil(k / step), 2], step
+// 256 or 128 (the fp8 kernel's k step: 128 for int8 weights); sets *pending when a
+// step is marked (act_split.cu).
 cudaError_t launch_act_split(const void* x, int64_t m, int64_t k, int32_t step, void* planes, float* scale,
-                             cudaStream_t stream);
+                             uint32_t* pending, cudaStream_t stream);
 
 // Per-token-group e4m3 quantisation of bf16 activations (quantize.cu); group
 // 64, 128 or 256, k % group == 0.

@@ -7,7 +7,11 @@ absolute values.  The bound covers fp32 accumulation of up to ~4096 products
 (at most 2^-9 of |result| for round-to-nearest-even).  Where the definition's
 result is not finite (an infinite or NaN input: x * inf is +-inf, 0 * inf and
 inf - inf are NaN, IEEE arithmetic in the pages' dot_general) the GPU must give
-the same infinity, or a NaN where ref is NaN."""
+the same infinity, or a NaN where ref is NaN.  Below the output format's
+smallest normal (2^-126 for bf16 and f32) its values are spaced evenly, 2^-133
+apart for bf16 and 2^-149 for f32, so no stored value need lie within 2^-8 of
+ref there: the bound adds half that spacing, the most one rounding of the result
+to the format can cost."""
 
 import numpy as np
 import torch
@@ -27,8 +31,9 @@ def check_close(gpu: torch.Tensor, ref: np.ndarray, mag: np.ndarray, what: str):
     g = gpu.detach().cpu().to(torch.float64).numpy()
     assert g.shape == ref.shape, (g.shape, ref.shape)
     finite = np.isfinite(ref)
+    tiny = 2.0 ** -134 if gpu.dtype == torch.bfloat16 else 2.0 ** -150
     with np.errstate(invalid="ignore"):
-        bound = REL_MAG * mag + REL_REF * np.abs(ref)
+        bound = REL_MAG * mag + REL_REF * np.abs(ref) + tiny
         err = np.abs(g - ref)
         ok = np.where(finite, err <= bound, (g == ref) | (np.isnan(ref) & np.isnan(g)))
     bad = ~ok  # NaN in g fails here unless ref is NaN
