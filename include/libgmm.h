@@ -28,6 +28,10 @@
  *    once before its first use.  Calls that share a workspace must be
  *    stream-ordered.
  *  - Requires the current device to be compute capability 10.3 (GB300).
+ *  - The only environment variable read is GMM_LOG: when set (and not "0"),
+ *    every forward and tgmm call writes one line to stderr with its sizes, dtypes
+ *    and the kernel it chose.  Kernel choices are per-call arguments
+ *    (gmm_options) or tiling-table entries, never environment variables.
  */
 #ifndef LIBGMM_H_
 #define LIBGMM_H_
@@ -65,7 +69,10 @@ enum {
   GMM_ERR_WORKSPACE = 6,    /* workspace NULL, misaligned or smaller than GMM_WORKSPACE_MIN_BYTES */
   GMM_ERR_ARCH = 7,         /* current device is not compute capability 10.3 */
   GMM_ERR_CUDA = 8,         /* a CUDA runtime or driver call failed; see gmm_last_cuda_error() */
-  GMM_ERR_IO = 9            /* a tiling-table file could not be read, parsed or written */
+  GMM_ERR_IO = 9,           /* a tiling-table file could not be read, parsed or written */
+  /* from gmm_get_device_error() only: what the device recorded */
+  GMM_ERR_DEVICE_GROUP_SIZES = 10, /* some group_sizes[g] < 0, or sum(group_sizes) > m */
+  GMM_ERR_TIMEOUT = 11             /* an internal pipeline wait gave up; that call's output is undefined */
 };
 
 /* Sticky device-side error flags kept in the workspace. */
@@ -92,6 +99,74 @@ enum {
  * least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
  */
 size_t gmm_workspace_bytes(void);
+
+/*
+ * The workspace size that lets a gmm() / gmm_ex() call of this shape run its
+ * fastest way: GMM_WORKSPACE_MIN_BYTES, plus for bf16 activations (lhs_dtype
+ * GMM_DTYPE_BF16) with an 8- or 4-bit rhs_dtype the split scratch described above
+ * (4 m k bytes rounded up to 256, then 8 m ceil(k / step) bytes, step 256, or 128
+ * for int8).  num_total_groups, num_local_groups and n do not change it today; they
+ * are taken so that callers size workspaces by the problem.  0 for negative sizes.
+ */
+size_t gmm_workspace_bytes_for(int64_t m, int64_t k, int64_t n, int32_t num_total_groups, int32_t num_local_groups,
+                               int lhs_dtype, int rhs_dtype);
+
+/* bf16 forward kernels, as gmm_options and the tiling table name them. */
+enum {
+  GMM_KERNEL_AUTO = 0,      /* no choice / built-in rule */
+  GMM_KERNEL_PAIR = 1,      /* SM-pair 256 x 256 row tiles */
+  GMM_KERNEL_SWAP_PAIR = 2, /* SM-pair, 256 weight rows x up to 256 group rows */
+  GMM_KERNEL_SWAP = 3,      /* one SM, 128 weight rows x up to 256 group rows */
+  GMM_KERNEL_SINGLE = 4     /* one SM, 128 x 256 row tiles */
+};
+
+/* gmm_options.e4m3_kernel */
+enum { GMM_E4M3_AUTO = 0, GMM_E4M3_TENSOR = 1, GMM_E4M3_DECODE = 2 };
+/* gmm_options.act_split */
+enum { GMM_SPLIT_AUTO = 0, GMM_SPLIT_PASS = 1, GMM_SPLIT_KERNEL = 2 };
+/* gmm_options.tgmm_kernel */
+enum { GMM_TGMM_AUTO = 0, GMM_TGMM_SINGLE = 1, GMM_TGMM_PAIR = 2 };
+
+/*
+ * Per-call choices for gmm_ex() and tgmm_ex(); NULL, or a zero-filled struct,
+ * means every default.  Every field is checked: an unknown value is
+ * GMM_ERR_SHAPE.  These replace no result: every choice computes the same
+ * outputs within the bound (the kernels differ in speed).
+ *   bf16_kernel   bf16 weights without scale: GMM_KERNEL_AUTO (the tiling table's
+ *                 entry for the problem's class, else the built-in rule) or one of
+ *                 the GMM_KERNEL_* kernels.
+ *   e4m3_kernel   e4m3 weights with bf16 activations: GMM_E4M3_AUTO / _TENSOR (the
+ *                 e4m3 tensor cores, the activations split exactly) or _DECODE (the
+ *                 kernel that decodes the weights to bf16; f32 rhs_scale only).
+ *   act_split     8- and 4-bit weights with bf16 activations: GMM_SPLIT_AUTO (split
+ *                 each row once by a pass when the workspace holds it, else inside
+ *                 the kernel), _PASS (the pass; GMM_ERR_WORKSPACE when the workspace
+ *                 cannot hold it) or _KERNEL (inside the kernel).
+ *   tgmm_kernel   tgmm_ex(): GMM_TGMM_AUTO / _SINGLE (one SM per 128 x 256 output
+ *                 tile) or _PAIR (SM pairs on 256 x 256 tiles).
+ *   wait_limit_cycles  0: the default bound of every internal pipeline wait (about
+ *                 4e9 clock cycles, ~2 s).  Otherwise the bound used by the bf16
+ *                 gmm kernels GMM_KERNEL_SINGLE, _PAIR and _SWAP_PAIR and by the
+ *                 tgmm pair kernel (GMM_TGMM_PAIR), for tests of the timeout path;
+ *                 other kernels ignore it.
+ *   test_drop_stage  0: none.  s > 0 (test of the timeout path): in the one-SM bf16
+ *                 kernel, CTA 0 does not issue the copies of its s-th pipeline
+ *                 stage; in the pair kernels above, the second CTA of the first
+ *                 pair stops issuing copies before its s-th stage.  The wait for
+ *                 that stage runs out: GMM_DEVERR_TIMEOUT is set, the call still
+ *                 returns, every copy and MMA in flight is waited for and the
+ *                 tensor memory freed; that call's output is undefined.  Other
+ *                 kernels ignore it.
+ */
+typedef struct gmm_options {
+  int32_t bf16_kernel;
+  int32_t e4m3_kernel;
+  int32_t act_split;
+  int32_t tgmm_kernel;
+  int64_t wait_limit_cycles;
+  int32_t test_drop_stage;
+  int32_t reserved;
+} gmm_options;
 
 /*
  * Forward grouped matmul (page "tpu-inference ...", gmm.py: gmm).
@@ -133,20 +208,15 @@ size_t gmm_workspace_bytes(void);
  *                and NaNs); realistic activations almost never need it.  Infinite e5m2
  *                weights give +-inf or NaN in the columns they touch (the split's terms can
  *                be zero: inf * 0 is NaN).
- *                GMM_E4M3_KERNEL = decode instead decodes e4m3 weights to bf16 (any other
- *                value than auto, mma or decode: GMM_ERR_SHAPE).  With a full workspace the
- *                split of bf16 activations is made once per row (see gmm_workspace_bytes);
- *                GMM_FP8_ACT_SPLIT = kernel keeps it in the kernel, pre requires the pass
- *                (GMM_ERR_WORKSPACE if it does not fit; any other value than auto, kernel or
- *                pre: GMM_ERR_SHAPE).
+ *                With a workspace that holds it the split of bf16 activations is made once
+ *                per row (see gmm_workspace_bytes); gmm_ex() options choose the other ways
+ *                (gmm_options: e4m3_kernel, act_split).
  *                Without scale, bf16 weights run on one of four kernels chosen from the average
  *                group size m / num_total_groups: SM-pair 256x256 row tiles (>= 1024 rows),
  *                SM-pair tiles of 256 weight rows x up to 256 group rows rounded to 32 (>= 16),
  *                or single-SM tiles of 128 weight rows x group rows rounded to 16 (fewer).
  *                A tiling-table entry for the problem's class (gmm_tune, gmm_tuning_set)
- *                replaces that rule.  The environment variable GMM_BF16_KERNEL = auto |
- *                pair | swap_pair | swap | single overrides both (any other value:
- *                GMM_ERR_SHAPE).  All give
+ *                replaces that rule, and gmm_ex()'s options.bf16_kernel both.  All give
  *                results within the same bound; they may differ in the last bits.
  *   rhs_bias     NULL or device [num_local_groups, 1, n] of bias_dtype (BF16 or F32).
  *   out          [m, n] of out_dtype (BF16 or F32).
@@ -246,16 +316,17 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *                    caller's contents (gmm_into).
  *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k
  *   sub-tile is one e4m3 MMA per token row (exact products, fp32 sums), folded in fp32 as
- *   acc += s[g', b, c] * lhs_scale[r, j] * D.  GMM_E4M3_KERNEL = decode with e4m3 lhs or
- *   E8M0 scales: GMM_ERR_DTYPE.
+ *   acc += s[g', b, c] * lhs_scale[r, j] * D.  options->e4m3_kernel = GMM_E4M3_DECODE with
+ *   e4m3 lhs or E8M0 scales: GMM_ERR_DTYPE.
+ *   options          NULL (every default) or the per-call choices of gmm_options.
  */
 int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_lhs_blocks, int64_t m, int64_t k,
            const void* rhs, int rhs_dtype, int32_t num_local_groups, int64_t n, int transpose_rhs,
            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
            const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
            const void* rhs_block_scale, int rhs_block_scale_dtype, int32_t block_size, const void* rhs_bias,
-           int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace, size_t workspace_bytes,
-           void* stream);
+           int bias_dtype, void* out, int out_dtype, int keep_other_rows, const gmm_options* options, void* workspace,
+           size_t workspace_bytes, void* stream);
 
 /*
  * Backward weight gradient (drhs) per group (page "Megablox: transposed-RHS
@@ -269,9 +340,8 @@ int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_l
  *   group_sizes device int32 [num_groups], 1 <= num_groups <= GMM_MAX_GROUPS.
  *   Sizes: m >= 0, k % 8 == 0, n % 8 == 0, k, n >= 8; pointers 16-byte aligned.
  *   Two kernels give the same results within the bound: one SM per 128 x 256
- *   output tile (default) and SM pairs on 256 x 256 tiles; the environment
- *   variable GMM_TGMM_KERNEL = single | pair | auto selects one (any other value:
- *   GMM_ERR_SHAPE).
+ *   output tile (default) and SM pairs on 256 x 256 tiles (tgmm_ex() with
+ *   options.tgmm_kernel chooses).
  *   For an NT weight [G, n, k] the matching gradient is tgmm(dout, x): pass the
  *   forward output gradient as `lhs` and the forward input as `dout`.
  */
@@ -302,6 +372,15 @@ int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype,
                int32_t num_local_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
                void* stream);
 
+/*
+ * tgmm_ex: tgmm_local() with per-call options (NULL: every default); only
+ * options->tgmm_kernel applies.
+ */
+int tgmm_ex(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
+            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset, int32_t num_local_groups,
+            void* out, int out_dtype, const gmm_options* options, void* workspace, size_t workspace_bytes,
+            void* stream);
+
 /* Size of the device scratch array compiled into the library for gmm_noalloc(). */
 #define GMM_NOALLOC_SCRATCH_BYTES 256
 
@@ -321,9 +400,13 @@ int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype,
  *    same kernels run); GMM_ERR_WORKSPACE if the library's scratch need ever
  *    exceeded the array (it is one word of error flags, independent of the
  *    problem size, so every size gmm() accepts fits).
- *  - The first call on a device sets up that device: with the device current
- *    it takes the array's device address (cudaGetSymbolAddress).  Make that
- *    first call before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress; after cudaDeviceReset it finds the new copy).  The
+ *    first call on a device also loads the library's device code there: make
+ *    it before any stream capture.
+ *  - It takes every default of gmm_options: with bf16 activations and 8- or
+ *    4-bit weights the kernel splits the rows itself (the array has no room
+ *    for the split pass).
  *  - Every call on a device shares the array, and the array keeps the last
  *    call's contents; each call first clears the error-flag word (an
  *    asynchronous memset on `stream`).  Calls that overlap on the GPU (on
@@ -362,17 +445,11 @@ int gmm_quantize_e4m3(const void* x, int x_dtype, int64_t m, int64_t k, int64_t 
  *   rows_log2 = floor(log2(m / num_total_groups)) (average rows per group),
  *   k, n, num_total_groups, transpose_rhs (0/1), out_dtype.
  * gmm(), gmm_into() and gmm_device_offset() with bf16 weights and no scale use
- * the table's entry for their class when there is one (the GMM_BF16_KERNEL
- * environment variable still overrides it), else the built-in rule.  The table is
+ * the table's entry for their class when there is one (gmm_ex()'s options.bf16_kernel
+ * still overrides it), else the built-in rule.  The table is
  * guarded by a mutex; calls on any thread see every completed update.
  */
-enum {
-  GMM_KERNEL_AUTO = 0,      /* no entry / built-in rule */
-  GMM_KERNEL_PAIR = 1,      /* SM-pair 256 x 256 row tiles */
-  GMM_KERNEL_SWAP_PAIR = 2, /* SM-pair, 256 weight rows x up to 256 group rows */
-  GMM_KERNEL_SWAP = 3,      /* one SM, 128 weight rows x up to 256 group rows */
-  GMM_KERNEL_SINGLE = 4     /* one SM, 128 x 256 row tiles */
-};
+/* (The kernel ids are the GMM_KERNEL_* values above.) */
 
 /* Sets the entry of one problem class.  raster: 0 (default, 8) or 1..64 n tiles
  * per super-column (used by PAIR and SINGLE).  GMM_ERR_SHAPE for invalid values. */
@@ -413,6 +490,15 @@ int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
  * (GMM_DEVERR_*) of `workspace` into *flags.  Returns GMM_OK or GMM_ERR_CUDA.
  */
 int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags);
+
+/*
+ * The device's report as one status: synchronises `stream`, reads and clears the
+ * sticky flags of `workspace` (as gmm_read_device_errors) and returns GMM_OK when
+ * none is set, else GMM_ERR_TIMEOUT, GMM_ERR_DEVICE_GROUP_SIZES or
+ * GMM_ERR_GROUP_OFFSET (in that order of precedence), or GMM_ERR_NULL /
+ * GMM_ERR_CUDA when it cannot read them.
+ */
+int gmm_get_device_error(void* workspace, void* stream);
 
 /* Static English text for a status code. */
 const char* gmm_status_string(int status);

@@ -23,7 +23,8 @@ import threading
 import torch
 
 __all__ = ["gmm", "gmm_into", "tgmm", "tgmm_local", "quantize_e4m3", "tune", "tuning_set", "tuning_get", "tuning_clear",
-           "tuning_save", "tuning_load", "tuning_rows_log2", "read_device_errors", "workspace_for", "GmmError", "LIB_PATH", "load_library",
+           "tuning_save", "tuning_load", "tuning_rows_log2", "read_device_errors", "get_device_error", "workspace_for",
+           "release_workspaces", "options", "GmmOptions", "GmmError", "LIB_PATH", "load_library",
            "DEVERR_NEGATIVE_GROUP_SIZE", "DEVERR_GROUP_SIZES_EXCEED_M", "DEVERR_TIMEOUT"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
@@ -31,8 +32,13 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgmm.so")
 DTYPE_BF16, DTYPE_F32, DTYPE_E4M3, DTYPE_E5M2, DTYPE_INT8, DTYPE_INT4, DTYPE_UINT4, DTYPE_E2M1, DTYPE_E8M0 = range(9)
 # Packed 4-bit weight formats (uint8 tensors [L, n, k / 2], even k in the low nibble), by name.
 PACKED_FORMATS = {"int4": DTYPE_INT4, "uint4": DTYPE_UINT4, "e2m1": DTYPE_E2M1}
-# bf16 forward kernels, as the tiling table names them.
+# bf16 forward kernels, as the tiling table and the options name them.
 KERNEL_AUTO, KERNEL_PAIR, KERNEL_SWAP_PAIR, KERNEL_SWAP, KERNEL_SINGLE = range(5)
+KERNEL_IDS = {"auto": KERNEL_AUTO, "pair": KERNEL_PAIR, "swap_pair": KERNEL_SWAP_PAIR, "swap": KERNEL_SWAP,
+              "single": KERNEL_SINGLE}
+E4M3_KERNELS = {"auto": 0, "tensor": 1, "decode": 2}
+ACT_SPLITS = {"auto": 0, "pass": 1, "kernel": 2}
+TGMM_KERNELS = {"auto": 0, "single": 1, "pair": 2}
 DEVERR_NEGATIVE_GROUP_SIZE, DEVERR_GROUP_SIZES_EXCEED_M, DEVERR_TIMEOUT, DEVERR_GROUP_OFFSET = 0x1, 0x2, 0x4, 0x8
 
 _TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.float8_e4m3fn: DTYPE_E4M3,
@@ -41,6 +47,51 @@ _TORCH_TO_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.fl
 _lock = threading.Lock()
 _lib = None
 _workspaces: dict[tuple[int, int], torch.Tensor] = {}
+_defaults = threading.local()
+
+
+class GmmOptions(ctypes.Structure):
+    """gmm_options of the C ABI: per-call kernel choices (0 everywhere = every default)."""
+    _fields_ = [("bf16_kernel", ctypes.c_int32), ("e4m3_kernel", ctypes.c_int32), ("act_split", ctypes.c_int32),
+                ("tgmm_kernel", ctypes.c_int32), ("wait_limit_cycles", ctypes.c_int64),
+                ("test_drop_stage", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def _make_options(bf16_kernel="auto", e4m3_kernel="auto", act_split="auto", tgmm_kernel="auto", wait_limit_cycles=0,
+                  test_drop_stage=0, **unknown):
+    if unknown:
+        raise TypeError(f"unknown options {sorted(unknown)}")
+    o = GmmOptions()
+    o.bf16_kernel = bf16_kernel if isinstance(bf16_kernel, int) else KERNEL_IDS[bf16_kernel]
+    o.e4m3_kernel = e4m3_kernel if isinstance(e4m3_kernel, int) else E4M3_KERNELS[e4m3_kernel]
+    o.act_split = act_split if isinstance(act_split, int) else ACT_SPLITS[act_split]
+    o.tgmm_kernel = tgmm_kernel if isinstance(tgmm_kernel, int) else TGMM_KERNELS[tgmm_kernel]
+    o.wait_limit_cycles = int(wait_limit_cycles)
+    o.test_drop_stage = int(test_drop_stage)
+    return o
+
+
+class options:
+    """Kernel choices for the calls made on this thread inside the block, e.g.
+    ``with options(bf16_kernel="pair"): gmm(...)``; passed to the library as its
+    per-call gmm_options (the library reads no environment variable for them)."""
+
+    def __init__(self, **kw):
+        self.kw = kw
+
+    def __enter__(self):
+        self.saved = getattr(_defaults, "kw", {})
+        _defaults.kw = {**self.saved, **self.kw}
+        return self
+
+    def __exit__(self, *exc):
+        _defaults.kw = self.saved
+        return False
+
+
+def _current_options(extra):
+    kw = {**getattr(_defaults, "kw", {}), **(extra or {})}
+    return _make_options(**kw) if kw else None
 
 # Every function the header declares, with its ctypes signature.
 _P, _I, _I32, _I64, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t,
@@ -48,6 +99,7 @@ _P, _I, _I32, _I64, _SZ, _U32P = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32,
 _IP = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "gmm_workspace_bytes": ([], _SZ),
+    "gmm_workspace_bytes_for": ([_I64, _I64, _I64, _I32, _I32, _I, _I], _SZ),
     "gmm": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
     "tgmm": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _P, _I, _P, _SZ, _P], _I),
     "gmm_into": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P, _SZ, _P], _I),
@@ -57,7 +109,8 @@ SIGNATURES = {
     "gmm_noalloc": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I32, _P, _I, _P, _I, _P], _I),
     "gmm_quantize_e4m3": ([_P, _I, _I64, _I64, _I64, _P, _P, _P], _I),
     "gmm_ex": ([_P, _I, _P, _I32, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _P, _I, _I32, _P, _I, _I32, _P,
-                _I, _P, _I, _I, _P, _SZ, _P], _I),
+                _I, _P, _I, _I, _P, _P, _SZ, _P], _I),
+    "tgmm_ex": ([_P, _I, _P, _I, _I64, _I64, _I64, _P, _I32, _I32, _I32, _P, _I, _P, _P, _SZ, _P], _I),
     "gmm_tuning_set": ([_I32, _I64, _I64, _I32, _I, _I, _I, _I], _I),
     "gmm_tuning_get": ([_I32, _I64, _I64, _I32, _I, _I, _IP, _IP], _I),
     "gmm_tuning_clear": ([], _I),
@@ -66,6 +119,7 @@ SIGNATURES = {
     "gmm_tune": ([_P, _I, _I64, _I64, _P, _I, _I32, _I64, _I, _P, _I32, _I32, _P, _I, _P, _I, _P, _SZ, _P, _I, _IP,
                   _IP, ctypes.POINTER(ctypes.c_float)], _I),
     "gmm_read_device_errors": ([_P, _P, _U32P], _I),
+    "gmm_get_device_error": ([_P, _P], _I),
     "gmm_status_string": ([_I], ctypes.c_char_p),
     "gmm_last_cuda_error": ([], _I),
 }
@@ -117,6 +171,14 @@ def workspace_for(device: torch.device, stream=None) -> torch.Tensor:
     return ws
 
 
+def release_workspaces(device=None) -> None:
+    """Drops the cached default workspaces (of one device, or of all), e.g. after using
+    many short-lived streams.  Their device error flags go with them."""
+    idx = None if device is None else torch.device(device).index
+    for key in [k for k in _workspaces if idx is None or k[0] == idx]:
+        del _workspaces[key]
+
+
 def _code(t: torch.Tensor) -> int:
     try:
         return _TORCH_TO_CODE[t.dtype]
@@ -138,8 +200,9 @@ def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out, out_dtype,
-              workspace, stream, rhs_format, lhs_scale=None, rhs_block_scale=None):
+              workspace, stream, rhs_format, lhs_scale=None, rhs_block_scale=None, opts=None):
     lib = load_library()
+    opt = _current_options(opts)
     _dev(lhs, "lhs"), _dev(rhs, "rhs"), _dev(group_sizes, "group_sizes")
     if group_sizes.dtype != torch.int32:
         raise TypeError("group_sizes must be int32")
@@ -171,8 +234,9 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
         _dev(rhs_block_scale, "rhs_block_scale")
         if rhs_block_scale.dim() != 3 or k % rhs_block_scale.shape[2] != 0:
             raise ValueError("rhs_block_scale must be [G_local, n, k / block_size]")
-    if lhs.dtype == torch.float8_e4m3fn or lhs_scale is not None or e8m0 or rhs_block_scale is not None:
-        # e4m3 activations with their scales, or E8M0 weight scales: gmm_ex
+    if (lhs.dtype == torch.float8_e4m3fn or lhs_scale is not None or e8m0 or rhs_block_scale is not None
+            or opt is not None):
+        # e4m3 activations with their scales, E8M0 weight scales, block scales or options: gmm_ex
         if lhs_scale is not None:
             _dev(lhs_scale, "lhs_scale")
             if lhs_scale.dtype != torch.float32 or lhs_scale.dim() != 2 or lhs_scale.shape[0] != m:
@@ -193,7 +257,8 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
                         0 if rhs_block_scale is None else k // rhs_block_scale.shape[2],
                         None if rhs_bias is None else rhs_bias.data_ptr(),
                         0 if rhs_bias is None else _code(rhs_bias), out.data_ptr(), _code(out),
-                        int(fn == "gmm_into"), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
+                        int(fn == "gmm_into"), None if opt is None else ctypes.byref(opt), ws.data_ptr(), ws.numel(),
+                        _stream(lhs.device, stream))
         if rc != 0:
             raise GmmError("gmm_ex", rc)
         return out
@@ -219,7 +284,7 @@ def _gmm_call(fn, lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, gro
 
 def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0, out=None,
         out_dtype=torch.bfloat16, workspace=None, stream=None, rhs_format=None, lhs_scale=None,
-        rhs_block_scale=None):
+        rhs_block_scale=None, options=None):
     """out[r] = lhs[r] @ W_g^T (NT, rhs [G_local, n, k]) or lhs[r] @ W_g (NN, rhs [G_local, k, n])
     for each row r of local group g; all other rows of out are zero.  group_offset is an int, or a
     one-element int32 CUDA tensor that the kernel reads when it runs.  rhs is bf16, float8_e4m3fn,
@@ -228,23 +293,24 @@ def gmm(lhs, rhs, group_sizes, rhs_scale=None, rhs_bias=None, transpose_rhs=True
     E8M0 codes of that shape.  lhs may be float8_e4m3fn (W8A8) with lhs_scale float32
     [m, num_lhs_blocks] (quantize_e4m3's scales).  rhs_block_scale: microscaling scales, uint8 E8M0
     [G_local, n, k / 32] of float8_e4m3fn weights (MXFP8) or float8_e4m3fn [G_local, n, k / 16] of
-    packed e2m1 weights (NVFP4)."""
+    packed e2m1 weights (NVFP4).  options: a dict of gmm_options fields (bf16_kernel, e4m3_kernel,
+    act_split, wait_limit_cycles, test_drop_stage), over those of an enclosing ``options`` block."""
     return _gmm_call("gmm", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out_dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale)
+                     out_dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale, options)
 
 
 def gmm_into(lhs, rhs, group_sizes, out, rhs_scale=None, rhs_bias=None, transpose_rhs=True, group_offset=0,
-             workspace=None, stream=None, rhs_format=None, lhs_scale=None, rhs_block_scale=None):
+             workspace=None, stream=None, rhs_format=None, lhs_scale=None, rhs_block_scale=None, options=None):
     """As gmm, but only the local groups' rows of `out` are written; every other row keeps the
     caller's contents (the existing-output mode)."""
     if out is None:
         raise ValueError("gmm_into needs an output tensor")
     return _gmm_call("gmm_into", lhs, rhs, group_sizes, rhs_scale, rhs_bias, transpose_rhs, group_offset, out,
-                     out.dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale)
+                     out.dtype, workspace, stream, rhs_format, lhs_scale, rhs_block_scale, options)
 
 
 def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, out=None, out_dtype=torch.float32,
-               workspace=None, stream=None):
+               workspace=None, stream=None, options=None):
     """out[l] = lhs_g^T @ dout_g for g = group_offset + l, 0 <= l < num_local_groups (zero blocks for
     empty groups); group rows come from all of group_sizes."""
     lib = load_library()
@@ -263,15 +329,16 @@ def tgmm_local(lhs, dout, group_sizes, group_offset=0, num_local_groups=None, ou
     if tuple(out.shape) != (L, k, n):
         raise ValueError(f"out must be [{L}, {k}, {n}], got {list(out.shape)}")
     ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
-    rc = lib.tgmm_local(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(),
-                        G, int(group_offset), L, out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(),
-                        _stream(lhs.device, stream))
+    opt = _current_options(options)
+    rc = lib.tgmm_ex(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(),
+                     G, int(group_offset), L, out.data_ptr(), _code(out), None if opt is None else ctypes.byref(opt),
+                     ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
     if rc != 0:
-        raise GmmError("tgmm_local", rc)
+        raise GmmError("tgmm_ex", rc)
     return out
 
 
-def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=None, stream=None):
+def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=None, stream=None, options=None):
     """out[g] = lhs_g^T @ dout_g for every group g (zero blocks for empty groups)."""
     lib = load_library()
     _dev(lhs, "lhs"), _dev(dout, "dout"), _dev(group_sizes, "group_sizes")
@@ -286,6 +353,14 @@ def tgmm(lhs, dout, group_sizes, out=None, out_dtype=torch.float32, workspace=No
         out = torch.empty((G, k, n), dtype=out_dtype, device=lhs.device)
     _dev(out, "out")
     ws = workspace if workspace is not None else workspace_for(lhs.device, stream)
+    opt = _current_options(options)
+    if opt is not None:
+        rc = lib.tgmm_ex(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(), G,
+                         0, G, out.data_ptr(), _code(out), ctypes.byref(opt), ws.data_ptr(), ws.numel(),
+                         _stream(lhs.device, stream))
+        if rc != 0:
+            raise GmmError("tgmm_ex", rc)
+        return out
     rc = lib.tgmm(lhs.data_ptr(), _code(lhs), dout.data_ptr(), _code(dout), m, k, n, group_sizes.data_ptr(), G,
                   out.data_ptr(), _code(out), ws.data_ptr(), ws.numel(), _stream(lhs.device, stream))
     if rc != 0:
@@ -364,6 +439,15 @@ def tune(lhs, rhs, group_sizes, rhs_bias=None, transpose_rhs=True, group_offset=
                       int(iterations), ctypes.byref(kern), ctypes.byref(ras), ctypes.byref(ms))
     _check("gmm_tune", rc)
     return kern.value, ras.value, ms.value
+
+
+def get_device_error(device=None, workspace=None, stream=None) -> int:
+    """Synchronises the stream and returns the device's report as one status (0 = none),
+    clearing the flags (gmm_get_device_error)."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = workspace if workspace is not None else workspace_for(dev, stream)
+    return int(lib.gmm_get_device_error(ws.data_ptr(), _stream(dev, stream)))
 
 
 def read_device_errors(device=None, workspace=None, stream=None) -> int:

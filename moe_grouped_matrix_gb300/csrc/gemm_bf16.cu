@@ -65,6 +65,8 @@ struct Params {
   int32_t raster;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
+  long long wait_limit;             // bound of every pipeline wait, in clock cycles
+  int32_t drop_stage;               // 0, or s > 0: CTA 0 does not issue its s-th stage (timeout test)
 };
 
 template <bool kOutF32>
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_of = [&](int32_t w) {
     return decode_gemm_tile(w, m_tiles, n_tiles, p.raster, tiles, offs, go, p.num_local_groups, BM);
   };
+  auto waitb = [&](uint32_t bar, uint32_t parity) { return wait_bar(bar, parity, abort_flag, p.err, p.wait_limit); };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -167,12 +170,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, pend_mask = 0;
       uint32_t pend_par[STAGES];
       bool ok = true;
+      int32_t issued = 0;  // stages this CTA has handled
       for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const GemmTile t = tile_of(w);
         for (int32_t kb = 0; kb < k_blocks; ++kb) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+          if (!waitb(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
+          }
+          if (blockIdx.x == 0 && ++issued == p.drop_stage) {
+            // timeout test: this stage's copies are never issued (none is in
+            // flight for it), so the MMA warp's wait for it runs out
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -205,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      if (!wait_bar(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+      if (!waitb(acce_bar(acc), acc_phase ^ 1u)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int32_t kb = 0; kb < k_blocks; ++kb) {
-        if (!wait_bar(full_bar(stage), phase, abort_flag, p.err)) {
+        if (!waitb(full_bar(stage), phase)) {
           ok = false;
           break;
         }
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t w = blockIdx.x; w < total; w += gridDim.x) {
       const GemmTile t = tile_of(w);
-      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      if (!waitb(accf_bar(acc), acc_phase)) break;
       tc_fence_after();
       const int32_t row = t.row0 + row_in_tile;
       const bool valid = row < t.row_end;
@@ -302,7 +315,8 @@ cudaError_t launch_impl(const GemmLaunch& L, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.bias,
-           L.bias_f32, L.err, L.raster, L.zero_rest, L.group_offset_dev};
+           L.bias_f32, L.err, L.raster, L.zero_rest, L.group_offset_dev,
+           L.wait_limit > 0 ? (long long)L.wait_limit : kWaitLimitCycles, L.drop_stage};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

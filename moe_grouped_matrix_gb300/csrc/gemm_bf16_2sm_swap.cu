@@ -57,12 +57,14 @@ constexpr uint32_t OFF_ACCE = OFF_ACCF + 16;
 constexpr uint32_t OFF_DONE = OFF_ACCE + 16;
 constexpr uint32_t OFF_TMEM = OFF_DONE + 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
+constexpr uint32_t OFF_REPORT = OFF_ABORT + 4;  // pair_report's barrier and count (leader's)
+constexpr uint32_t OFF_RWORD = OFF_REPORT + 8;
 constexpr uint32_t OFF_OFFS = OFF_CTRL + 256;
 constexpr uint32_t OFF_TILES = OFF_OFFS + 4 * (kMaxGroups + 4);
 constexpr uint32_t SMEM_USED = OFF_TILES + 4 * (kMaxGroups + 4);
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
+static_assert(OFF_RWORD + 4 <= OFF_OFFS && OFF_REPORT % 8 == 0, "control block overlaps the tables");
 
 struct Params {
   const int32_t* group_sizes;
@@ -75,6 +77,8 @@ struct Params {
   int32_t raster;
   int32_t zero_rest;  // zero the rows outside the local groups (gmm) or leave them (gmm_into)
   const int32_t* group_offset_dev;  // NULL, or the device scalar that replaces group_offset
+  long long wait_limit;             // bound of every pipeline wait, in clock cycles
+  int32_t drop_stage;               // 0, or s > 0: the first pair's second CTA stops before its s-th stage (test)
 };
 
 // Rows of the item's chunk, and the MMA N covering them (a multiple of 32, so
@@ -117,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(b), 8);  // one lane of each epilogue warp of both CTAs
     }
     mbar_init(done_bar, 1);
+    mbar_init(sbase + OFF_REPORT, 1);  // the follower's pair_report
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch(&tm_lhs);
@@ -145,6 +150,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return decode_gemm_tile(w, t_tiles, n_tiles, n_tiles, tiles, offs, go, p.num_local_groups, CHUNK);
   };
 
+  // the bytes one CTA's copies of a stage of work item w carry
+  auto cta_stage_bytes = [&](int32_t w) {
+    return A_BYTES + uint32_t(KH * ((chunk_n(tile_of(w)) / 2 + 63) / 64)) * TBOX_BYTES;
+  };
+
+  uint32_t issued = 0;  // producer: stages of the pair's sequence this CTA issued (leader: armed)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
@@ -157,7 +168,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t trow = t.row0 + int32_t(rank) * half;
         const int32_t wrow = t.n_tile * PAIR_W + int32_t(rank) * BW;
         for (int32_t kb = 0; kb < k_blocks; ++kb) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err, p.wait_limit)) {
+            ok = false;
+            break;
+          }
+          if (blockIdx.x == 1 && issued + 1 == uint32_t(p.drop_stage)) {
+            // timeout test: the follower stops issuing, so the leader's wait for
+            // this stage's bytes runs out
             ok = false;
             break;
           }
@@ -178,19 +195,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int32_t j = 0; j < nbox; ++j)
               tma_load_2d_pair(b_dst + kh * B_HALF + j * TBOX_BYTES, &tm_lhs, fb, kc, trow + 64 * j);
           }
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // Copies already issued complete on their own within microseconds;
-        // give them a bounded moment before this CTA unwinds.
-        const long long t0 = clock64();
-        while (clock64() - t0 < kDrainLimitCycles) {
-        }
-      }
+      if (!leader) pair_report(sbase + OFF_REPORT, sbase + OFF_RWORD, issued);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (leader CTA)
@@ -201,11 +213,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const GemmTile t = tile_of(w);
         // A = weights (K-major for NT, MN-major for NN), B = the chunk's rows (K-major)
         const uint32_t idesc = idesc_bf16(2 * BW, chunk_n(t), !kNT, false);
-        if (!wait_bar_cluster(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (!wait_bar_cluster(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * CHUNK;
         for (int32_t kb = 0; kb < k_blocks; ++kb) {
-          if (!wait_bar(full_bar(stage), phase, abort_flag, p.err)) {
+          if (!wait_bar(full_bar(stage), phase, abort_flag, p.err, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -260,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bias = p.bias_f32 ? __ldg(static_cast<const float*>(p.bias) + bi)
                           : __bfloat162float(static_cast<const __nv_bfloat16*>(p.bias)[bi]);
       }
-      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err, p.wait_limit)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t(quarter * 32) << 16) + acc * CHUNK;
 #pragma unroll 1
@@ -309,7 +321,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the leader's MMAs are done and no signal targets either CTA any more
+  if (leader && warp == 0 && lane == 0 && *abort_flag) {
+    st_shared_cluster_u32(mapa_shared(sbase + OFF_ABORT, 1), 1u);  // the follower's waits end too
+    // stage i of the sequence belongs to the pair's (i / k_blocks)-th work item
+    pair_drain<STAGES>(full_bar(0), sbase + OFF_REPORT, sbase + OFF_RWORD, issued, p.wait_limit,
+                       [&](uint32_t i) { return cta_stage_bytes(pair + int32_t(i / uint32_t(k_blocks)) * npairs); });
+  }
+  cluster_sync();  // the leader's MMAs and every copy are done; no signal targets either CTA any more
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -332,7 +350,8 @@ cudaError_t launch_impl(const GemmLaunch& L, int max_ctas, cudaStream_t stream) 
   if (clusters < 1) return cudaErrorLaunchOutOfResources;
   const int grid = 2 * (clusters < max_ctas / 2 ? clusters : max_ctas / 2);
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.bias,
-           L.bias_f32, L.err, L.raster, L.zero_rest, L.group_offset_dev};
+           L.bias_f32, L.err, L.raster, L.zero_rest, L.group_offset_dev,
+           L.wait_limit > 0 ? (long long)L.wait_limit : kWaitLimitCycles, L.drop_stage};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_rhs, p);
   return cudaGetLastError();
 }

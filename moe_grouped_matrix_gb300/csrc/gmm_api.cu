@@ -8,6 +8,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -132,8 +133,8 @@ bool fits_i32(int64_t v) { return v >= 0 && v <= INT32_MAX; }
 //   kSingle   one SM, 128 x 256 tiles of rows x n.
 // Groups averaging 1024 rows or more go to kPair, 16 or more to kSwapPair,
 // fewer to kSwap, unless the tiling table has an entry for the problem's class
-// (tuning.cu).  GMM_BF16_KERNEL = single | pair | swap | swap_pair overrides both
-// (for tuning and tests).
+// (tuning.cu).  A per-call gmm_options.bf16_kernel overrides both (for tuning
+// and tests).
 enum class BF16Kernel { kSingle, kPair, kSwap, kSwapPair, kInvalid };
 
 BF16Kernel kernel_of_id(int id) {
@@ -147,18 +148,11 @@ BF16Kernel kernel_of_id(int id) {
 }
 
 // The kernel and raster (0: default) for a problem; `forced` (a GMM_KERNEL_* id,
-// from gmm_tune) wins over everything.
+// from gmm_tune or the caller's options) wins over everything.
 BF16Kernel choose_bf16_kernel(int64_t m, int64_t k, int64_t n, int32_t num_total_groups, int transpose_rhs,
                               int out_dtype, int forced, int32_t* raster) {
   *raster = 0;
   if (forced != GMM_KERNEL_AUTO) return kernel_of_id(forced);
-  if (const char* env = std::getenv("GMM_BF16_KERNEL")) {
-    if (std::strcmp(env, "single") == 0) return BF16Kernel::kSingle;
-    if (std::strcmp(env, "pair") == 0) return BF16Kernel::kPair;
-    if (std::strcmp(env, "swap") == 0) return BF16Kernel::kSwap;
-    if (std::strcmp(env, "swap_pair") == 0) return BF16Kernel::kSwapPair;
-    if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return BF16Kernel::kInvalid;
-  }
   int32_t id = GMM_KERNEL_AUTO;
   if (gmmk::tuning_lookup(gmmk::tuning_rows_log2(m, num_total_groups), k, n, num_total_groups, transpose_rhs != 0,
                           out_dtype, &id, raster))
@@ -168,28 +162,26 @@ BF16Kernel choose_bf16_kernel(int64_t m, int64_t k, int64_t n, int32_t num_total
   return BF16Kernel::kSwap;
 }
 
-// e4m3 weights run on the e4m3 tensor-core kernel (gemm_fp8.cu) by default;
-// GMM_E4M3_KERNEL = decode selects the kernel that decodes the weights to bf16
-// (gemm_scaled.cu), kept for comparison.  -1: unknown value.
-int choose_e4m3_decode() {
-  if (const char* env = std::getenv("GMM_E4M3_KERNEL")) {
-    if (std::strcmp(env, "decode") == 0) return 1;
-    if (std::strcmp(env, "auto") != 0 && std::strcmp(env, "mma") != 0 && env[0] != '\0') return -1;
-  }
-  return 0;
+// Every field of the caller's options in range (GMM_ERR_SHAPE otherwise).
+bool options_valid(const gmm_options& o) {
+  return o.bf16_kernel >= GMM_KERNEL_AUTO && o.bf16_kernel <= GMM_KERNEL_SINGLE && o.e4m3_kernel >= GMM_E4M3_AUTO &&
+         o.e4m3_kernel <= GMM_E4M3_DECODE && o.act_split >= GMM_SPLIT_AUTO && o.act_split <= GMM_SPLIT_KERNEL &&
+         o.tgmm_kernel >= GMM_TGMM_AUTO && o.tgmm_kernel <= GMM_TGMM_PAIR && o.wait_limit_cycles >= 0 &&
+         o.test_drop_stage >= 0 && o.reserved == 0;
 }
 
-// GMM_FP8_ACT_SPLIT = kernel keeps the two-term split of bf16 activations inside
-// the fp8 kernel (per row and weight tile) instead of a split pass per row;
-// pre insists on the pass (GMM_ERR_WORKSPACE when the workspace cannot hold
-// it).  1: auto, 0: kernel, 2: pre, -1: unknown value.
-int choose_act_split() {
-  if (const char* env = std::getenv("GMM_FP8_ACT_SPLIT")) {
-    if (std::strcmp(env, "kernel") == 0) return 0;
-    if (std::strcmp(env, "pre") == 0) return 2;
-    if (std::strcmp(env, "auto") != 0 && env[0] != '\0') return -1;
-  }
-  return 1;
+// GMM_LOG: one line per call on stderr when the variable is set and not "0".
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GMM_LOG");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+const char* dtype_name(int d) {
+  static const char* names[] = {"bf16", "f32", "e4m3", "e5m2", "int8", "int4", "uint4", "e2m1", "e8m0"};
+  return d >= 0 && d <= GMM_DTYPE_E8M0 ? names[d] : "?";
 }
 
 }  // namespace
@@ -197,6 +189,17 @@ int choose_act_split() {
 extern "C" {
 
 size_t gmm_workspace_bytes(void) { return kWorkspaceBytes; }
+
+size_t gmm_workspace_bytes_for(int64_t m, int64_t k, int64_t n, int32_t num_total_groups, int32_t num_local_groups,
+                               int lhs_dtype, int rhs_dtype) {
+  (void)n, (void)num_total_groups, (void)num_local_groups;
+  if (m < 0 || k < 0) return 0;
+  const bool split = lhs_dtype == GMM_DTYPE_BF16 && rhs_dtype >= GMM_DTYPE_E4M3 && rhs_dtype <= GMM_DTYPE_E2M1;
+  if (!split) return kWorkspaceMinBytes;
+  const int64_t step = rhs_dtype == GMM_DTYPE_INT8 ? 128 : 256;
+  const size_t scales_at = (kActOffset + size_t(4 * m * k) + 255) & ~size_t(255);
+  return scales_at + size_t(m * ((k + step - 1) / step)) * 2 * sizeof(float);
+}
 
 const char* gmm_status_string(int status) {
   switch (status) {
@@ -210,6 +213,8 @@ const char* gmm_status_string(int status) {
     case GMM_ERR_ARCH: return "current device is not compute capability 10.3";
     case GMM_ERR_CUDA: return "CUDA call failed";
     case GMM_ERR_IO: return "tiling-table file could not be read, parsed or written";
+    case GMM_ERR_DEVICE_GROUP_SIZES: return "the device saw negative group sizes or sizes summing past m";
+    case GMM_ERR_TIMEOUT: return "an internal pipeline wait gave up (the call's output is undefined)";
   }
   return "unknown status";
 }
@@ -223,6 +228,15 @@ int gmm_read_device_errors(void* workspace, void* stream, uint32_t* flags) {
   if (e == cudaSuccess) e = cudaMemcpy(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(workspace, 0, sizeof(uint32_t));
   if (e != cudaSuccess) return cuda_fail(e);
+  return GMM_OK;
+}
+
+int gmm_get_device_error(void* workspace, void* stream) {
+  uint32_t flags = 0;
+  if (int st = gmm_read_device_errors(workspace, stream, &flags)) return st;
+  if (flags & GMM_DEVERR_TIMEOUT) return GMM_ERR_TIMEOUT;
+  if (flags & (GMM_DEVERR_NEGATIVE_GROUP_SIZE | GMM_DEVERR_GROUP_SIZES_EXCEED_M)) return GMM_ERR_DEVICE_GROUP_SIZES;
+  if (flags & GMM_DEVERR_GROUP_OFFSET) return GMM_ERR_GROUP_OFFSET;
   return GMM_OK;
 }
 
@@ -248,8 +262,12 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              int32_t num_total_groups, int32_t group_offset, const void* rhs_scale, int32_t num_quant_blocks,
              const void* rhs_bias, int bias_dtype, void* out, int out_dtype, void* workspace,
              size_t workspace_bytes, void* stream, int32_t zero_rest, const int32_t* group_offset_dev,
-             int forced_kernel = GMM_KERNEL_AUTO, int32_t forced_raster = 0, const ExtArgs& ext = ExtArgs{}) {
+             const gmm_options* options = nullptr, int32_t forced_raster = 0, const ExtArgs& ext = ExtArgs{},
+             const char* entry = "gmm") {
   if (lhs == nullptr || rhs == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
+  const gmm_options opt = options != nullptr ? *options : gmm_options{};
+  if (!options_valid(opt)) return GMM_ERR_SHAPE;
+  const int forced_kernel = opt.bf16_kernel;
   // e4m3 activations (W8A8) run on the fp8 kernels only: 8- or 4-bit weights.
   const bool lhs8 = lhs_dtype == GMM_DTYPE_E4M3;
   if (lhs_dtype != GMM_DTYPE_BF16 && !lhs8) return GMM_ERR_DTYPE;
@@ -303,6 +321,8 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       (rhs_scale && !aligned16(rhs_scale)))
     return GMM_ERR_ALIGN;
   if (rhs_dtype == GMM_DTYPE_E2M1 && (reinterpret_cast<uintptr_t>(rhs) & 31u) != 0) return GMM_ERR_ALIGN;
+  // the e4m3 decoding kernel takes bf16 activations and f32 scales
+  if (rhs_dtype == GMM_DTYPE_E4M3 && opt.e4m3_kernel == GMM_E4M3_DECODE && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;
   if (workspace == nullptr || workspace_bytes < kWorkspaceMinBytes || !aligned16(workspace)) return GMM_ERR_WORKSPACE;
   DeviceInfo dev;
   if (int st = current_device(&dev)) return st;
@@ -363,8 +383,8 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     S.lhs_raw = lhs;
     S.rhs_raw = rhs;
     const bool f32 = out_dtype == GMM_DTYPE_F32;
-    const int act_split = choose_act_split();
-    if (act_split < 0) return GMM_ERR_SHAPE;
+    // 1: split pass when the workspace holds it, 2: the pass or GMM_ERR_WORKSPACE, 0: in the kernel
+    const int act_split = opt.act_split == GMM_SPLIT_KERNEL ? 0 : (opt.act_split == GMM_SPLIT_PASS ? 2 : 1);
     // The fp8 kernels; bf16 activations are split once per row into the
     // workspace when it has room (act_split.cu), in the kernel's k steps.
     auto fp8_kernel = [&](int fmt) -> int {
@@ -390,20 +410,35 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
           return GMM_ERR_WORKSPACE;
         }
       }
+      if (log_enabled())
+        std::fprintf(stderr, "libgmm: %s m=%lld k=%lld n=%lld groups=%d local=%d offset=%s lhs=%s rhs=%s out=%s "
+                             "kernel=fp8 split=%s\n",
+                     entry, (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups,
+                     group_offset_dev ? "device" : "host", dtype_name(lhs_dtype), dtype_name(rhs_dtype),
+                     dtype_name(out_dtype), lhs8 ? "none" : (S.lhs_split ? "pass" : "kernel"));
       if (cudaError_t e2 = gmmk::launch_fp8(S, fmt, f32, dev.sms, s)) return cuda_fail(e2);
       return GMM_OK;
     };
+    auto log_decoding = [&] {
+      if (log_enabled())
+        std::fprintf(stderr, "libgmm: %s m=%lld k=%lld n=%lld groups=%d local=%d offset=%s lhs=%s rhs=%s out=%s "
+                             "kernel=decoding%s\n",
+                     entry, (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups,
+                     group_offset_dev ? "device" : "host", dtype_name(lhs_dtype), dtype_name(rhs_dtype),
+                     dtype_name(out_dtype), mx ? " block-scales" : "");
+    };
     cudaError_t e;
     if (rhs_dtype == GMM_DTYPE_BF16) {
+      log_decoding();
       e = gmmk::launch_scaled(S, false, f32, dev.sms, s);
     } else if (rhs_dtype == GMM_DTYPE_E4M3) {
-      int decode = choose_e4m3_decode();
-      if (decode < 0) return GMM_ERR_SHAPE;
-      if (decode && (lhs8 || scale_e8m0)) return GMM_ERR_DTYPE;  // the decoding kernel takes bf16 lhs, f32 scales
+      int decode = opt.e4m3_kernel == GMM_E4M3_DECODE ? 1 : 0;
       if (mx) decode = 1;  // per-32 scales are applied as the weights are decoded
       if (!decode) return fp8_kernel(gmmk::kWeightE4M3);
+      log_decoding();
       e = gmmk::launch_scaled(S, true, f32, dev.sms, s);
     } else if (nvfp4) {
+      log_decoding();
       e = gmmk::launch_scaled_nvfp4(S, f32, dev.sms, s);
     } else {
       const int fmt = rhs_dtype == GMM_DTYPE_E5M2   ? gmmk::kWeightE5M2
@@ -458,6 +493,17 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   L.raster = raster > 0 ? raster : 8;
   L.zero_rest = zero_rest;
   L.group_offset_dev = group_offset_dev;
+  L.wait_limit = opt.wait_limit_cycles;
+  L.drop_stage = opt.test_drop_stage;
+  if (log_enabled()) {
+    static const char* kname[] = {"single", "pair", "swap_pair", "swap", "single"};
+    const int id = kind == BF16Kernel::kPair ? 1 : kind == BF16Kernel::kSwapPair ? 2 : kind == BF16Kernel::kSwap ? 3 : 4;
+    std::fprintf(stderr, "libgmm: %s m=%lld k=%lld n=%lld groups=%d local=%d offset=%s layout=%s out=%s kernel=%s "
+                         "raster=%d\n",
+                 entry, (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups,
+                 group_offset_dev ? "device" : "host", transpose_rhs ? "nt" : "nn", dtype_name(out_dtype), kname[id],
+                 L.raster);
+  }
   // Work items (row tiles x n tiles, at most (m/128 + groups) x n/128) must fit in int32.
   const int64_t m_tiles_max = (m + 127) / 128 + num_local_groups;
   if (m_tiles_max * ((n + 127) / 128) > INT32_MAX) return GMM_ERR_SHAPE;
@@ -491,7 +537,7 @@ int gmm_into(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
              size_t workspace_bytes, void* stream) {
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out,
-                  out_dtype, workspace, workspace_bytes, stream, 0, nullptr);
+                  out_dtype, workspace, workspace_bytes, stream, 0, nullptr, nullptr, 0, ExtArgs{}, "gmm_into");
 }
 
 int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* rhs, int rhs_dtype,
@@ -502,7 +548,8 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
   if (group_offset == nullptr) return GMM_ERR_NULL;
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, 0, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype, workspace,
-                  workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset);
+                  workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset, nullptr, 0, ExtArgs{},
+                  "gmm_device_offset");
 }
 
 int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_lhs_blocks, int64_t m, int64_t k,
@@ -510,8 +557,8 @@ int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_l
            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
            const int32_t* group_offset_dev, const void* rhs_scale, int rhs_scale_dtype, int32_t num_quant_blocks,
            const void* rhs_block_scale, int rhs_block_scale_dtype, int32_t block_size, const void* rhs_bias,
-           int bias_dtype, void* out, int out_dtype, int keep_other_rows, void* workspace, size_t workspace_bytes,
-           void* stream) {
+           int bias_dtype, void* out, int out_dtype, int keep_other_rows, const gmm_options* options, void* workspace,
+           size_t workspace_bytes, void* stream) {
   ExtArgs ext;
   ext.lhs_scale = lhs_scale;
   ext.num_lhs_blocks = num_lhs_blocks;
@@ -521,8 +568,8 @@ int gmm_ex(const void* lhs, int lhs_dtype, const float* lhs_scale, int32_t num_l
   ext.block_size = block_size;
   return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                   num_total_groups, group_offset, rhs_scale, num_quant_blocks, rhs_bias, bias_dtype, out, out_dtype,
-                  workspace, workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset_dev, GMM_KERNEL_AUTO, 0,
-                  ext);
+                  workspace, workspace_bytes, stream, keep_other_rows ? 0 : 1, group_offset_dev, options, 0, ext,
+                  "gmm_ex");
 }
 
 int gmm_quantize_e4m3(const void* x, int x_dtype, int64_t m, int64_t k, int64_t group, void* q, float* scale,
@@ -564,10 +611,12 @@ int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   float best = -1.f;
   Candidate chosen{GMM_KERNEL_AUTO, 0};
   for (const Candidate& c : kCandidates) {
+    gmm_options o{};
+    o.bf16_kernel = c.kernel;
     auto run = [&]() {
       return gmm_impl(lhs, lhs_dtype, m, k, rhs, rhs_dtype, num_local_groups, n, transpose_rhs, group_sizes,
                       num_total_groups, group_offset, nullptr, 0, rhs_bias, bias_dtype, out, out_dtype, workspace,
-                      workspace_bytes, stream, 1, nullptr, c.kernel, c.raster);
+                      workspace_bytes, stream, 1, nullptr, &o, c.raster, ExtArgs{}, "gmm_tune");
     };
     status = run();  // warm-up; also validates the arguments
     if (status != GMM_OK) break;
@@ -595,10 +644,12 @@ int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   return GMM_OK;
 }
 
-int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,
-               int64_t n, const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
-               int32_t num_local_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
-               void* stream) {
+int tgmm_ex(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,
+            const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset, int32_t num_local_groups,
+            void* out, int out_dtype, const gmm_options* options, void* workspace, size_t workspace_bytes,
+            void* stream) {
+  const gmm_options opt = options != nullptr ? *options : gmm_options{};
+  if (!options_valid(opt)) return GMM_ERR_SHAPE;
   if (lhs == nullptr || dout == nullptr || group_sizes == nullptr || out == nullptr) return GMM_ERR_NULL;
   if (lhs_dtype != GMM_DTYPE_BF16 || dout_dtype != GMM_DTYPE_BF16) return GMM_ERR_DTYPE;
   if (out_dtype != GMM_DTYPE_BF16 && out_dtype != GMM_DTYPE_F32) return GMM_ERR_DTYPE;
@@ -651,20 +702,28 @@ int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype,
   L.k = int32_t(k);
   L.out = out;
   L.err = static_cast<uint32_t*>(workspace);
-  // One SM per tile by default; GMM_TGMM_KERNEL = pair selects the SM-pair
-  // kernel (256 x 256 tiles; as fast on the 128-expert workload, kept for
+  L.wait_limit = opt.wait_limit_cycles;
+  L.drop_stage = opt.test_drop_stage;
+  // One SM per tile by default; options.tgmm_kernel = GMM_TGMM_PAIR selects the
+  // SM-pair kernel (256 x 256 tiles; as fast on the 128-expert workload, kept for
   // comparison).
-  bool pair = false;
-  if (const char* env = std::getenv("GMM_TGMM_KERNEL")) {
-    if (std::strcmp(env, "pair") == 0)
-      pair = true;
-    else if (std::strcmp(env, "single") != 0 && std::strcmp(env, "auto") != 0 && env[0] != '\0')
-      return GMM_ERR_SHAPE;
-  }
+  const bool pair = opt.tgmm_kernel == GMM_TGMM_PAIR;
+  if (log_enabled())
+    std::fprintf(stderr, "libgmm: tgmm m=%lld k=%lld n=%lld groups=%d local=%d offset=%d out=%s kernel=%s\n",
+                 (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups, group_offset,
+                 dtype_name(out_dtype), pair ? "pair" : "single");
   cudaError_t e = pair ? gmmk::launch_tgmm_2sm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s)
                        : gmmk::launch_tgmm(L, out_dtype == GMM_DTYPE_F32, dev.sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return GMM_OK;
+}
+
+int tgmm_local(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k,
+               int64_t n, const int32_t* group_sizes, int32_t num_total_groups, int32_t group_offset,
+               int32_t num_local_groups, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  return tgmm_ex(lhs, lhs_dtype, dout, dout_dtype, m, k, n, group_sizes, num_total_groups, group_offset,
+                 num_local_groups, out, out_dtype, nullptr, workspace, workspace_bytes, stream);
 }
 
 int tgmm(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, int64_t m, int64_t k, int64_t n,

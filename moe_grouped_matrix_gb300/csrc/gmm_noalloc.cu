@@ -18,7 +18,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/libgmm.h"
 
@@ -28,25 +27,15 @@ namespace {
 // on a device.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[GMM_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_setup_status[kMaxDevices] = {};
-std::once_flag g_setup_once[kMaxDevices];
-
 // The host-side name g_noalloc_scratch is only a stand-in for the symbol, not a
-// device address; the device address comes from cudaGetSymbolAddress, taken
-// once per device with that device current.
+// device address.  The device address of the current device's copy is looked up
+// on every call (a host-side lookup, no allocation), so it stays right after the
+// device's context is destroyed and created again (cudaDeviceReset), which moves
+// the array.
 int scratch_for_current_device(void** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GMM_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return GMM_ERR_ARCH;
-  std::call_once(g_setup_once[dev], [dev] {
-    void* p = nullptr;
-    g_setup_status[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch_ptr[dev] = p;
-  });
-  if (g_setup_status[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return GMM_ERR_CUDA;
-  *ptr = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GMM_ERR_CUDA;
+  *ptr = p;
   return GMM_OK;
 }
 

@@ -22,6 +22,9 @@ struct GemmLaunch {
   int32_t raster;     // n-tiles per L2 super-column
   int32_t zero_rest;                // 1: zero rows outside the local groups; 0: leave them as they are
   const int32_t* group_offset_dev;  // NULL, or a device int32 that replaces group_offset
+  int64_t wait_limit;               // single/pair/swap_pair: 0, or the bound of their pipeline waits (cycles)
+  int32_t drop_stage;               // 0, or s > 0 (test): single: CTA 0 skips its s-th stage's copies;
+                                    // pair, swap_pair: the first pair's second CTA stops before its s-th
 };
 
 cudaError_t launch_gemm_bf16(const GemmLaunch& p, bool nt, bool out_f32, int grid, cudaStream_t stream);
@@ -51,6 +54,8 @@ struct TgmmLaunch {
   int32_t m, n, k;
   void* out;  // [L, k, n]: local group g is group group_offset + g
   uint32_t* err;
+  int64_t wait_limit;  // pair kernel: 0, or the bound of its pipeline waits (cycles)
+  int32_t drop_stage;  // pair kernel: 0, or s > 0: the first pair's second CTA stops before its s-th stage (test)
 };
 
 cudaError_t launch_tgmm(const TgmmLaunch& p, bool out_f32, int grid, cudaStream_t stream);

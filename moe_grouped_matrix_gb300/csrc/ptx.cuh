@@ -60,16 +60,16 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (without waiting further) once the CTA-wide abort flag is set, or
-// after kWaitLimitCycles, in which case it sets the abort flag and records a
-// timeout in the device error word.
+// after `limit` cycles (kWaitLimitCycles unless a test asks for less), in which
+// case it sets the abort flag and records a timeout in the device error word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         uint32_t* err) {
+                                         uint32_t* err, long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1u;
       atomicOr(err, kErrTimeout);
       return false;
@@ -361,12 +361,12 @@ __device__ __forceinline__ uint32_t mbar_test_wait_cluster(uint32_t bar, uint32_
 
 // Bounded spin on mbar_test_wait_cluster.
 __device__ __forceinline__ bool spin_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                 uint32_t* err) {
+                                                 uint32_t* err, long long limit = kWaitLimitCycles) {
   const long long t0 = clock64();
   for (;;) {
     if (mbar_test_wait_cluster(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1u;
       atomicOr(err, kErrTimeout);
       return false;
@@ -376,13 +376,13 @@ __device__ __forceinline__ bool spin_bar_cluster(uint32_t bar, uint32_t parity, 
 
 // Bounded wait for arrivals that come from other CTAs of the cluster.
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                 uint32_t* err) {
+                                                 uint32_t* err, long long limit = kWaitLimitCycles) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1u;
       atomicOr(err, kErrTimeout);
       return false;
@@ -453,6 +453,61 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, 
 // the cluster before its later async-proxy operations.
 __device__ __forceinline__ void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// 4-byte store into the shared memory of a CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Takes `bytes` off the transaction count of this CTA's mbarrier, as if copies of
+// that many bytes had landed.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------------ unwinding a CTA pair
+// In the pair kernels the copies of both CTAs for a pipeline stage complete on
+// the leader's full barrier of that stage, which the leader alone arms (one
+// expect_tx for both CTAs' bytes) and alone can wait on.  When a wait gives up,
+// the two producers may stop at different stages of their common sequence.  The
+// follower reports how many stages it issued (pair_report, at the end of its
+// producer loop, whether or not it gave up).  After the leader's roles have all
+// finished, and only if one of its waits gave up, the leader's producer thread
+// settles the last `kStages` stages of the sequence (pair_drain): a stage the
+// follower issued but the leader never armed gets the expect_tx of the
+// follower's bytes; a stage the leader armed but the follower never issued gets
+// the follower's missing bytes as complete_tx.  Then it waits, bounded, for
+// every one of them to complete, which is when no copy into either CTA's shared
+// memory is in flight any more.  Neither producer runs more than kStages stages
+// ahead of the MMAs, which consumed (and so completed) every earlier stage.  The
+// final cluster barrier keeps the follower from exiting before the drain ends.
+__device__ __forceinline__ void pair_report(uint32_t report_bar, uint32_t report_word, uint32_t issued) {
+  st_shared_cluster_u32(mapa_shared(report_word, 0), issued);
+  mbar_arrive_cluster(mapa_shared(report_bar, 0));  // release: the count is visible first
+}
+
+// `follower_bytes(i)`: the bytes the follower's copies of stage i of the sequence
+// carry (i counts from 0); `armed`: stages the leader armed.
+template <int kStages, class FollowerBytes>
+__device__ __forceinline__ void pair_drain(uint32_t full_bar0, uint32_t report_bar, uint32_t report_word,
+                                           uint32_t armed, long long limit, FollowerBytes follower_bytes) {
+  uint32_t issued = armed;  // without a report, the leader's own count
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(report_bar, 0)) {
+    if (clock64() - t0 > limit) break;
+  }
+  if (mbar_test_wait_cluster(report_bar, 0))
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(issued) : "r"(report_word) : "memory");
+  const uint32_t hi = armed > issued ? armed : issued;
+  for (uint32_t i = hi > uint32_t(kStages) ? hi - kStages : 0u; i < hi; ++i) {
+    const uint32_t bar = full_bar0 + 8u * (i % kStages);
+    if (i >= armed)
+      mbar_arrive_expect_tx(bar, follower_bytes(i));
+    else if (i >= issued)
+      mbar_complete_tx(bar, follower_bytes(i));
+    drain_bar(bar, (i / kStages) & 1u);
+  }
 }
 
 // ------------------------------------------------------------------ misc

@@ -12,7 +12,7 @@
 // a 128 x 256 tile on one SM needs, so the same shared memory holds a 5-deep ring
 // (320 rows in flight per SM instead of 192).  On the 128-expert workload this
 // runs as fast as the one-SM kernel (the output write stream sets both), which
-// stays the default; this one is selected with GMM_TGMM_KERNEL=pair.
+// stays the default; this one is selected per call (gmm_options.tgmm_kernel).
 //
 // A group's last chunk may run into the next group's rows.  Their products must
 // not enter the sum, and zero rows of B (dout) suffice for that whatever A
@@ -66,11 +66,13 @@ constexpr uint32_t OFF_ACCE = OFF_ACCF + 16;
 constexpr uint32_t OFF_DONE = OFF_ACCE + 16;
 constexpr uint32_t OFF_TMEM = OFF_DONE + 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
+constexpr uint32_t OFF_REPORT = OFF_ABORT + 4;  // pair_report's barrier and count (leader's)
+constexpr uint32_t OFF_RWORD = OFF_REPORT + 8;
 constexpr uint32_t OFF_OFFS = OFF_CTRL + 256;
 constexpr uint32_t SMEM_USED = OFF_OFFS + 4 * (kMaxGroups + 4);
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
+static_assert(OFF_RWORD + 4 <= OFF_OFFS && OFF_REPORT % 8 == 0, "control block overlaps the tables");
 
 struct Params {
   const int32_t* group_sizes;
@@ -78,6 +80,8 @@ struct Params {
   int32_t m, n, k;
   void* out;
   uint32_t* err;
+  long long wait_limit;  // bound of every pipeline wait, in clock cycles
+  int32_t drop_stage;    // 0, or s > 0: the first pair's second CTA stops before its s-th stage (test)
 };
 
 // One warp writes its 32 rows x 128 bytes (32 fp32 or 64 bf16 columns) into a
@@ -152,6 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(b), 8);  // one lane of each epilogue warp of both CTAs
     }
     mbar_init(done_bar, 1);
+    mbar_init(sbase + OFF_REPORT, 1);  // the follower's pair_report
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch(&tm_lhs);
@@ -177,6 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // loffs[g] (offsets run over all groups) and it writes out[g].
   const int32_t* loffs = offs + p.group_offset;
 
+  uint32_t issued = 0;  // producer: stages of the pair's sequence this CTA issued (leader: armed)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
@@ -190,7 +196,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t kc = kp * PAIR_M + int32_t(rank) * BM;        // this CTA's lhs columns
         const int32_t nc = nt * BN + int32_t(rank) * (BN / 2);      // this CTA's dout columns
         for (int32_t c = 0; c * BR < rows; ++c) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.err, p.wait_limit)) {
+            ok = false;
+            break;
+          }
+          if (blockIdx.x == 1 && issued + 1 == uint32_t(p.drop_stage)) {
+            // timeout test: the follower stops issuing, so the leader's wait for
+            // this stage's bytes runs out
             ok = false;
             break;
           }
@@ -203,19 +215,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(a_dst + j * BOX_BYTES, &tm_lhs, fb, kc + 64 * j, row);
 #pragma unroll
           for (int j = 0; j < BN / 128; ++j) tma_load_2d_pair(b_dst + j * BOX_BYTES, &tm_dout, fb, nc + 64 * j, row);
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // Copies already issued complete on their own within microseconds;
-        // give them a bounded moment before this CTA unwinds.
-        const long long t0 = clock64();
-        while (clock64() - t0 < kDrainLimitCycles) {
-        }
-      }
+      if (!leader) pair_report(sbase + OFF_REPORT, sbase + OFF_RWORD, issued);
     }
   } else if (warp == 1) {
     if (leader) {
@@ -228,11 +235,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t g = w / per_group;
         const int32_t rows = loffs[g + 1] - loffs[g];
         if (rows == 0) continue;  // the epilogues write zeros; no accumulator is used
-        if (!wait_bar_cluster(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (!wait_bar_cluster(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int32_t c = 0; c * BR < rows; ++c) {
-          if (!wait_bar(full_bar(stage), phase, abort_flag, p.err)) {
+          if (!wait_bar(full_bar(stage), phase, abort_flag, p.err, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -317,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      if (!wait_bar(accf_bar(acc), acc_phase, abort_flag, p.err, p.wait_limit)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
@@ -351,7 +358,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the leader's MMAs are done and no signal targets either CTA any more
+  if (leader && warp == 0 && lane == 0 && *abort_flag) {
+    st_shared_cluster_u32(mapa_shared(sbase + OFF_ABORT, 1), 1u);  // the follower's waits end too
+    pair_drain<STAGES>(full_bar(0), sbase + OFF_REPORT, sbase + OFF_RWORD, issued, p.wait_limit,
+                       [](uint32_t) { return STAGE_BYTES; });
+  }
+  cluster_sync();  // the leader's MMAs and every copy are done; no signal targets either CTA any more
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -373,7 +385,8 @@ cudaError_t launch_impl(const TgmmLaunch& L, int max_ctas, cudaStream_t stream) 
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorLaunchOutOfResources;
   const int grid = 2 * (clusters < max_ctas / 2 ? clusters : max_ctas / 2);
-  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.err};
+  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.err,
+           L.wait_limit > 0 ? (long long)L.wait_limit : kWaitLimitCycles, L.drop_stage};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, L.tm_out, p);
   return cudaGetLastError();
 }

@@ -17,6 +17,7 @@ import numpy as np
 import torch
 
 import oracle
+import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300.workloads import stored_bits
 
 REL_MAG = 1e-3
@@ -60,3 +61,11 @@ def oracle_gmm(lhs, rhs, group_sizes_np, *, transpose_rhs=True, group_offset=0, 
 
 def oracle_tgmm(lhs, dout, group_sizes_np, k_rows=None):
     return oracle.tgmm(bits(lhs), bits(dout), group_sizes_np, k_rows=k_rows)
+
+
+def use_options(monkeypatch, **kw):
+    """Kernel choices (gmm_options fields, e.g. bf16_kernel="pair", act_split="kernel") for the
+    library calls of the rest of the test; undone when the test ends."""
+    current = dict(getattr(G._defaults, "kw", {}))
+    current.update(kw)
+    monkeypatch.setattr(G._defaults, "kw", current, raising=False)

@@ -31,7 +31,8 @@ def test_header_declares_the_expected_calls():
     assert declared_functions() == sorted(
         ["gmm", "tgmm", "gmm_workspace_bytes", "gmm_read_device_errors", "gmm_status_string", "gmm_last_cuda_error",
          "gmm_noalloc", "gmm_into", "tgmm_local", "gmm_device_offset", "gmm_tuning_set", "gmm_tuning_get",
-         "gmm_tuning_clear", "gmm_tuning_save", "gmm_tuning_load", "gmm_tune", "gmm_quantize_e4m3", "gmm_ex"])
+         "gmm_tuning_clear", "gmm_tuning_save", "gmm_tuning_load", "gmm_tune", "gmm_quantize_e4m3", "gmm_ex",
+         "tgmm_ex", "gmm_get_device_error", "gmm_workspace_bytes_for"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -42,8 +43,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert lib.gmm_status_string(0) == b"ok"
-    for code in range(1, 10):
+    for code in range(1, 12):
         assert lib.gmm_status_string(code) != b"unknown status"
+    assert lib.gmm_status_string(12) == b"unknown status"
     # the error flags (256 bytes, the smallest workspace a call accepts), then scratch
     assert lib.gmm_workspace_bytes() > 256 and lib.gmm_workspace_bytes() % 256 == 0
 
@@ -80,7 +82,8 @@ def test_gmm_host_validation(lib, fn, over, status):
 def call_gmm_ex(lib, **over):
     a = dict(lhs=FAKE, lhs_dtype=2, lscale=FAKE, nlb=2, m=256, k=256, rhs=FAKE, rhs_dtype=2, L=4, n=256, trhs=1,
              gs=FAKE, G=4, go=0, godev=None, scale=FAKE, scale_dtype=8, nb=2, bscale=None, bscale_dtype=8, bsize=0,
-             bias=None, bias_dtype=0, out=FAKE, out_dtype=0, keep=0, ws=FAKE, ws_bytes=256, stream=None)
+             bias=None, bias_dtype=0, out=FAKE, out_dtype=0, keep=0, options=None, ws=FAKE, ws_bytes=256,
+             stream=None)
     a.update(over)
     return lib.gmm_ex(*a.values())
 
@@ -110,6 +113,52 @@ def test_gmm_ex_host_validation(lib, over, status):
     assert call_gmm_ex(lib, **over) == status
 
 
+def opts(**kw):
+    return ctypes.byref(G._make_options(**kw))
+
+
+def test_options_layout():
+    # gmm_options: four int32 choices, an int64 wait bound, the drop-stage test hook, a reserved word
+    assert ctypes.sizeof(G.GmmOptions) == 32
+    assert G.GmmOptions.wait_limit_cycles.offset == 16 and G.GmmOptions.test_drop_stage.offset == 24
+
+
+@pytest.mark.parametrize("over", [
+    dict(bf16_kernel=5), dict(bf16_kernel=-1), dict(e4m3_kernel=3), dict(act_split=3), dict(tgmm_kernel=3),
+    dict(wait_limit_cycles=-5), dict(test_drop_stage=-1)])
+def test_bad_options_are_rejected(lib, over):
+    # checked before anything else reads the (fake) pointers: GMM_ERR_SHAPE
+    assert call_gmm_ex(lib, lhs_dtype=0, lscale=None, rhs_dtype=0, scale=None, nb=0, options=opts(**over)) == 3
+    bad = G._make_options()
+    bad.reserved = 1
+    assert call_gmm_ex(lib, lhs_dtype=0, lscale=None, rhs_dtype=0, scale=None, nb=0, options=ctypes.byref(bad)) == 3
+
+
+def test_options_reach_the_checks(lib):
+    # the e4m3 decoding kernel takes neither e4m3 activations nor E8M0 scales (GMM_ERR_DTYPE)
+    assert call_gmm_ex(lib, options=opts(e4m3_kernel="decode")) == 2
+    # the split pass is requested but the workspace (256 bytes) cannot hold it: GMM_ERR_WORKSPACE,
+    # unless the device check comes first (GMM_ERR_ARCH / GMM_ERR_CUDA on a machine without a GB300)
+    st = call_gmm_ex(lib, lhs_dtype=0, lscale=None, scale_dtype=1, options=opts(act_split="pass"))
+    assert st in (6, 7, 8)
+
+
+def test_workspace_bytes_for(lib):
+    f = lib.gmm_workspace_bytes_for
+    assert f(256, 4096, 2048, 64, 64, G.DTYPE_BF16, G.DTYPE_BF16) == 256          # bf16 weights: flags only
+    assert f(256, 4096, 2048, 64, 64, G.DTYPE_E4M3, G.DTYPE_E4M3) == 256          # e4m3 activations
+    # bf16 activations, e4m3 weights: 4 m k bytes of split terms, then (s1, s2) per 256-wide step
+    assert f(256, 4096, 2048, 64, 64, G.DTYPE_BF16, G.DTYPE_E4M3) == 256 + 4 * 256 * 4096 + 8 * 256 * 16
+    # int8 weights split in 128-wide steps; rows whose terms end off a 256-byte boundary
+    assert f(3, 640, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_INT8) == 256 + 7680 + 8 * 3 * 5
+    assert f(-1, 128, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_E4M3) == 0
+    assert f(256, 4096, 2048, 64, 64, G.DTYPE_BF16, G.DTYPE_E4M3) > lib.gmm_workspace_bytes() // 8
+
+
+def test_device_error_needs_a_workspace(lib):
+    assert lib.gmm_get_device_error(None, None) == 1
+
+
 def test_quantize_host_validation(lib):
     q = lambda **o: lib.gmm_quantize_e4m3(o.get("x", FAKE), o.get("xd", 0), o.get("m", 4), o.get("k", 256),
                                           o.get("group", 128), o.get("q", FAKE), o.get("s", FAKE), None)
@@ -130,6 +179,12 @@ def test_tgmm_host_validation(lib):
     assert t(G=0) == 3
     assert t(out=ctypes.c_void_p((1 << 20) + 2)) == 4
     assert t(wb=0) == 6
+
+
+def test_tgmm_ex_options(lib):
+    t = lambda o: lib.tgmm_ex(FAKE, 0, FAKE, 0, 64, 128, 256, FAKE, 8, 2, 4, FAKE, 1, o, FAKE, 256, None)
+    assert t(opts(tgmm_kernel=3)) == 3
+    assert t(opts(bf16_kernel=7)) == 3
 
 
 def test_tgmm_local_host_validation(lib):

@@ -1,6 +1,6 @@
 """bf16 activations with 8- and 4-bit weights: the two-level e4m3 split of each
 activation row, made once per row by a pass into the workspace (the default with a full
-workspace) or inside the fp8 kernel for every weight tile (GMM_FP8_ACT_SPLIT=kernel, or a
+workspace) or inside the fp8 kernel for every weight tile (options act_split="kernel", or a
 workspace of the minimum size).  Both feed the same operand rows and scales to the same MMAs
 and fold, so their outputs must be the same bits.  They must also match the fp64 oracle,
 with groups whose rows span two chunks, a ragged last k step, an n tail, a group_offset
@@ -14,7 +14,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import ORACLE_FORMAT, bits, check_close
+from parity import ORACLE_FORMAT, bits, check_close, use_options
 from split_statement import split_statement
 
 pytestmark = pytest.mark.gpu
@@ -42,15 +42,15 @@ def _inputs(fmt, m, k, n, L, nb, seed):
 
 def _both(monkeypatch, call):
     """The call's output with the split pass and with the in-kernel split."""
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    use_options(monkeypatch, act_split="pass")
     pre = call()
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    use_options(monkeypatch, act_split="kernel")
     inside = call()
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
-    monkeypatch.delenv("GMM_FP8_ACT_SPLIT")
+    use_options(monkeypatch, act_split="auto")
     return pre, inside
 
 
@@ -123,7 +123,7 @@ def test_minimum_workspace_splits_inside(monkeypatch):
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0 and G.read_device_errors(workspace=small) == 0
     _same_bits(full, minimal)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    use_options(monkeypatch, act_split="pass")
     with pytest.raises(G.GmmError):
         G.gmm(lhs, rhs, gs, rhs_scale=scale, workspace=small)
 
@@ -135,12 +135,12 @@ def test_activations_beyond_the_scratch_split_inside(monkeypatch):
     lhs, rhs, scale, _, _ = _inputs("e4m3", m, k, n, 3, 32, 120)
     gs = torch.tensor(sizes, device=DEV)
     auto = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    use_options(monkeypatch, act_split="kernel")
     inside = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
     _same_bits(auto, inside)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    use_options(monkeypatch, act_split="pass")
     with pytest.raises(G.GmmError):
         G.gmm(lhs, rhs, gs, rhs_scale=scale)
     rows = np.array([0, 999, 1000, 2303])
@@ -180,13 +180,13 @@ def test_scratch_boundary(m, fits, monkeypatch):
     sizes = np.array([m // 2, 0, m - m // 2], np.int32)
     lhs, rhs, scale, _, _ = _inputs("e4m3", m, k, n, 3, 16, 150)
     gs = torch.tensor(sizes, device=DEV)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "pre")
+    use_options(monkeypatch, act_split="pass")
     if not fits:
         with pytest.raises(G.GmmError):
             G.gmm(lhs, rhs, gs, rhs_scale=scale)
         return
     pre = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "kernel")
+    use_options(monkeypatch, act_split="kernel")
     inside = G.gmm(lhs, rhs, gs, rhs_scale=scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
@@ -284,6 +284,6 @@ def test_split_rows_equal_a_host_statement_of_the_split(fmt, step):
 
 def test_unknown_setting_is_rejected(monkeypatch):
     lhs, rhs, scale, _, _ = _inputs("e4m3", 16, 256, 128, 1, 1, 130)
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", "sometimes")
+    use_options(monkeypatch, act_split=5)
     with pytest.raises(G.GmmError):
         G.gmm(lhs, rhs, torch.tensor([16], dtype=torch.int32, device=DEV), rhs_scale=scale)

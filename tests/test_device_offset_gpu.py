@@ -11,7 +11,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import check_close, oracle_gmm
+from parity import check_close, oracle_gmm, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -39,7 +39,7 @@ SIZES = [60, 0, 130, 7, 200, 33, 90]  # 7 groups, sum 520
 @pytest.mark.parametrize("kernel", BF16_KERNELS)
 @pytest.mark.parametrize("go,L", [(0, 3), (2, 4), (4, 3)])
 def test_bf16_device_offset_equals_host_offset(kernel, go, L, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", kernel)
+    use_options(monkeypatch, bf16_kernel=kernel)
     m, k, n = 560, 192, 264
     lhs = W.normal((m, k), 1.0, 1, DEV)
     rhs = W.normal((L, n, k), 0.05, 2, DEV)
@@ -90,7 +90,7 @@ def test_out_of_range_device_offset_is_flagged_and_writes_nothing(kernel, bad, m
     if kernel == "fp8":
         rhs = W.weights("e4m3", (L, n, k), 11, DEV)
     else:
-        monkeypatch.setenv("GMM_BF16_KERNEL", kernel)
+        use_options(monkeypatch, bf16_kernel=kernel)
         rhs = W.normal((L, n, k), 0.05, 11, DEV)
     out = torch.full((m, n), 7.0, dtype=torch.bfloat16, device=DEV)
     G.gmm(lhs, rhs, _gs(SIZES), group_offset=_dev_offset(bad), out=out)

@@ -14,7 +14,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import bits, check_close, oracle_gmm, oracle_tgmm
+from parity import bits, check_close, oracle_gmm, oracle_tgmm, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -55,8 +55,8 @@ KERNELS = ["single", "pair", "swap", "swap_pair"]
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    """Runs the test once per bf16 forward kernel (GMM_BF16_KERNEL override)."""
-    monkeypatch.setenv("GMM_BF16_KERNEL", request.param)
+    """Runs the test once per bf16 forward kernel (options.bf16_kernel)."""
+    use_options(monkeypatch, bf16_kernel=request.param)
     return request.param
 
 
@@ -161,8 +161,8 @@ def test_stream_ordering_on_side_stream():
 # ------------------------------------------------------------------------ tgmm
 @pytest.fixture(params=["pair", "single"])
 def tgmm_kernel(request, monkeypatch):
-    """Runs the test on the one-SM tgmm kernel (default) and the SM-pair kernel (GMM_TGMM_KERNEL)."""
-    monkeypatch.setenv("GMM_TGMM_KERNEL", request.param)
+    """Runs the test on the one-SM tgmm kernel (default) and the SM-pair kernel (options.tgmm_kernel)."""
+    use_options(monkeypatch, tgmm_kernel=request.param)
     return request.param
 
 
@@ -210,7 +210,7 @@ def test_tgmm_pair_matches_single_sm_kernel(monkeypatch):
     dout = W.normal((520, 136), 1.0, 62, DEV)
     outs = {}
     for kern in ("pair", "single"):
-        monkeypatch.setenv("GMM_TGMM_KERNEL", kern)
+        use_options(monkeypatch, tgmm_kernel=kern)
         outs[kern] = G.tgmm(lhs, dout, _gs(sizes))
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
@@ -223,7 +223,7 @@ def test_tgmm_pair_matches_single_sm_kernel(monkeypatch):
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
 @pytest.mark.parametrize("out_dtype", ODT)
 def test_pair_ragged_tiles_and_tails(transpose_rhs, out_dtype, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
+    use_options(monkeypatch, bf16_kernel="pair")
     # 256-row pair tiles over groups of 300, 0, 513, 1, 400 rows (sum 1214 < m = 1500);
     # k = 200 and n = 520 leave tails in both dimensions.
     _gmm_case(1500, 200, 520, [300, 0, 513, 1, 400], transpose_rhs=transpose_rhs, out_dtype=out_dtype, seed=3)
@@ -231,18 +231,18 @@ def test_pair_ragged_tiles_and_tails(transpose_rhs, out_dtype, monkeypatch):
 
 @pytest.mark.parametrize("go,local", [(0, 3), (2, 3), (5, 1)])
 def test_pair_group_offset_slices(go, local, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
+    use_options(monkeypatch, bf16_kernel="pair")
     _gmm_case(1800, 192, 264, [250, 0, 333, 700, 7, 300], group_offset=go, local=local, seed=10 + go)
 
 
 def test_pair_bias_and_single_group(monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
+    use_options(monkeypatch, bf16_kernel="pair")
     _gmm_case(1024, 256, 520, [1024], bias_dtype=torch.bfloat16, out_dtype=torch.float32, seed=17)
 
 
 @pytest.mark.parametrize("transpose_rhs", LAYOUTS)
 def test_pair_integer_inputs_bit_exact(transpose_rhs, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", "pair")
+    use_options(monkeypatch, bf16_kernel="pair")
     m, k, n = 1100, 256, 264
     sizes = np.array([257, 0, 255, 400, 1], np.int32)
     lhs = W.integer_valued((m, k), -8, 8, 13, DEV)
@@ -265,14 +265,14 @@ def test_three_kernels_agree_on_the_same_problem(monkeypatch):
     ref, mag = oracle_gmm(lhs, w, sizes)
     outs = {}
     for kern in KERNELS:
-        monkeypatch.setenv("GMM_BF16_KERNEL", kern)
+        use_options(monkeypatch, bf16_kernel=kern)
         outs[kern] = G.gmm(lhs, w, _gs(sizes), out_dtype=torch.float32)
         check_close(outs[kern], ref, mag, kern)
     assert torch.equal(outs["pair"], outs["single"])
 
 
-def test_unknown_kernel_override_is_rejected(monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", "fastest")
+def test_unknown_kernel_choice_is_rejected(monkeypatch):
+    use_options(monkeypatch, bf16_kernel=9)
     lhs = W.normal((64, 64), 1.0, 1, DEV)
     w = W.normal((1, 64, 64), 0.05, 2, DEV)
     with pytest.raises(G.GmmError):

@@ -17,7 +17,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import check_close, oracle_gmm, oracle_tgmm
+from parity import check_close, oracle_gmm, oracle_tgmm, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,7 +59,7 @@ def _check_into(out, before, ref, mag, mask, what):
 @pytest.mark.parametrize("transpose_rhs", [True, False], ids=["NT", "NN"])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16out", "f32out"])
 def test_gmm_into_keeps_rows_outside_the_slice(kernel, transpose_rhs, out_dtype, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", kernel)
+    use_options(monkeypatch, bf16_kernel=kernel)
     # 7 groups, slice [2, 5) holds an empty group and a one-row group; sum 603 < m = 650.
     m, k, n = 650, 136, 264
     sizes = np.array([100, 37, 0, 1, 250, 120, 95], np.int32)
@@ -80,7 +80,7 @@ def test_gmm_into_keeps_rows_outside_the_slice(kernel, transpose_rhs, out_dtype,
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_two_shards_into_one_buffer_make_the_full_product(kernel, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", kernel)
+    use_options(monkeypatch, bf16_kernel=kernel)
     m, k, n = 520, 128, 256
     sizes = np.array([90, 0, 130, 64, 1, 200], np.int32)  # sum 485 < m
     rhs_all = W.normal((6, n, k), 0.05, 22, DEV)

@@ -10,7 +10,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import check_close
+from parity import check_close, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -89,7 +89,7 @@ def test_unit_block_scales_equal_the_plain_decoding_kernel(monkeypatch):
     sizes = torch.tensor([30, 0, 50, 40], dtype=torch.int32, device=DEV)
     ones = torch.full((L, n, k // 32), 127, dtype=torch.uint8, device=DEV)
     with_mx = G.gmm(lhs, rhs, sizes, rhs_block_scale=ones, out_dtype=torch.float32)
-    monkeypatch.setenv("GMM_E4M3_KERNEL", "decode")
+    use_options(monkeypatch, e4m3_kernel="decode")
     plain = G.gmm(lhs, rhs, sizes, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(with_mx, plain)

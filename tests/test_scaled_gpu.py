@@ -10,7 +10,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import bits, check_close, oracle_gmm
+from parity import bits, check_close, oracle_gmm, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -23,11 +23,11 @@ def library():
     oracle.build()
 
 
-@pytest.fixture(autouse=True, params=["mma", "decode"])
+@pytest.fixture(autouse=True, params=["tensor", "decode"])
 def e4m3_kernel(request, monkeypatch):
     """Every test runs on both e4m3 kernels: the e4m3 tensor-core kernel (default) and the
-    kernel that decodes the weights to bf16 (GMM_E4M3_KERNEL=decode)."""
-    monkeypatch.setenv("GMM_E4M3_KERNEL", request.param)
+    kernel that decodes the weights to bf16 (options.e4m3_kernel = "decode")."""
+    use_options(monkeypatch, e4m3_kernel=request.param)
     return request.param
 
 

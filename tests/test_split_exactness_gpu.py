@@ -7,8 +7,8 @@ so every product is exact and only the fp32 sums round; x * inf is +-inf, 0 * in
 
 The hard rows put a large value on weights that are zero and small values on live weights, so
 that mag (the sum of |x w s|) is made of the small values alone while the large one sets the
-row's scale.  Both ways of splitting the rows run: the split pass (GMM_FP8_ACT_SPLIT=pre) and
-the split inside the kernel (GMM_FP8_ACT_SPLIT=kernel)."""
+row's scale.  Both ways of splitting the rows run: the split pass (options act_split="pass") and
+the split inside the kernel (act_split="kernel")."""
 
 import numpy as np
 import pytest
@@ -18,7 +18,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import ORACLE_FORMAT, bits, check_close
+from parity import ORACLE_FORMAT, bits, check_close, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -32,9 +32,9 @@ def library():
     oracle.build()
 
 
-@pytest.fixture(params=["pre", "kernel"])
+@pytest.fixture(params=["pass", "kernel"])
 def split(request, monkeypatch):
-    monkeypatch.setenv("GMM_FP8_ACT_SPLIT", request.param)
+    use_options(monkeypatch, act_split=request.param)
     return request.param
 
 
@@ -189,3 +189,23 @@ def test_fp8_decode_workload_with_wide_rows(split):
     check_close(out[torch.from_numpy(rows).to(DEV)], ref, mag, f"decode workload, hard rows, split={split}")
     keep = [r for r in range(256) if r % 16 != 0]
     assert torch.equal(out[keep], plain[keep])
+
+
+def test_infinite_e5m2_weights(split):
+    """Reading on infinite e5m2 weights: the split's terms can be zero (0 * inf = NaN), so a
+    column that meets an infinite weight comes out +-inf or NaN where the definition gives
+    +-inf; every other column is within the bound."""
+    m, k, n = 12, 512, 128
+    lhs = W.normal((m, k), 1.0, 310, DEV)
+    codes = W.weights("e5m2", (1, n, k), 311, DEV).view(torch.uint8).clone()
+    touched = [3, 40, 77, 100]
+    for j, c in enumerate(touched):
+        codes[0, c, 17 * (j + 1)] = 0x7C if j % 2 == 0 else 0xFC  # +inf, -inf
+    rhs = codes.view(torch.float8_e5m2)
+    scale = W.uniform((1, 2, 1, n), 1.0, 2.0, 312, DEV)
+    out, ref, mag = _run(lhs, rhs, "e5m2", np.array([m], np.int32), scale)
+    assert np.isinf(ref[:, touched]).all()
+    o = out.cpu()
+    assert not torch.isfinite(o[:, touched]).any()
+    rest = [c for c in range(n) if c not in touched]
+    check_close(o[:, rest], ref[:, rest], mag[:, rest], f"e5m2 split={split}: columns without infinities")

@@ -1,6 +1,6 @@
 """The tiling table on the GPU: gmm_tune times every bf16 kernel choice and records the fastest;
 gmm then runs that choice (its output equals the forced kernel's bit for bit); a table entry
-replaces the built-in rule; GMM_BF16_KERNEL still overrides both."""
+replaces the built-in rule; a per-call bf16_kernel option still overrides both."""
 
 import numpy as np
 import pytest
@@ -25,8 +25,7 @@ def library():
 
 
 @pytest.fixture(autouse=True)
-def clean_table(monkeypatch):
-    monkeypatch.delenv("GMM_BF16_KERNEL", raising=False)
+def clean_table():
     G.tuning_clear()
     yield
     G.tuning_clear()
@@ -40,11 +39,8 @@ def _problem(seed=0):
     return lhs, rhs, sizes, torch.tensor(sizes, dtype=torch.int32, device=DEV)
 
 
-def _forced(lhs, rhs, gs, name, monkeypatch):
-    monkeypatch.setenv("GMM_BF16_KERNEL", name)
-    out = G.gmm(lhs, rhs, gs, out_dtype=torch.float32)
-    monkeypatch.delenv("GMM_BF16_KERNEL")
-    return out
+def _forced(lhs, rhs, gs, name):
+    return G.gmm(lhs, rhs, gs, out_dtype=torch.float32, options={"bf16_kernel": name})
 
 
 def test_tune_records_the_fastest_choice_and_gmm_uses_it(monkeypatch):
@@ -56,7 +52,7 @@ def test_tune_records_the_fastest_choice_and_gmm_uses_it(monkeypatch):
     out = G.gmm(lhs, rhs, gs, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
-    assert torch.equal(out, _forced(lhs, rhs, gs, NAMES[kernel], monkeypatch))
+    assert torch.equal(out, _forced(lhs, rhs, gs, NAMES[kernel]))
     ref, mag = oracle_gmm(lhs, rhs, sizes)
     check_close(out, ref, mag, f"tuned choice {NAMES[kernel]} raster {raster}")
 
@@ -67,15 +63,12 @@ def test_table_entry_replaces_the_rule(kernel, monkeypatch):
     rows = G.tuning_rows_log2(lhs.shape[0], sizes.size)
     G.tuning_set(rows, lhs.shape[1], rhs.shape[1], sizes.size, True, torch.float32, kernel, 16)
     out = G.gmm(lhs, rhs, gs, out_dtype=torch.float32)
-    assert torch.equal(out, _forced(lhs, rhs, gs, NAMES[kernel], monkeypatch))
-    # the environment override wins over the entry
+    assert torch.equal(out, _forced(lhs, rhs, gs, NAMES[kernel]))
+    # a per-call choice wins over the entry
     other = G.KERNEL_SINGLE if kernel != G.KERNEL_SINGLE else G.KERNEL_SWAP
-    assert torch.equal(_forced(lhs, rhs, gs, NAMES[other], monkeypatch),
-                       _forced(lhs, rhs, gs, NAMES[other], monkeypatch))
-    monkeypatch.setenv("GMM_BF16_KERNEL", NAMES[other])
-    with_env = G.gmm(lhs, rhs, gs, out_dtype=torch.float32)
-    monkeypatch.delenv("GMM_BF16_KERNEL")
-    assert torch.equal(with_env, _forced(lhs, rhs, gs, NAMES[other], monkeypatch))
+    with G.options(bf16_kernel=NAMES[other]):
+        with_option = G.gmm(lhs, rhs, gs, out_dtype=torch.float32)
+    assert torch.equal(with_option, _forced(lhs, rhs, gs, NAMES[other]))
     ref, mag = oracle_gmm(lhs, rhs, sizes)
     check_close(out, ref, mag, f"table entry {NAMES[kernel]}")
 

@@ -3,10 +3,12 @@ device memory belongs to another component's allocator, or cudaMalloc is not all
 their path).  It runs the gmm kernels with a scratch array compiled into the library in
 place of a caller-supplied workspace.
 
-Called here through the C ABI (ctypes), twice in a row on different inputs; each result
-must agree with gmm() (which uses its own workspace) within the bound the other parity
-tests use, |a - b| <= 1e-3 * mag + 2^-8 * |b|, with mag from the oracle.  This file is
-collected last so that a run stopping at the first failure has run every other test."""
+Called here through the C ABI (ctypes), three times in a row on different inputs; each result
+must match the fp64 oracle within the bound the other parity tests use,
+|gpu - ref| <= 1e-3 * mag + 2^-8 * |ref|, and agree with gmm() (which uses its own workspace)
+within the same bound.  The third call has activation rows whose split marks them, so the
+fp8 kernel's last CTA recomputes them through the counters kept in the library's array.  This
+file is collected last so that a run stopping at the first failure has run every other test."""
 
 import numpy as np
 import pytest
@@ -16,7 +18,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import REL_MAG, REL_REF, oracle_gmm
+from parity import REL_MAG, REL_REF, check_close, oracle_gmm
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -60,15 +62,34 @@ def test_noalloc_matches_gmm_on_two_calls_in_a_row():
     bias2 = W.normal((3, 1, 256), 1.0, 66, DEV)
     gs2 = torch.tensor(sizes2, device=DEV)
 
+    # call 3: e4m3 weights, rows holding three magnitudes 2^22 apart (1.0, 3 * 2^-22, 2^-44):
+    # the two split levels hold only two, so the rows are marked and summed again
+    sizes3 = np.array([20, 44], np.int32)
+    lhs3 = W.normal((64, 512), 1.0, 67, DEV)
+    lhs3[::5] = 3 * 2.0 ** -22
+    lhs3[::5, ::64] = 1.0
+    lhs3[::5, 1::64] = 2.0 ** -44
+    rhs3 = W.e4m3_normal((2, 256, 512), 68, DEV)
+    scale3 = W.uniform((2, 2, 1, 256), 0.5 / 448, 2.0 / 448, 69, DEV)
+    gs3 = torch.tensor(sizes3, device=DEV)
+
     out1 = _noalloc(lhs1, rhs1, gs1, torch.full((700, 520), float("nan"), dtype=torch.bfloat16, device=DEV))
     out2 = _noalloc(lhs2, rhs2, gs2, torch.full((64, 256), float("nan"), dtype=torch.bfloat16, device=DEV),
                     scale=scale2, bias=bias2, group_offset=2)
+    out3 = _noalloc(lhs3, rhs3, gs3, torch.full((64, 256), float("nan"), dtype=torch.bfloat16, device=DEV),
+                    scale=scale3)
     torch.cuda.synchronize()
 
     ref1 = G.gmm(lhs1, rhs1, gs1)
     ref2 = G.gmm(lhs2, rhs2, gs2, rhs_scale=scale2, rhs_bias=bias2, group_offset=2)
+    ref3 = G.gmm(lhs3, rhs3, gs3, rhs_scale=scale3)
     torch.cuda.synchronize()
-    _, mag1 = oracle_gmm(lhs1, rhs1, sizes1)
-    _, mag2 = oracle_gmm(lhs2, rhs2, sizes2, group_offset=2, rhs_scale=scale2, rhs_bias=bias2)
+    oref1, mag1 = oracle_gmm(lhs1, rhs1, sizes1)
+    oref2, mag2 = oracle_gmm(lhs2, rhs2, sizes2, group_offset=2, rhs_scale=scale2, rhs_bias=bias2)
+    oref3, mag3 = oracle_gmm(lhs3, rhs3, sizes3, rhs_scale=scale3)
+    check_close(out1, oref1, mag1, "noalloc bf16 weights")
+    check_close(out2, oref2, mag2, "noalloc e4m3 weights, scales, bias, offset")
+    check_close(out3, oref3, mag3, "noalloc e4m3 weights, marked rows")
     _agree(out1, ref1, mag1)
     _agree(out2, ref2, mag2)
+    _agree(out3, ref3, mag3)
