@@ -134,7 +134,11 @@ struct Cfg {
   // words that are non-zero when some row of the chunk has a second level in
   // the step (one per split warp; with split activations only the first);
   // one scale per sub-tile and row with e4m3 activations
-  static constexpr int SC_PER = kSplit ? 2 * BT + 4 : QPS * BT;
+  static constexpr int SC_TOK = kSplit ? 2 * BT + 4 : QPS * BT;
+  // then the weight scales of the step's (at most two) quant blocks for the
+  // item's 128 columns, as stored (f32, or E8M0 bytes), one 512-byte row per
+  // block: the epilogue reads them from here, not from DRAM
+  static constexpr int SC_PER = SC_TOK + 2 * BMW;
   static constexpr int SLOT_COLS = QPS * SUB_COLS;  // sub-tile h: [slot * SLOT_COLS + 64 h, + N)
   // One barrier per step records that the step's MMAs have completed (a single
   // tcgen05.commit): it frees the step's A stage (raw for e4m3 / e5m2,
@@ -760,6 +764,33 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
            wait_bar(stepdone_bar((j - depth) % NDONE), ((j - depth) / NDONE) & 1u, abort_flag, p.err);
   };
 
+  // The weight scales of step ks of item t, into scale slot sc: one row per
+  // quant block the step touches (at most two), the item's 128 columns as
+  // stored.  Bulk copies completing on the slot's full barrier; returns their
+  // bytes, which the caller's arrive expects.  Rows whose pitch is not a
+  // multiple of 16 bytes (E8M0 with n % 16 != 0) are loaded by this warp
+  // instead (0 bytes).
+  auto load_weight_scales = [&](uint32_t sc, const GemmTile& t, int32_t ks) -> uint32_t {
+    if (p.scale == nullptr) return 0u;
+    const int esz = p.scale_e8m0 ? 1 : 4;
+    const int32_t b0 = ks * QPS / q_per_block, b1 = min(nb - 1, (ks * QPS + halves(ks) - 1) / q_per_block);
+    const int32_t cols = min(BMW, p.n - t.n_tile * BMW);
+    const uint32_t dst = smem_u32(tscale + sc * C::SC_PER + C::SC_TOK);
+    const uint8_t* src = static_cast<const uint8_t*>(p.scale) +
+                         ((int64_t(t.local_group) * nb + b0) * p.n + int64_t(t.n_tile) * BMW) * esz;
+    if ((p.n * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(p.scale) % 16 == 0) {
+      const uint32_t bytes = uint32_t(cols * esz + 15) & ~15u;
+      if (lane == 0)
+        for (int32_t b = b0; b <= b1; ++b)
+          bulk_load(dst + uint32_t(b - b0) * 512u, src + int64_t(b - b0) * p.n * esz, bytes, sfull_bar(sc));
+      return uint32_t(b1 - b0 + 1) * bytes;
+    }
+    uint8_t* d8 = reinterpret_cast<uint8_t*>(tscale + sc * C::SC_PER + C::SC_TOK);
+    for (int32_t b = b0; b <= b1; ++b)
+      for (int c = lane; c < cols * esz; c += 32) d8[(b - b0) * 512 + c] = __ldg(src + int64_t(b - b0) * p.n * esz + c);
+    return 0u;
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -921,29 +952,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     uint32_t slot = 0, sph = 0, sc = 0, scph = 0;
     bool ok = true;
-    // Weight scales are first-touch DRAM reads: fetched kPre blocks ahead.  The
-    // fold loop is unrolled kPre times; with split activations, whose fold has
-    // the second level's branch, 4 measured faster than 8 (less code to fetch).
-    constexpr int kPre = C::kSplit ? 4 : 8;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
       const int32_t col = t.n_tile * BMW + wrow;
       const bool col_ok = col < p.n;
-      const int64_t sidx = int64_t(t.local_group) * nb * p.n + col;  // scale of block 0 for this column
-      // Prefetched as stored (f32 bits or an E8M0 byte), widened only when used, so
-      // that no instruction waits for the loads before then.
-      auto load_scales = [&](int32_t b0, uint32_t (&dst)[kPre]) {
-#pragma unroll
-        for (int j = 0; j < kPre; ++j) {
-          dst[j] = p.scale_e8m0 ? 127u : 0x3F800000u;  // 1
-          if (p.scale != nullptr && col_ok && b0 + j < nb) {
-            const int64_t i = sidx + int64_t(b0 + j) * p.n;
-            dst[j] = p.scale_e8m0 ? uint32_t(__ldg(static_cast<const uint8_t*>(p.scale) + i))
-                                  : __float_as_uint(__ldg(static_cast<const float*>(p.scale) + i));
-          }
-        }
-      };
-      auto widen = [&](uint32_t v) { return p.scale_e8m0 ? e8m0_value(v) : __uint_as_float(v); };
       float bias = 0.f;
       if (p.bias != nullptr && col_ok) {
         const int64_t bi = int64_t(t.local_group) * p.n + col;
@@ -955,80 +967,73 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
         float acc[T8];
 #pragma unroll
         for (int i = 0; i < T8; ++i) acc[i] = 0.f;
-        uint32_t s_cur[kPre], s_next[kPre];
-        load_scales(0, s_cur);
-        int32_t q = 0;
-        for (int32_t c0 = 0; c0 < nb && ok; c0 += kPre) {
-          load_scales(c0 + kPre, s_next);
+        for (int32_t q = 0; q < nq && ok; ++q) {
+          const int h = q % QPS;
+          if (h == 0) {
+            if (!wait_bar(stepdone_bar(slot), sph, abort_flag, p.err) ||
+                !wait_bar(sfull_bar(sc), scph, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          // the weight scale of the sub-tile's block for this column, staged with
+          // the step's token scales (row 0: the step's first block)
+          const int srow = q / q_per_block - (q - h) / q_per_block;
+          const uint8_t* wsc = reinterpret_cast<const uint8_t*>(tscale + sc * C::SC_PER + C::SC_TOK) + srow * 512;
+          const float sw = p.scale == nullptr ? 1.f
+                           : p.scale_e8m0   ? e8m0_value(wsc[wrow])
+                                            : reinterpret_cast<const float*>(wsc)[wrow];
+          const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * SUB_COLS;
+          if constexpr (!C::kSplit) {
+            // one e4m3 product per token: its T8 columns, times the sub-tile's token scale
+            const float* ts = tscale + sc * C::SC_PER + h * C::BT;
+            float d[T8];
+            tmem_ld_cols<T8>(col0, d);
 #pragma unroll
-          for (int bi = 0; bi < kPre; ++bi) {
-            if (c0 + bi >= nb || !ok) break;
-            const float sw = widen(s_cur[bi]);
-            for (int32_t qq = 0; qq < q_per_block; ++qq) {
-              const int h = q % QPS;
-              if (h == 0) {
-                if (!wait_bar(stepdone_bar(slot), sph, abort_flag, p.err) ||
-                    !wait_bar(sfull_bar(sc), scph, abort_flag, p.err)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-              const uint32_t col0 = tmem_base + lane_base + slot * C::SLOT_COLS + uint32_t(h) * SUB_COLS;
-              if constexpr (!C::kSplit) {
-                // one e4m3 product per token: its T8 columns, times the sub-tile's token scale
-                const float* ts = tscale + sc * C::SC_PER + h * C::BT;
-                float d[T8];
-                tmem_ld_cols<T8>(col0, d);
+            for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
+          } else {
+            // Chunk row 8 b + i has its h, l, h2, l2 products in columns 32 b + i,
+            // + 8, + 16, + 24.  The h2 and l2 columns are read only in steps where
+            // some row of the chunk has a second level (s2 != 0).
+            const float2* ts = reinterpret_cast<const float2*>(tscale + sc * C::SC_PER);
+            const uint4 lv2 = *reinterpret_cast<const uint4*>(tscale + sc * C::SC_PER + 2 * C::BT);
+            const bool two = (lv2.x | lv2.y | lv2.z | lv2.w) != 0u;
 #pragma unroll
-                for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
-              } else {
-                // Chunk row 8 b + i has its h, l, h2, l2 products in columns 32 b + i,
-                // + 8, + 16, + 24.  The h2 and l2 columns are read only in steps where
-                // some row of the chunk has a second level (s2 != 0).
-                const float2* ts = reinterpret_cast<const float2*>(tscale + sc * C::SC_PER);
-                const uint4 lv2 = *reinterpret_cast<const uint4*>(tscale + sc * C::SC_PER + 2 * C::BT);
-                const bool two = (lv2.x | lv2.y | lv2.z | lv2.w) != 0u;
+            for (int b = 0; b < T8 / 8; ++b) {
+              float d[16];
+              tmem_ld_cols<16>(col0 + 32 * b, d);
 #pragma unroll
-                for (int b = 0; b < T8 / 8; ++b) {
-                  float d[16];
-                  tmem_ld_cols<16>(col0 + 32 * b, d);
+              for (int i = 0; i < 8; ++i)
+                acc[8 * b + i] = fmaf(sw * ts[8 * b + i].x, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
+              if (two) {
+                tmem_ld_cols<16>(col0 + 32 * b + 16, d);
 #pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    acc[8 * b + i] = fmaf(sw * ts[8 * b + i].x, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
-                  if (two) {
-                    tmem_ld_cols<16>(col0 + 32 * b + 16, d);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                      // a row without a second level keeps its sum (its h2 / l2 products
-                      // are with zero codes, NaN against an infinite weight)
-                      const float s2 = ts[8 * b + i].y;
-                      if (s2 != 0.f) acc[8 * b + i] = fmaf(sw * s2, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
-                    }
-                  }
-                }
-              }
-              ++q;
-              if (h == QPS - 1 || q == nq) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                  mbar_arrive(acce_bar(slot));
-                  mbar_arrive(sempty_bar(sc));
-                }
-                if (++slot == NACC) {
-                  slot = 0;
-                  sph ^= 1u;
-                }
-                if (++sc == NSC) {
-                  sc = 0;
-                  scph ^= 1u;
+                for (int i = 0; i < 8; ++i) {
+                  // a row without a second level keeps its sum (its h2 / l2 products
+                  // are with zero codes, NaN against an infinite weight)
+                  const float s2 = ts[8 * b + i].y;
+                  if (s2 != 0.f) acc[8 * b + i] = fmaf(sw * s2, fmaf(d[8 + i], 0.0625f, d[i]), acc[8 * b + i]);
                 }
               }
             }
           }
-#pragma unroll
-          for (int j = 0; j < kPre; ++j) s_cur[j] = s_next[j];
+          if (h == QPS - 1 || q + 1 == nq) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(acce_bar(slot));
+              mbar_arrive(sempty_bar(sc));
+            }
+            if (++slot == NACC) {
+              slot = 0;
+              sph ^= 1u;
+            }
+            if (++sc == NSC) {
+              sc = 0;
+              scph ^= 1u;
+            }
+          }
         }
         if (!ok || !col_ok) return;
 #pragma unroll
@@ -1076,6 +1081,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     const int32_t nlb = p.lhs_scale != nullptr ? p.num_lhs_blocks : 1;
     const int32_t q_per_lblock = nq / nlb;  // (k / nlb) % 128 == 0 on this path
     uint32_t sc = 0, scph = 0;
+    uint32_t wpend = 0, wpar = 0;  // slots with weight-scale copies issued, and their phases
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
@@ -1106,14 +1112,23 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
             tscale[sc * C::SC_PER + idx] = v;
           }
         }
+        const uint32_t wbytes = load_weight_scales(sc, t, ks);
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfull_bar(sc));
+        if (lane == 0) mbar_arrive_expect_tx(sfull_bar(sc), wbytes);
+        if (wbytes != 0u) {
+          wpend |= 1u << sc;
+          wpar = (wpar & ~(1u << sc)) | (scph << sc);
+        }
         if (++sc == NSC) {
           sc = 0;
           scph ^= 1u;
         }
       }
     }
+    // a wait gave up: the weight-scale copies still in flight land before exit
+    if (!ok && lane == 0)
+      for (int s2 = 0; s2 < NSC; ++s2)
+        if (wpend >> s2 & 1u) drain_bar(sfull_bar(s2), wpar >> s2 & 1u);
   } else if (!kA8 && warp < 10) {
     // ---------------------------------------------------------------- token split
     // The 128 threads share a step's T8 rows evenly: 128 / T8 adjacent lanes per
@@ -1126,6 +1141,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
     // R % 8 = r % 8.
     const int ct = int(threadIdx.x) - 192;
     uint32_t rs = 0, rph = 0, bs = 0, sc = 0, scph = 0;
+    uint32_t wpend = 0, wpar = 0;  // warp 6: slots with weight-scale copies issued, and their phases
     uint32_t j = 0;  // steps split so far
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -1193,6 +1209,8 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
             // a marked row: the last CTA sums it again (see fix_marked_rows)
             if (live && (__float_as_uint(s2) >> 31)) atomicOr(p.err + 1, 1u);
           }
+          // warp 6 brings the step's weight scales (its arrive expects their bytes)
+          const uint32_t wbytes = warp == 6 ? load_weight_scales(sc, t, ks) : 0u;
           // this warp's rows: any second level in the step (read by the epilogue)
           const bool two = __any_sync(0xffffffffu, seg == 0 && live && __float_as_uint(s2) != 0u);
           if (lane == 0)
@@ -1201,7 +1219,11 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(bfull_bar(bs));
-            mbar_arrive(sfull_bar(sc));
+            mbar_arrive_expect_tx(sfull_bar(sc), wbytes);
+          }
+          if (wbytes != 0u) {
+            wpend |= 1u << sc;
+            wpar = (wpar & ~(1u << sc)) | (scph << sc);
           }
           if (++rs == C::RTS) {
             rs = 0;
@@ -1220,6 +1242,10 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
       else
         run(std::integral_constant<int, 16>{});
     }
+    // a wait gave up: the weight-scale copies still in flight land before exit
+    if (!ok && warp == 6 && lane == 0)
+      for (int s2 = 0; s2 < NSC; ++s2)
+        if (wpend >> s2 & 1u) drain_bar(sfull_bar(s2), wpar >> s2 & 1u);
   } else if constexpr (C::kConv) {
     // ---------------------------------------------------------------- weight rewrite
     // Thread t rewrites part t / 128 (of kRowParts) of weight row r = t % 128 of

@@ -42,6 +42,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to this CTA's shared memory; their arrival completes as transactions on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // try_wait suspends the calling thread until the phase completes or about
 // kSuspendHintNs have passed, so waiting warps do not spin on issue slots.
 constexpr uint32_t kSuspendHintNs = 20000;
