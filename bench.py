@@ -48,10 +48,12 @@ def load_peaks():
 
 
 def kernel_hash() -> str:
-    """Hash of the headline kernel's source and the headers it includes."""
+    """Hash of the headline kernel's source, the headers it includes and the host code that
+    picks its tile order."""
     h = hashlib.sha256()
     for path in (KERNEL_SRC, os.path.join(os.path.dirname(KERNEL_SRC), "ptx.cuh"),
-                 os.path.join(os.path.dirname(KERNEL_SRC), "worklist.cuh")):
+                 os.path.join(os.path.dirname(KERNEL_SRC), "worklist.cuh"),
+                 os.path.join(os.path.dirname(KERNEL_SRC), "gmm_api.cu")):
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

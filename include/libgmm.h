@@ -451,8 +451,13 @@ int gmm_quantize_e4m3(const void* x, int x_dtype, int64_t m, int64_t k, int64_t 
  */
 /* (The kernel ids are the GMM_KERNEL_* values above.) */
 
-/* Sets the entry of one problem class.  raster: 0 (default, 8) or 1..64 n tiles
- * per super-column (used by PAIR and SINGLE).  GMM_ERR_SHAPE for invalid values. */
+/* Sets the entry of one problem class.  raster (used by PAIR and SINGLE; the
+ * order in which their output tiles are visited): 0, the default; 1..64 n tiles
+ * per super-column, m tiles of all groups outer and the super-column's n tiles
+ * inner; or -64..-1: group by group, in blocks of up to -raster m tiles, each
+ * block meeting the n tiles in turn with its m tiles inner.  GMM_ERR_SHAPE for
+ * invalid values.  The default is -16 for PAIR and -32 for SINGLE (blocks of
+ * 4096 rows). */
 int gmm_tuning_set(int32_t rows_log2, int64_t k, int64_t n, int32_t num_total_groups, int transpose_rhs,
                    int out_dtype, int kernel, int raster);
 
@@ -472,8 +477,8 @@ int gmm_tuning_save(const char* path);
 int gmm_tuning_load(const char* path);
 
 /*
- * Times every bf16 kernel choice (PAIR with rasters 4, 8 and 16, SWAP_PAIR, SWAP,
- * SINGLE with raster 8) on this problem, with the caller's buffers (`out` is
+ * Times every bf16 kernel choice (PAIR with rasters -16, -4 and 8, SWAP_PAIR, SWAP,
+ * SINGLE with raster -32) on this problem, with the caller's buffers (`out` is
  * written), `iterations` launches each after one warm-up launch, using CUDA events
  * on `stream`, which it synchronises.  Records the fastest in the table and returns
  * it in *kernel, *raster and its mean time in *ms.  Arguments as gmm(); bf16

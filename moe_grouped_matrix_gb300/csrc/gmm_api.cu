@@ -490,7 +490,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
   L.bias = rhs_bias;
   L.bias_f32 = bias_dtype == GMM_DTYPE_F32 ? 1 : 0;
   L.err = err;
-  L.raster = raster > 0 ? raster : 8;
+  // Default tile order: group by group, blocks of 4096 rows (16 pair tiles, 32
+  // one-SM tiles) meeting the n tiles in turn, so that every weight tile and
+  // every lhs row block comes from DRAM once (on the Mixtral up-projection the
+  // pair kernel's DRAM reads drop from 1.74x to 1.03x the algorithmic bytes).
+  L.raster = raster != 0 ? raster : (kind == BF16Kernel::kPair ? -16 : -32);
   L.zero_rest = zero_rest;
   L.group_offset_dev = group_offset_dev;
   L.wait_limit = opt.wait_limit_cycles;
@@ -597,8 +601,8 @@ int gmm_tune(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     int kernel;
     int32_t raster;
   };
-  static const Candidate kCandidates[] = {{GMM_KERNEL_PAIR, 4},      {GMM_KERNEL_PAIR, 8}, {GMM_KERNEL_PAIR, 16},
-                                          {GMM_KERNEL_SWAP_PAIR, 0}, {GMM_KERNEL_SWAP, 0}, {GMM_KERNEL_SINGLE, 8}};
+  static const Candidate kCandidates[] = {{GMM_KERNEL_PAIR, -16},    {GMM_KERNEL_PAIR, -4}, {GMM_KERNEL_PAIR, 8},
+                                          {GMM_KERNEL_SWAP_PAIR, 0}, {GMM_KERNEL_SWAP, 0},  {GMM_KERNEL_SINGLE, -32}};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaEvent_t t0 = nullptr, t1 = nullptr;
   cudaError_t e = cudaEventCreate(&t0);

@@ -7,7 +7,9 @@
 // 0.13.2.dev20251230", gmm.py: "If tiling is callable, look up the problem
 // dimensions in the LUT").  Here the tiles of each kernel are fixed; what varies
 // per problem is which of the four bf16 kernels runs and, for the row-tile
-// kernels, how many n tiles share a super-column of the L2 raster.  m changes
+// kernels, the order of their tiles (how many n tiles share a super-column of
+// the L2 raster, or, negative, how many m tiles of a group form a block that
+// meets every n tile in turn).  m changes
 // with routing, so the table keys on floor(log2(m / num_total_groups)), the
 // average rows per group, next to k, n, the group count, the layout and the
 // output dtype.
@@ -71,7 +73,7 @@ void tuning_store(int32_t rows_log2, int64_t k, int64_t n, int32_t groups, int32
 }
 
 bool tuning_valid(int32_t kernel, int32_t raster) {
-  return kernel >= GMM_KERNEL_PAIR && kernel <= GMM_KERNEL_SINGLE && raster >= 0 && raster <= 64;
+  return kernel >= GMM_KERNEL_PAIR && kernel <= GMM_KERNEL_SINGLE && raster >= -64 && raster <= 64;
 }
 
 }  // namespace gmmk

@@ -113,13 +113,33 @@ struct GemmTile {
   int32_t n_tile;
 };
 
-// Work item w -> tile.  Items are ordered in super-columns of `raster` n-tiles:
-// within a super-column, m-tiles (across all groups, in row order) are outer
-// and its n-tiles inner, so CTAs running at the same time share the same few
-// weight tiles and lhs row blocks in L2.
+// Work item w -> tile.  With raster > 0 items are ordered in super-columns of
+// `raster` n-tiles: within a super-column, m-tiles (across all groups, in row
+// order) are outer and its n-tiles inner, so CTAs running at the same time
+// share the same few weight tiles and lhs row blocks in L2.  With raster < 0
+// they go group by group, each group in blocks of up to -raster of its m-tiles,
+// and within a block the n-tiles outer and the m-tiles inner: the CTAs running
+// at the same time read each weight tile once between them, and the block's
+// lhs rows stay in L2 while every weight tile of the group passes (each lhs
+// row block is read once per block, not once per super-column).
 __device__ __forceinline__ GemmTile decode_gemm_tile(int32_t w, int32_t m_tiles, int32_t n_tiles, int32_t raster,
                                                      const int32_t* tiles, const int32_t* offs, int32_t first,
                                                      int32_t local, int32_t bm) {
+  if (raster < 0) {
+    GemmTile t;
+    t.local_group = find_group(tiles, local, int32_t(w / n_tiles));  // tiles[g] * n_tiles <= w
+    const int32_t g0 = tiles[t.local_group], mt_g = tiles[t.local_group + 1] - g0;
+    const int32_t r = w - g0 * n_tiles;                              // item within the group
+    const int32_t blk = -raster;
+    const int32_t b0 = (r / (blk * n_tiles)) * blk;                  // first m-tile of r's block
+    const int32_t width = min(blk, mt_g - b0);
+    const int32_t rb = r - b0 * n_tiles;
+    t.n_tile = rb / width;
+    const int32_t mt = g0 + b0 + (rb - t.n_tile * width);
+    t.row0 = offs[first + t.local_group] + (mt - g0) * bm;
+    t.row_end = offs[first + t.local_group + 1];
+    return t;
+  }
   const int64_t per_col = int64_t(m_tiles) * raster;
   const int32_t sc = int32_t(w / per_col);
   const int32_t n0 = sc * raster;

@@ -207,23 +207,27 @@ def test_tiling_table_set_get_save_load(lib, tmp_path):
     assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_AUTO, 0)
     G.tuning_set(7, 4096, 28672, 8, True, torch.bfloat16, G.KERNEL_SINGLE, 16)
     G.tuning_set(3, 2048, 2048, 128, False, torch.float32, G.KERNEL_SWAP)
+    G.tuning_set(9, 1024, 2048, 16, True, torch.bfloat16, G.KERNEL_PAIR, -8)  # group-major blocks of 8 m tiles
     assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_SINGLE, 16)
+    assert G.tuning_get(9, 1024, 2048, 16, True, torch.bfloat16) == (G.KERNEL_PAIR, -8)
     assert G.tuning_get(7, 4096, 28672, 8, False, torch.bfloat16) == (G.KERNEL_AUTO, 0)
     path = tmp_path / "table.txt"
     G.tuning_save(str(path))
     lines = path.read_text().splitlines()
     assert lines[0] == "# libgmm tiling table 1"
-    assert sorted(lines[1:]) == sorted(["7 4096 28672 8 1 0 4 16", "3 2048 2048 128 0 1 3 0"])
+    assert sorted(lines[1:]) == sorted(["7 4096 28672 8 1 0 4 16", "3 2048 2048 128 0 1 3 0", "9 1024 2048 16 1 0 1 -8"])
     G.tuning_clear()
     assert G.tuning_get(3, 2048, 2048, 128, False, torch.float32) == (G.KERNEL_AUTO, 0)
     G.tuning_load(str(path))
     assert G.tuning_get(3, 2048, 2048, 128, False, torch.float32) == (G.KERNEL_SWAP, 0)
     assert G.tuning_get(7, 4096, 28672, 8, True, torch.bfloat16) == (G.KERNEL_SINGLE, 16)
+    assert G.tuning_get(9, 1024, 2048, 16, True, torch.bfloat16) == (G.KERNEL_PAIR, -8)
     G.tuning_clear()
 
 
 @pytest.mark.parametrize("body", ["7 4096 28672 8 1 0 9 0\n", "7 4096 28672 8 1 0 1\n", "7 4096 x 8 1 0 1 0\n",
-                                  "7 4096 28672 8 1 0 1 65\n", "7 4096 28672 8 1 0 1 0 extra\n"])
+                                  "7 4096 28672 8 1 0 1 65\n", "7 4096 28672 8 1 0 1 -65\n",
+                                  "7 4096 28672 8 1 0 1 0 extra\n"])
 def test_tiling_table_rejects_malformed_files(lib, tmp_path, body):
     G.tuning_clear()
     good = "3 2048 2048 128 0 1 3 0\n"
@@ -240,5 +244,6 @@ def test_tiling_table_rejects_bad_entries(lib):
     assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 0, 0) == 3   # AUTO is not an entry
     assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 5, 0) == 3
     assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 1, 99) == 3
+    assert lib.gmm_tuning_set(7, 4096, 4096, 8, 1, 0, 1, -65) == 3
     assert lib.gmm_tuning_set(-1, 4096, 4096, 8, 1, 0, 1, 0) == 3
     assert G.tuning_rows_log2(16384, 8) == 11 and G.tuning_rows_log2(5, 8) == 0 and G.tuning_rows_log2(32768, 128) == 8
