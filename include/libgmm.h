@@ -91,12 +91,18 @@ enum {
  * Size in bytes of a full workspace (a constant, 16 MiB + 256): the error
  * flags, then scratch for the 8- and 4-bit weight kernels.  With bf16
  * activations, a call of those kernels whose split activations fit the
- * caller's workspace (256 bytes of flags, then 4 m k bytes of e4m3 terms
- * rounded up to 256, then 8 m ceil(k / 256) bytes of step scales, 8 m k / 128
- * for int8 weights) first splits each activation row once there, and the kernel
- * reads the terms instead of splitting every row again for each 128-wide weight
- * tile.  The result is the same, bit for bit.  With a smaller workspace (at
- * least GMM_WORKSPACE_MIN_BYTES) the kernel splits inside.
+ * caller's workspace first splits each activation row once there:
+ *  - e4m3, e5m2, e2m1 and uint4 weights: 256 bytes of flags, then 4 m k bytes of e4m3
+ *    terms rounded up to 256, then 8 m ceil(k / 256) bytes of step scales; the
+ *    fp8 kernel reads the terms instead of splitting every row again for each
+ *    128-wide weight tile, and the result is the same, bit for bit;
+ *  - int8 and int4 weights: 256 bytes of flags, then 2 m k bytes of fp16
+ *    values rounded up to 256, then 8 m k / 128 bytes of (scale, mark) pairs;
+ *    the weights are then rewritten as fp16 and multiplied on the fp16 tensor
+ *    cores.  Both ways give exact products and fp32 sums, but the sums may
+ *    round differently from the in-kernel split's.
+ * With a smaller workspace (at least GMM_WORKSPACE_MIN_BYTES) the fp8 kernel
+ * splits inside (e4m3 terms, for every format).
  */
 size_t gmm_workspace_bytes(void);
 
@@ -104,9 +110,10 @@ size_t gmm_workspace_bytes(void);
  * The workspace size that lets a gmm() / gmm_ex() call of this shape run its
  * fastest way: GMM_WORKSPACE_MIN_BYTES, plus for bf16 activations (lhs_dtype
  * GMM_DTYPE_BF16) with an 8- or 4-bit rhs_dtype the split scratch described above
- * (4 m k bytes rounded up to 256, then 8 m ceil(k / step) bytes, step 256, or 128
- * for int8).  num_total_groups, num_local_groups and n do not change it today; they
- * are taken so that callers size workspaces by the problem.  0 for negative sizes.
+ * (e4m3, e5m2, e2m1, uint4: 4 m k bytes rounded up to 256, then 8 m ceil(k / 256)
+ * bytes; int8, int4: 2 m k bytes rounded up to 256, then 8 m k / 128 bytes).
+ * num_total_groups, num_local_groups and n do not change it today; they are taken
+ * so that callers size workspaces by the problem.  0 for negative sizes.
  */
 size_t gmm_workspace_bytes_for(int64_t m, int64_t k, int64_t n, int32_t num_total_groups, int32_t num_local_groups,
                                int lhs_dtype, int rhs_dtype);
@@ -141,7 +148,9 @@ enum { GMM_TGMM_AUTO = 0, GMM_TGMM_SINGLE = 1, GMM_TGMM_PAIR = 2 };
  *   act_split     8- and 4-bit weights with bf16 activations: GMM_SPLIT_AUTO (split
  *                 each row once by a pass when the workspace holds it, else inside
  *                 the kernel), _PASS (the pass; GMM_ERR_WORKSPACE when the workspace
- *                 cannot hold it) or _KERNEL (inside the kernel).
+ *                 cannot hold it) or _KERNEL (inside the kernel).  With the pass,
+ *                 int8 and int4 weights run on the fp16 tensor cores (an fp16
+ *                 split); inside the kernel every format runs on the fp8 ones.
  *   tgmm_kernel   tgmm_ex(): GMM_TGMM_AUTO / _SINGLE (one SM per 128 x 256 output
  *                 tile) or _PAIR (SM pairs on 256 x 256 tiles).
  *   wait_limit_cycles  0: the default bound of every internal pipeline wait (about

@@ -104,6 +104,27 @@ int make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, int rank,
   return GMM_OK;
 }
 
+// A map with explicit byte strides (strides[i] between consecutive indices of
+// dimension i + 1); dimension 0 is contiguous.
+int make_map_strided(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = strides[i - 1];
+  }
+  CUresult r = fn(map, dt, cuuint32_t(rank), const_cast<void*>(base), gdim, gstride, bdim, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(int(r));
+  return GMM_OK;
+}
+
 // e2m1 weights [L, n, k], two codes per byte (even k in the low nibble), in
 // {128 k, 128 rows} boxes that land in shared memory as 128-byte rows, each 8
 // bytes of codes followed by an 8-byte gap (the 4-bit operand layout of
@@ -196,8 +217,10 @@ size_t gmm_workspace_bytes_for(int64_t m, int64_t k, int64_t n, int32_t num_tota
   if (m < 0 || k < 0) return 0;
   const bool split = lhs_dtype == GMM_DTYPE_BF16 && rhs_dtype >= GMM_DTYPE_E4M3 && rhs_dtype <= GMM_DTYPE_E2M1;
   if (!split) return kWorkspaceMinBytes;
-  const int64_t step = rhs_dtype == GMM_DTYPE_INT8 ? 128 : 256;
-  const size_t scales_at = (kActOffset + size_t(4 * m * k) + 255) & ~size_t(255);
+  // int8 and int4: the fp16 split, 2 m k bytes, then (scale, mark) per 128-wide step
+  const bool intw = rhs_dtype == GMM_DTYPE_INT8 || rhs_dtype == GMM_DTYPE_INT4;
+  const int64_t step = intw ? 128 : 256;
+  const size_t scales_at = (kActOffset + size_t((intw ? 2 : 4) * m * k) + 255) & ~size_t(255);
   return scales_at + size_t(m * ((k + step - 1) / step)) * 2 * sizeof(float);
 }
 
@@ -388,7 +411,46 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     // The fp8 kernels; bf16 activations are split once per row into the
     // workspace when it has room (act_split.cu), in the kernel's k steps.
     auto fp8_kernel = [&](int fmt) -> int {
-      if (!lhs8 && act_split != 0) {
+      // int8 and int4 with bf16 activations: the fp16 split (2 m k bytes of
+      // fp16 values, then (scale, mark) per 128-wide step) and the fp16-MMA
+      // kernel, when the workspace holds the split; else the e4m3 path below.
+      // uint4 stays on the e4m3 path: its code table makes the e4m3 rewrite
+      // cheap, and there the e4m3 kernel measured faster (120 us against 129 us
+      // on the decode workload; int4 131 against 136, int8 124 against 229).
+      const bool intw = fmt == gmmk::kWeightInt8 || fmt == gmmk::kWeightInt4;
+      if (!lhs8 && act_split != 0 && intw) {
+        const int64_t ksteps = k / 128;
+        const size_t scales_at = (kActOffset + size_t(2 * m * k) + 255) & ~size_t(255);
+        const size_t end = scales_at + size_t(m * ksteps) * 2 * sizeof(float);
+        if (end <= workspace_bytes) {
+          uint8_t* plane = static_cast<uint8_t*>(workspace) + kActOffset;
+          float* scales = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + scales_at);
+          // the plane as [k / 64, m, 64]: a {64, 16, 2} box is a step's two
+          // 128-byte swizzled atoms of 16 rows, one after the other
+          const uint64_t dims[3] = {64u, uint64_t(m), uint64_t(k / 64)};
+          const uint64_t strides[2] = {uint64_t(2 * k), 128u};
+          const uint32_t box[3] = {64u, 16u, 2u};
+          if (int st = make_map_strided(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, plane, dims, strides, box,
+                                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return st;
+          S.lhs_split = 1;
+          S.lhs_scale = scales;
+          S.num_lhs_blocks = int32_t(ksteps);
+          if (cudaError_t e1 = gmmk::launch_act_split_f16(lhs, m, k, plane, scales, err + 1,
+                                                          fmt != gmmk::kWeightInt8, s))
+            return cuda_fail(e1);
+          if (log_enabled())
+            std::fprintf(stderr, "libgmm: %s m=%lld k=%lld n=%lld groups=%d local=%d offset=%s lhs=%s rhs=%s out=%s "
+                                 "kernel=f16w split=f16\n",
+                         entry, (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups,
+                         group_offset_dev ? "device" : "host", dtype_name(lhs_dtype), dtype_name(rhs_dtype),
+                         dtype_name(out_dtype));
+          if (cudaError_t e2 = gmmk::launch_f16w(S, fmt, f32, dev.sms, s)) return cuda_fail(e2);
+          return GMM_OK;
+        }
+        if (act_split == 2) return GMM_ERR_WORKSPACE;
+      }
+      if (!lhs8 && act_split != 0 && !intw) {
         const int32_t step = fmt == gmmk::kWeightInt8 ? 128 : 256;
         const int64_t ksteps = (k + step - 1) / step;
         const size_t scales_at = (kActOffset + size_t(4 * m * k) + 255) & ~size_t(255);

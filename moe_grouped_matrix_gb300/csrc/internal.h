@@ -127,6 +127,18 @@ cudaError_t launch_fp8_ps_converted(const ScaledLaunch& p, int weight_format, bo
 // step is marked (act_split.cu).
 cudaError_t launch_act_split(const void* x, int64_t m, int64_t k, int32_t step, void* planes, float* scale,
                              uint32_t* pending, cudaStream_t stream);
+// The fp16 split of bf16 rows [m, k] (k % 128 == 0) for the fp16-MMA kernel of
+// the integer formats: plane [m, k] fp16 (each 8 k in the order 0, 4, 1, 5, 2,
+// 6, 3, 7 when `perm`) and (scale, mark) pairs [m, k / 128, 2]; sets *pending
+// when a step is marked (act_split.cu).
+cudaError_t launch_act_split_f16(const void* x, int64_t m, int64_t k, void* plane, float* scale, uint32_t* pending,
+                                 bool perm, cudaStream_t stream);
+// int8, int4 and uint4 weights on the fp16 tensor cores (gemm_f16w.cu): tm_lhs
+// spans the fp16 split plane [m, k] (box {64, 16}, 128-byte swizzle), lhs_scale
+// its (scale, mark) pairs, num_lhs_blocks = k / 128; tm_rhs the weight bytes
+// (box {128, 128, 1}, 128-byte swizzle).  Launched as the programmatic
+// dependent of the split pass.
+cudaError_t launch_f16w(const ScaledLaunch& p, int weight_format, bool out_f32, int grid, cudaStream_t stream);
 
 // Per-token-group e4m3 quantisation of bf16 activations (quantize.cu); group
 // 64, 128 or 256, k % group == 0.

@@ -93,3 +93,36 @@ def reconstruct(planes, scales, step):
     s2 = np.abs(np.repeat(scales[:, :, 1], step, axis=1)[:, :k].astype(np.float64))
     marked = np.signbit(scales[:, :, 1])
     return s1 * (v[0] + v[1] / 16) + s2 * (v[2] + v[3] / 16), marked
+
+
+F16_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])  # k of each stored position within 8 k (4-bit weights)
+
+
+def split_statement_f16(x_bits, perm):
+    """The fp16 split of the integer-weight kernel (act_split_f16): per row and 128-wide step, with
+    e the exponent field of the largest |x| (at least 15), sc = 2^(e - 141) and the fp16 values
+    rne_f16(x / sc); a step is marked (second scale word -0) when some x is not sc times its fp16
+    value, or it holds an infinity or a NaN.  Returns plane uint16 [m, k] (fp16 bits; each 8 k in
+    the order F16_ORDER when perm) and scales float32 [m, k / 128, 2] (sc, +-0)."""
+    m, k = x_bits.shape
+    ksteps = k // 128
+    xf = (x_bits.astype(np.uint32) << 16).view(np.float32)
+    plane = np.zeros((m, k), np.uint16)
+    scales = np.zeros((m, ksteps, 2), np.float32)
+    for s in range(ksteps):
+        cols = slice(128 * s, 128 * (s + 1))
+        x = xf[:, cols]
+        amax = (x.view(np.uint32) & 0x7FFFFFFF).max(axis=1)
+        e = np.maximum(amax >> 23, 15).astype(np.uint32)
+        sc = ((e - 14) << 23).astype(np.uint32).view(np.float32)
+        inv = ((268 - e) << 23).astype(np.uint32).view(np.float32)
+        with np.errstate(invalid="ignore", over="ignore"):
+            h = (x * inv[:, None]).astype(np.float16)
+            exact = h.astype(np.float32) * sc[:, None] == x
+        marked = ~exact.all(axis=1) | (amax >= 0x7F800000)
+        plane[:, cols] = h.view(np.uint16)
+        scales[:, s, 0] = sc
+        scales[:, s, 1] = np.where(marked, np.float32(-0.0), np.float32(0.0))
+    if perm:
+        plane = plane.reshape(m, k // 8, 8)[:, :, F16_ORDER].reshape(m, k)
+    return plane, scales

@@ -149,8 +149,12 @@ def test_workspace_bytes_for(lib):
     assert f(256, 4096, 2048, 64, 64, G.DTYPE_E4M3, G.DTYPE_E4M3) == 256          # e4m3 activations
     # bf16 activations, e4m3 weights: 4 m k bytes of split terms, then (s1, s2) per 256-wide step
     assert f(256, 4096, 2048, 64, 64, G.DTYPE_BF16, G.DTYPE_E4M3) == 256 + 4 * 256 * 4096 + 8 * 256 * 16
-    # int8 weights split in 128-wide steps; rows whose terms end off a 256-byte boundary
-    assert f(3, 640, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_INT8) == 256 + 7680 + 8 * 3 * 5
+    # int8 / int4 weights: the fp16 split, 2 m k bytes rounded up to 256, then (scale, mark) per
+    # 128-wide step
+    assert f(3, 640, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_INT8) == 256 + 3840 + 8 * 3 * 5
+    assert f(5, 640, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_INT4) == 256 + 6400 + 8 * 5 * 5  # 6656 is 256-aligned
+    # uint4 stays on the e4m3 split: 4 m k bytes, then (s1, s2) per 256-wide step
+    assert f(5, 640, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_UINT4) == 256 + 12800 + 8 * 5 * 3
     assert f(-1, 128, 128, 1, 1, G.DTYPE_BF16, G.DTYPE_E4M3) == 0
     assert f(256, 4096, 2048, 64, 64, G.DTYPE_BF16, G.DTYPE_E4M3) > lib.gmm_workspace_bytes() // 8
 

@@ -15,7 +15,7 @@ import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
 from parity import ORACLE_FORMAT, bits, check_close, use_options
-from split_statement import split_statement
+from split_statement import split_statement, split_statement_f16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -54,6 +54,19 @@ def _both(monkeypatch, call):
     return pre, inside
 
 
+# With bf16 activations the split pass feeds these formats to the fp16-MMA kernel (an fp16
+# split, gemm_f16w.cu), the split inside the kernel to the e4m3 kernel: two exact methods whose
+# fp32 sums may round differently, so both are held to the oracle instead of to each other.
+F16_FORMATS = {"int8", "int4"}
+
+
+def _modes_agree(fmt, pre, inside, ref, mag, what):
+    if fmt in F16_FORMATS:
+        check_close(inside, ref, mag, f"{what}, split inside the kernel")
+    else:
+        _same_bits(pre, inside)
+
+
 def _same_bits(a, b):
     ia = a.view(torch.int16 if a.element_size() == 2 else torch.int32)
     ib = b.view(torch.int16 if b.element_size() == 2 else torch.int32)
@@ -71,10 +84,10 @@ def test_pass_equals_kernel_split_and_oracle(fmt, out_dtype, monkeypatch):
     gs = torch.tensor(SIZES, device=DEV)
     pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias,
                                                    out_dtype=out_dtype, **kw))
-    _same_bits(pre, inside)
     ref, mag = oracle.gmm(bits(lhs), bits(rhs), SIZES, rhs_scale=bits(scale), rhs_bias=bits(bias),
                           rhs_dtype=ORACLE_FORMAT[fmt])
     check_close(pre, ref, mag, f"{fmt} split pass")
+    _modes_agree(fmt, pre, inside, ref, mag, fmt)
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -86,10 +99,10 @@ def test_group_offset_slice_without_scale(fmt, monkeypatch):
     gs = torch.tensor(sizes, device=DEV)
     pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_bias=bias, group_offset=go,
                                                    out_dtype=torch.float32, **kw))
-    _same_bits(pre, inside)
     ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, group_offset=go, rhs_bias=bits(bias),
                           rhs_dtype=ORACLE_FORMAT[fmt])
     check_close(pre, ref, mag, f"{fmt} go={go}")
+    _modes_agree(fmt, pre, inside, ref, mag, f"{fmt} go={go}")
 
 
 def test_wide_range_infinities_and_nan(monkeypatch):
@@ -166,10 +179,10 @@ def test_smallest_shapes(fmt, m, k, monkeypatch):
     gs = torch.tensor(sizes, device=DEV)
     pre, inside = _both(monkeypatch, lambda: G.gmm(lhs, rhs, gs, rhs_scale=scale, rhs_bias=bias,
                                                    out_dtype=torch.float32, **kw))
-    _same_bits(pre, inside)
     ref, mag = oracle.gmm(bits(lhs), bits(rhs), sizes, rhs_scale=bits(scale), rhs_bias=bits(bias),
                           rhs_dtype=ORACLE_FORMAT[fmt])
     check_close(pre, ref, mag, f"{fmt} m={m} k={k}")
+    _modes_agree(fmt, pre, inside, ref, mag, f"{fmt} m={m} k={k}")
 
 
 @pytest.mark.parametrize("m,fits", [(2032, True), (2040, False)])
@@ -249,7 +262,26 @@ def test_captured_graph_replays_with_new_activations(fmt):
         _same_bits(out, ref)
 
 
-@pytest.mark.parametrize("fmt,step", [("e4m3", 256), ("int8", 128)])
+def _hard_split_rows(m, k):
+    x = W.normal((m, k), 1.0, 190).float()
+    x[1] = 0.0                                                   # a zero row: e clamps
+    x[2] = -0.0                                                  # negative zeros
+    x[3] = x[3] * 1e-30                                          # tiny values
+    x[4] = x[4] * torch.pow(2.0, torch.linspace(-30, 20, k))     # many binades per step
+    x[5, :8] = torch.tensor([128.0, 1.0625, 1.1875, -1.0625, 3.0, 0.0078125, -0.0, 2.0 ** -20])  # ties
+    x[6] = x[6] * 3e4                                            # large values
+    x[7, 1:] = 3 * 2.0 ** -22                                    # one large value, small ones
+    x[7, 0] = x[7, 128] = x[7, 256] = x[7, 384] = x[7, 512] = 1.0
+    x[8] = torch.where(torch.arange(k) % 2 == 0, 1.5 * 2.0 ** -30, 1.25 * 2.0 ** -60)  # marked steps
+    x[8, ::128] = 1.0
+    x[9, ::128] = 1.0                                            # fp16 subnormals: held to 2^-24 sc
+    x[9, 1::128] = 2.0 ** -33
+    x[10, ::128] = 1.0                                           # below fp16's grid: marked
+    x[10, 1::128] = 1.5 * 2.0 ** -40
+    return x.to(torch.bfloat16).to(DEV)
+
+
+@pytest.mark.parametrize("fmt,step", [("e4m3", 256)])
 def test_split_rows_equal_a_host_statement_of_the_split(fmt, step):
     # the pass's h / l / h2 / l2 planes and (s1, s2) step scales, read back from the workspace,
     # bit for bit
@@ -287,3 +319,27 @@ def test_unknown_setting_is_rejected(monkeypatch):
     use_options(monkeypatch, act_split=5)
     with pytest.raises(G.GmmError):
         G.gmm(lhs, rhs, torch.tensor([16], dtype=torch.int32, device=DEV), rhs_scale=scale)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+def test_fp16_split_rows_equal_a_host_statement(fmt):
+    # the integer formats' split pass: fp16 values (each 8 k reordered for 4-bit weights) and
+    # (scale, mark) per 128-wide step, read back from the workspace, bit for bit
+    m, k, n = 37, 640, 128
+    lhs = _hard_split_rows(m, k)
+    rhs = W.weights(fmt, (1, n, k), 191, DEV)
+    kw = {"rhs_format": fmt} if fmt in W.PACKED else {}
+    G.gmm(lhs, rhs, torch.tensor([m], dtype=torch.int32, device=DEV), out_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ws = G.workspace_for(torch.device(DEV))
+    ksteps = k // 128
+    plane = ws[256:256 + 2 * m * k].cpu().numpy().view(np.uint16).reshape(m, k)
+    at = (256 + 2 * m * k + 255) // 256 * 256
+    scales = ws[at:at + 8 * m * ksteps].cpu().numpy().view(np.float32).reshape(m, ksteps, 2)
+    want_plane, want_scales = split_statement_f16(bits(lhs), fmt != "int8")
+    assert np.signbit(want_scales[10, :, 1]).all() and not np.signbit(want_scales[9, :, 1]).any()
+    assert np.signbit(want_scales[8, :, 1]).all() and not np.signbit(want_scales[7, :, 1]).any()
+    bad = np.argwhere(plane != want_plane)
+    assert bad.size == 0, f"{len(bad)} values differ, first at {bad[:3].tolist()}"
+    assert np.array_equal(scales.view(np.uint32), want_scales.view(np.uint32))

@@ -2,7 +2,8 @@
 one item per CTA over a long k (64 or 128 steps), item counts just above the CTA count, ragged
 chunks with quant blocks wider than a step (a step's weight scales from one block, or from two
 when a step straddles a block boundary), and e4m3 activations in 32-row chunks.  Each result is
-checked against the fp64 oracle, and the split pass against the in-kernel split (same bits)."""
+checked against the fp64 oracle, and the split pass against the in-kernel split (same bits where
+both run the e4m3 kernel; int8 runs on the fp16-MMA kernel after the pass)."""
 
 import numpy as np
 import pytest
@@ -61,8 +62,12 @@ def test_edge_shapes_match_the_oracle(fmt, sizes, k, n, nb):
         inside = call()
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
-    assert torch.equal(pre, inside)
     _check(pre, sizes, lhs, rhs, scale, bias, fmt, f"{fmt} sizes={sizes.tolist()} k={k}")
+    if fmt == "int8":
+        # the split pass feeds int8 to the fp16-MMA kernel, the in-kernel split to the e4m3 one
+        _check(inside, sizes, lhs, rhs, scale, bias, fmt, f"{fmt} sizes={sizes.tolist()} k={k}, split inside")
+    else:
+        assert torch.equal(pre, inside)
 
 
 def test_e4m3_activations_in_32_row_chunks():

@@ -170,3 +170,47 @@ def test_zero_and_negative_zero_steps():
     assert (planes[2:, 1] == 0).all()                                   # no second level
     assert (scales[:, :, 0] == np.float32(2.0 ** -126)).all()          # e clamped to 8
     assert (scales[:, :, 1] == 0).all() and not np.signbit(scales[:, :, 1]).any()
+
+
+# ------------------------------------------------------------------ the fp16 split (integer weights)
+def _rows_of_128(bits256):
+    # the 256-wide rows above cut into two 128-wide rows, each led by its step's maximum
+    b = bits256.reshape(-1, 128).copy()
+    b[1::2, 0] = bits256[:, 0]
+    return b
+
+
+@pytest.mark.parametrize("top", [0x3F80, 0x3FFF, 0x4780, 0x0080, 0x0001])  # M = 1, 1.99.., 65536, 2^-126, 2^-133
+def test_fp16_split_range_for_every_smaller_bf16_magnitude(top):
+    # with E = floor(log2 M) (at least -112 through the clamp) x is held exactly when
+    # |x| >= 2^(E-28) (an fp16 normal), and below that exactly when x is a multiple of fp16's
+    # subnormal spacing 2^(E-38); a step holding any other x is marked, and only then
+    from split_statement import split_statement_f16
+    bits = _rows_of_128(_rows_with_every_code_below(top))
+    plane, scales = split_statement_f16(bits, perm=False)
+    x = _values(bits)
+    back = plane.view(np.float16).astype(np.float64) * scales[:, 0:1, 0].astype(np.float64)
+    E = max(int(np.floor(np.log2(_values(np.array([top], np.uint16))[0]))), -112)
+    spacing = 2.0 ** (E - 38)
+    held = (np.abs(x) >= 2.0 ** (E - 28)) | (np.mod(x, spacing) == 0)
+    assert np.array_equal(back == x, held)
+    assert np.array_equal(np.signbit(scales[:, 0, 1]), ~held.all(axis=1))
+
+
+def test_fp16_split_marks_nonfinite_steps_and_orders_four_bit_rows():
+    from split_statement import F16_ORDER, split_statement_f16
+    rng = np.random.default_rng(5)
+    bits = (rng.standard_normal((6, 256)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    bits[2, 7] = 0x7F80   # +inf
+    bits[3, 200] = 0x7FC0  # NaN
+    plane, scales = split_statement_f16(bits, perm=False)
+    permuted, scales_p = split_statement_f16(bits, perm=True)
+    marks = np.signbit(scales[:, :, 1])
+    assert marks[2, 0] and not marks[2, 1] and marks[3, 1] and not marks[3, 0]
+    assert not marks[[0, 1, 4, 5]].any(), "N(0, 1) steps are held whole"
+    assert np.array_equal(scales.view(np.uint32), scales_p.view(np.uint32))
+    assert np.array_equal(permuted.reshape(6, 32, 8), plane.reshape(6, 32, 8)[:, :, F16_ORDER])
+    # unmarked steps give every value back
+    back = plane.view(np.float16).astype(np.float64) * np.repeat(scales[:, :, 0], 128, axis=1)
+    ok = ~np.repeat(marks, 128, axis=1)
+    assert np.array_equal(back[ok], _values(bits)[ok])
