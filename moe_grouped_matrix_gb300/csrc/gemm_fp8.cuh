@@ -155,7 +155,12 @@ struct Cfg {
   // row) with e4m3 activations, whose single token warp leaves room
   static constexpr int kWConvWarps = kConv ? (kA8 ? 8 : 4) : 0;
   static constexpr int kRowParts = kWConvWarps / 4;
-  static constexpr int kThreads = 192 + 32 * (kConvWarps + kWConvWarps);
+  // MMA issuers: warp 1 and the warps from kMma2 on, each taking every
+  // kIssuers-th step (one thread issues a tcgen05.mma only every ~44-80 cycles;
+  // issuers on several warps add up)
+  static constexpr int kIssuers = 2;
+  static constexpr int kMma2 = 6 + kConvWarps + kWConvWarps;
+  static constexpr int kThreads = 32 * (kMma2 + kIssuers - 1);
 
   static constexpr uint32_t OFF_RAW = 0;
   static constexpr uint32_t OFF_CONV = OFF_RAW + RAWST * RAW_BYTES;
@@ -174,7 +179,7 @@ struct Cfg {
   static constexpr uint32_t OFF_SEMPTY = OFF_SFULL + 8 * NSC;
   static constexpr uint32_t OFF_ACCE = OFF_SEMPTY + 8 * NSC;
   static constexpr uint32_t OFF_DONE = OFF_ACCE + 8 * NACC;
-  static constexpr uint32_t OFF_TMEM = OFF_DONE + 8;
+  static constexpr uint32_t OFF_TMEM = OFF_DONE + 8 * kIssuers;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
   static constexpr uint32_t OFF_OFFS = OFF_CTRL + 1024;
   static constexpr uint32_t OFF_TILES = OFF_OFFS + 4 * (kMaxGroups + 4);
@@ -724,7 +729,7 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
       mbar_init(sempty_bar(s), 4);
     }
     for (int s = 0; s < NACC; ++s) mbar_init(acce_bar(s), 4);
-    mbar_init(done_bar, 1);
+    for (int s = 0; s < C::kIssuers; ++s) mbar_init(done_bar + 8 * s, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch(&tm_lhs);
@@ -886,18 +891,25 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           if (rpend >> s & 1u) drain_bar(kA8 ? bfull_bar(s) : rfull_bar(s), rpar[s]);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp >= C::kMma2) {
+    // ---------------------------------------------------------------- MMA issuers
     // Step j accumulates sub-tile h into TMEM columns [SLOT_COLS slot + 64 h,
     // + 2 T8) of slot j % NACC; the epilogue frees the slot after reading it.
-    uint32_t as = 0, aph = 0, bs = 0, bph = 0, slot = 0, sph = 0;
+    // Issuer `mine` takes the steps j with j % kIssuers == mine: each step has
+    // its own A stage, operand stage, slot and commit, so they share nothing.
+    const uint32_t mine = warp == 1 ? 0u : uint32_t(warp - C::kMma2 + 1);
+    constexpr uint32_t kAst = C::kConv ? C::CST : C::RAWST;
     bool ok = true;
+    uint32_t j = 0;  // the step's index over the CTA's items
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
       const int t8 = t8_of(chunk_rows(t));
       // N: the h, l, h2 and l2 rows of the split (4 T8), or the e4m3 token rows (16 or 32).
       const uint32_t idesc = idesc_e4m3(BMW, C::kSplit ? 4 * t8 : max(t8, 16)) | (C::kAType << 7);
-      for (int32_t ks = 0; ks < ksteps; ++ks) {
+      for (int32_t ks = 0; ks < ksteps; ++ks, ++j) {
+        if (j % C::kIssuers != mine) continue;
+        const uint32_t as = j % kAst, aph = (j / kAst) & 1u, bs = j % C::BST, bph = (j / C::BST) & 1u;
+        const uint32_t slot = j % NACC, sph = (j / NACC) & 1u;
         const int32_t hq = halves(ks);
         const uint32_t afull = C::kConv ? convfull_bar(as) : rawfull_bar(as);
         if (!wait_bar(acce_bar(slot), sph ^ 1u, abort_flag, p.err) || !wait_bar(afull, aph, abort_flag, p.err) ||
@@ -923,23 +935,11 @@ __global__ void __launch_bounds__(Cfg<F, kA8, kPS>::kThreads, 1)
           mma_commit(stepdone_bar(slot));
         }
         __syncwarp();
-        if (++as == (C::kConv ? C::CST : C::RAWST)) {
-          as = 0;
-          aph ^= 1u;
-        }
-        if (++bs == C::BST) {
-          bs = 0;
-          bph ^= 1u;
-        }
-        if (++slot == NACC) {
-          slot = 0;
-          sph ^= 1u;
-        }
       }
     }
     if (lane == 0) {
-      mma_commit(done_bar);
-      drain_bar(done_bar, 0);
+      mma_commit(done_bar + 8 * mine);
+      drain_bar(done_bar + 8 * mine, 0);
     }
     __syncwarp();
   } else if (warp < 6) {

@@ -737,20 +737,31 @@ int tgmm_ex(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, in
   // With m == 0 every group is empty and no copy is issued; the maps still
   // need a non-zero extent.
   const uint64_t rows = m > 0 ? uint64_t(m) : 1;
-  {
-    const uint64_t dims[2] = {uint64_t(k), rows};
+  // One SM per tile by default; options.tgmm_kernel = GMM_TGMM_PAIR selects the
+  // SM-pair kernel (256 x 256 tiles; as fast on the 128-expert workload, kept for
+  // comparison).
+  const bool pair = opt.tgmm_kernel == GMM_TGMM_PAIR;
+  // The one-SM kernel reads a chunk's 128 lhs columns and 256 dout columns as one
+  // box each, over the matrices viewed as [features / 64, rows, 64] (the 64-wide
+  // 128-byte swizzle atoms one after the other).  The view needs the feature
+  // count to be a multiple of 64: its last atom would otherwise reach past the
+  // row into the next one (and past the end of the matrix on the last row).
+  auto feature_map = [&](CUtensorMap* map, const void* base, int64_t features, bool view3, uint32_t atoms) {
+    if (view3) {
+      const uint64_t dims[3] = {64u, rows, uint64_t(features / 64)};
+      const uint64_t strides[2] = {uint64_t(2 * features), 128u};
+      const uint32_t box[3] = {64u, 64u, atoms};
+      return make_map_strided(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    const uint64_t dims[2] = {uint64_t(features), rows};
     const uint32_t box[2] = {64, 64};
-    if (int st = make_map(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, lhs, dims, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return st;
-  }
-  {
-    const uint64_t dims[2] = {uint64_t(n), rows};
-    const uint32_t box[2] = {64, 64};
-    if (int st = make_map(&L.tm_dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dout, dims, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return st;
-  }
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, base, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  L.lhs_3d = !pair && k % 64 == 0 ? 1 : 0;
+  L.dout_3d = !pair && n % 64 == 0 ? 1 : 0;
+  if (int st = feature_map(&L.tm_lhs, lhs, k, L.lhs_3d != 0, 2u)) return st;
+  if (int st = feature_map(&L.tm_dout, dout, n, L.dout_3d != 0, 4u)) return st;
   {
     const bool f32 = out_dtype == GMM_DTYPE_F32;
     const uint64_t dims[3] = {uint64_t(n), uint64_t(k), uint64_t(num_local_groups)};
@@ -770,10 +781,6 @@ int tgmm_ex(const void* lhs, int lhs_dtype, const void* dout, int dout_dtype, in
   L.err = static_cast<uint32_t*>(workspace);
   L.wait_limit = opt.wait_limit_cycles;
   L.drop_stage = opt.test_drop_stage;
-  // One SM per tile by default; options.tgmm_kernel = GMM_TGMM_PAIR selects the
-  // SM-pair kernel (256 x 256 tiles; as fast on the 128-expert workload, kept for
-  // comparison).
-  const bool pair = opt.tgmm_kernel == GMM_TGMM_PAIR;
   if (log_enabled())
     std::fprintf(stderr, "libgmm: tgmm m=%lld k=%lld n=%lld groups=%d local=%d offset=%d out=%s kernel=%s\n",
                  (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups, group_offset,

@@ -46,8 +46,8 @@ cudaError_t launch_gemm_bf16_2sm(const GemmLaunch& p, bool nt, bool out_f32, int
 
 // tgmm: out[g] = lhs_g^T dout_g (bf16 operands, fp32 accumulate).
 struct TgmmLaunch {
-  CUtensorMap tm_lhs;   // lhs  [m, k], box {64, 64}
-  CUtensorMap tm_dout;  // dout [m, n], box {64, 64}
+  CUtensorMap tm_lhs;   // lhs  [m, k], box {64, 64}; lhs_3d: [k / 64, m, 64], box {64, 64, 2}
+  CUtensorMap tm_dout;  // dout [m, n], box {64, 64}; dout_3d: [n / 64, m, 64], box {64, 64, 4}
   CUtensorMap tm_out;   // out [L, k, n], box {128 bytes of n, 32, 1}
   const int32_t* group_sizes;  // [num_total_groups]
   int32_t num_total_groups, group_offset, num_local_groups;
@@ -56,6 +56,7 @@ struct TgmmLaunch {
   uint32_t* err;
   int64_t wait_limit;  // pair kernel: 0, or the bound of its pipeline waits (cycles)
   int32_t drop_stage;  // pair kernel: 0, or s > 0: the first pair's second CTA stops before its s-th stage (test)
+  int32_t lhs_3d, dout_3d;  // one-SM kernel: the maps are the 3D views (k % 64 == 0, n % 64 == 0)
 };
 
 cudaError_t launch_tgmm(const TgmmLaunch& p, bool out_f32, int grid, cudaStream_t stream);

@@ -66,6 +66,7 @@ struct Params {
   int32_t m, n, k;
   void* out;
   uint32_t* err;
+  int32_t lhs_3d, dout_3d;  // tm_lhs / tm_dout are the [features / 64, rows, 64] views
 };
 
 // One warp writes its 32 rows x 128 bytes (32 fp32 or 64 bf16 columns) into a
@@ -159,10 +160,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = sbase + OFF_A + stage * A_BYTES;
           const uint32_t b_dst = sbase + OFF_B + stage * B_BYTES;
           const int32_t row = row_begin + c * BR;
+          // one copy per operand where the shapes allow it: a thread's copy
+          // issue, not the bytes, paced this loop with six boxes a chunk
+          if (p.lhs_3d) {
+            tma_load_3d(a_dst, &tm_lhs, fb, 0, row, kt * (BM / 64));
+          } else {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * BOX_BYTES, &tm_lhs, fb, kt * BM + 64 * j, row);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * BOX_BYTES, &tm_lhs, fb, kt * BM + 64 * j, row);
+          }
+          if (p.dout_3d) {
+            tma_load_3d(b_dst, &tm_dout, fb, 0, row, nt * (BN / 64));
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * BOX_BYTES, &tm_dout, fb, nt * BN + 64 * j, row);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * BOX_BYTES, &tm_dout, fb, nt * BN + 64 * j, row);
+          }
           pend_par[stage] = phase;
           pend_mask |= 1u << stage;
           if (++stage == STAGES) {
@@ -335,7 +346,8 @@ cudaError_t launch_impl(const TgmmLaunch& L, int grid, cudaStream_t stream) {
   auto kern = tgmm_kernel<kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.err};
+  Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.out, L.err,
+           L.lhs_3d, L.dout_3d};
   kern<<<grid, kThreads, SMEM_BYTES, stream>>>(L.tm_lhs, L.tm_dout, L.tm_out, p);
   return cudaGetLastError();
 }
