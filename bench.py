@@ -631,6 +631,12 @@ def _ncu_decode_int4(torch, G, W, dev):
                          rhs_format="int4")
 
 
+def _ncu_decode_int8(torch, G, W, dev):
+    fd = W.fp8_decode(dev, fmt="int8")
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
+    return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_scale=fd["rhs_scale"], rhs_bias=fd["rhs_bias"])
+
+
 def _ncu_w8a8_decode(torch, G, W, dev):
     fd = W.fp8_decode(dev)
     gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
@@ -646,7 +652,8 @@ def _ncu_moe128_wi(torch, G, W, dev):
 
 
 NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode,
-             "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4, "w8a8_decode": _ncu_w8a8_decode}
+             "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4, "decode_int8": _ncu_decode_int8,
+             "w8a8_decode": _ncu_w8a8_decode}
 
 
 def run_ncu_case(name):
