@@ -73,9 +73,10 @@ constexpr int CST = 4;
 constexpr uint32_t B_ATOM = BT * 128;      // 16 rows x 64 fp16
 constexpr uint32_t B_BYTES = 2 * B_ATOM;
 constexpr int BST = 8;
-constexpr int NACC = 8;                    // accumulator slots = step-done ring
+constexpr int NACC = 8;                    // accumulator slots
+constexpr int NDONE = 8;                   // step-done barriers: step j commits to j % NDONE
 constexpr int SLOT_COLS = 32;
-constexpr uint32_t A_COL0 = 256;           // the A tiles follow the accumulator slots
+constexpr uint32_t A_COL0 = NACC * SLOT_COLS;  // the A tiles follow the accumulator slots
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NSC = 8;
 constexpr int SC_TOK = BT;                 // the chunk rows' split scales
@@ -99,7 +100,7 @@ constexpr uint32_t OFF_RAWFULL = OFF_CTRL;
 constexpr uint32_t OFF_RAWEMPTY = OFF_RAWFULL + 8 * RAWST;
 constexpr uint32_t OFF_CONVFULL = OFF_RAWEMPTY + 8 * RAWST;
 constexpr uint32_t OFF_DONEB = OFF_CONVFULL + 8 * CST;
-constexpr uint32_t OFF_BFULL = OFF_DONEB + 8 * NACC;
+constexpr uint32_t OFF_BFULL = OFF_DONEB + 8 * NDONE;
 constexpr uint32_t OFF_SFULL = OFF_BFULL + 8 * BST;
 constexpr uint32_t OFF_SEMPTY = OFF_SFULL + 8 * NSC;
 constexpr uint32_t OFF_ACCE = OFF_SEMPTY + 8 * NSC;
@@ -113,7 +114,7 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_B % 1024 == 0 && B_ATOM % 1024 == 0, "swizzle atoms are 1024-byte aligned");
-static_assert(CST <= NACC && BST <= NACC, "step-done ring indexing");
+static_assert(CST <= NDONE && BST <= NDONE && NACC <= NDONE, "step-done ring indexing");
 static_assert(NACC * SLOT_COLS <= int(A_COL0) && A_COL0 + CST * A_COLS <= TMEM_COLS, "TMEM map");
 
 // kind::f16 with fp16 A and B (type code 0), both K-major, f32 D.
@@ -174,6 +175,17 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// A 4-byte asynchronous copy global -> shared, and the arrive on an mbarrier
+// that follows this thread's earlier such copies (the barrier's pending count
+// is raised now and lowered when they land, so the phase waits for them).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 32 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
@@ -220,10 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(rawempty_bar(s), kConvWarps);  // the rewrite warps, after the raw box's last step
     }
     for (int s = 0; s < CST; ++s) mbar_init(convfull_bar(s), kConvWarps);
-    for (int s = 0; s < NACC; ++s) {
-      mbar_init(stepdone_bar(s), 1);
-      mbar_init(acce_bar(s), 4);
-    }
+    for (int s = 0; s < NDONE; ++s) mbar_init(stepdone_bar(s), 1);
+    for (int s = 0; s < NACC; ++s) mbar_init(acce_bar(s), 4);
     for (int s = 0; s < BST; ++s) mbar_init(bfull_bar(s), 1);
     for (int s = 0; s < NSC; ++s) {
       mbar_init(sfull_bar(s), 1);
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Step j's converted / operand stage is reused by step j + depth once step j's MMAs are done.
   auto wait_step_done = [&](uint32_t j, int depth) {
     return j < uint32_t(depth) ||
-           wait_bar(stepdone_bar((j - depth) % NACC), ((j - depth) / NACC) & 1u, abort_flag, p.err);
+           wait_bar(stepdone_bar((j - depth) % NDONE), ((j - depth) / NDONE) & 1u, abort_flag, p.err);
   };
 
   if (warp == 0) {
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t atom = uint32_t(kk >> 2), off = uint32_t(kk & 3) * 32u;
             mma_f16_ts(d, a0 + 8u * kk, sw128_desc(b0 + atom * B_ATOM + off, 16, 1024), kIdesc, kk != 0 ? 1u : 0u);
           }
-          mma_commit(stepdone_bar(slot));
+          mma_commit(stepdone_bar(j % NDONE));
         }
         __syncwarp();
       }
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int wrow = quarter * 32 + lane;  // weight row in the tile = output column
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    uint32_t slot = 0, sph = 0, sc = 0, scph = 0;
+    uint32_t slot = 0, ds = 0, dph = 0, sc = 0, scph = 0;
     bool ok = true;
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const GemmTile t = item_of(w);
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < T8; ++i) acc[i] = 0.f;
         for (int32_t ks = 0; ks < ksteps && ok; ++ks) {
-          if (!wait_bar(stepdone_bar(slot), sph, abort_flag, p.err) || !wait_bar(sfull_bar(sc), scph, abort_flag, p.err)) {
+          if (!wait_bar(stepdone_bar(ds), dph, abort_flag, p.err) || !wait_bar(sfull_bar(sc), scph, abort_flag, p.err)) {
             ok = false;
             break;
           }
@@ -402,9 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(acce_bar(slot));
             mbar_arrive(sempty_bar(sc));
           }
-          if (++slot == NACC) {
-            slot = 0;
-            sph ^= 1u;
+          if (++slot == NACC) slot = 0;
+          if (++ds == NDONE) {
+            ds = 0;
+            dph ^= 1u;
           }
           if (++sc == NSC) {
             sc = 0;
@@ -446,90 +457,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 6 || warp == kScale2) {
     // ---------------------------------------------------------------- scales
     // Per step: the chunk rows' split scales (lhs_scale[row, step, 0]; 0 past
-    // the chunk), and the weight scales of the step's quant block for the
-    // item's 128 columns, as stored (bulk copies completing on the slot's
-    // barrier; E8M0 rows of n % 16 != 0 bytes loaded by this warp).
-    // The split scales are loaded kAhead of the warp's steps before they are
-    // stored, so that a step does not wait for a load.  Warp 6 serves the even
-    // steps, warp kScale2 the odd ones (one warp's address arithmetic, loads
-    // and copy issue took longer than a step).
+    // the chunk), one 4-byte asynchronous copy per row, and the weight scales
+    // of the step's quant block for the item's 128 columns, as stored (a bulk
+    // copy; E8M0 rows of n % 16 != 0 bytes loaded by this warp), all landing on
+    // the slot's full barrier.  The warp waits for no load.  Warp 6 serves the
+    // even steps, warp kScale2 the odd ones.
     griddep_wait();  // the split scales come from the kernel before
     const uint32_t mine = warp == 6 ? 0u : 1u;
     uint32_t wpend = 0, wpar = 0;
     bool ok = true;
     const int esz = p.scale_e8m0 ? 1 : 4;
     const bool bulk = (p.n * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(p.scale) % 16 == 0;
-    // one step forward over the CTA's items
-    auto step_fwd = [&](int32_t& w_, int32_t& ks_, uint32_t& j_, GemmTile& t_) {
-      ++j_;
-      if (++ks_ == ksteps) {
-        ks_ = 0;
-        w_ += gridDim.x;
-        if (w_ < total) t_ = item_of(w_);
-      }
-    };
-    auto own_fwd = [&](int32_t& w_, int32_t& ks_, uint32_t& j_, GemmTile& t_) {
-      step_fwd(w_, ks_, j_, t_);
-      if (w_ < total) step_fwd(w_, ks_, j_, t_);
-    };
-    constexpr int kAhead = 4;
-    float ahead[kAhead];
-    int32_t wl = blockIdx.x, ksl = 0;  // the step whose split scales load next
-    uint32_t jl = 0;
-    GemmTile tl = wl < total ? item_of(wl) : GemmTile{};
-    if (mine == 1u && wl < total) step_fwd(wl, ksl, jl, tl);
-    auto load_next = [&]() {
-      float v = 0.f;
-      if (wl < total) {
-        if (lane < min(chunk_rows(tl), int32_t(BT))) v = __ldg(p.lhs_scale + (int64_t(tl.row0 + lane) * ksteps + ksl) * 2);
-        own_fwd(wl, ksl, jl, tl);
-      }
-      return v;
-    };
-#pragma unroll
-    for (int i = 0; i < kAhead; ++i) ahead[i] = load_next();
-    // The step loop is unrolled kAhead times so that each step reads and
-    // refills its own register: shifting the look-ahead values from one
-    // register to the next would wait for the newest load every step.
     int32_t w = blockIdx.x, ks = 0;
-    uint32_t j = 0;
+    uint32_t j = 0;  // the step's index over the CTA's items
     GemmTile t = w < total ? item_of(w) : GemmTile{};
-    if (mine == 1u && w < total) step_fwd(w, ks, j, t);
-    while (w < total && ok) {
-#pragma unroll
-      for (int i = 0; i < kAhead; ++i) {
-        if (w >= total) break;
-        const uint32_t sc = j % NSC, scph = (j / NSC) & 1u;
-        if (!wait_bar(sempty_bar(sc), scph ^ 1u, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        if (lane < BT) tscale[sc * SC_PER + lane] = ahead[i];  // 0 past the chunk's rows
-        ahead[i] = load_next();
-        uint32_t wbytes = 0;
-        if (p.scale != nullptr) {
-          const int32_t cols = min(BMW, p.n - t.n_tile * BMW);
-          const int32_t b = ks / s_per_block;
-          const uint8_t* src = static_cast<const uint8_t*>(p.scale) +
-                               ((int64_t(t.local_group) * nb + b) * p.n + int64_t(t.n_tile) * BMW) * esz;
-          const uint32_t dst = smem_u32(tscale + sc * SC_PER + SC_TOK);
-          if (bulk) {
-            wbytes = uint32_t(cols * esz);  // a multiple of 16: n % 8 == 0 (f32) or n % 16 == 0 (E8M0)
-            if (lane == 0) bulk_load(dst, src, wbytes, sfull_bar(sc));
-          } else {
-            uint8_t* d8 = reinterpret_cast<uint8_t*>(tscale + sc * SC_PER + SC_TOK);
-            for (int c = lane; c < cols * esz; c += 32) d8[c] = __ldg(src + c);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(sfull_bar(sc), wbytes);
-        if (wbytes != 0u) {
-          wpend |= 1u << sc;
-          wpar = (wpar & ~(1u << sc)) | (scph << sc);
-        }
-        own_fwd(w, ks, j, t);
+    // the item's weight-scale row of the current quant block, and the step's place in that block
+    const int64_t block_pitch = int64_t(p.n) * esz;
+    int64_t wrow = 0;  // byte offset into p.scale
+    int32_t kb = 0;
+    auto item_start = [&]() {
+      wrow = (int64_t(t.local_group) * nb * p.n + int64_t(t.n_tile) * BMW) * esz;
+      kb = 0;
+    };
+    auto step_fwd = [&]() {
+      ++j;
+      if (++kb == s_per_block) {
+        kb = 0;
+        wrow += block_pitch;
       }
+      if (++ks == ksteps) {
+        ks = 0;
+        w += gridDim.x;
+        if (w < total) {
+          t = item_of(w);
+          item_start();
+        }
+      }
+    };
+    if (w < total) item_start();
+    if (mine == 1u && w < total) step_fwd();
+    while (w < total) {
+      const uint32_t sc = j % NSC, scph = (j / NSC) & 1u;
+      if (!wait_bar(sempty_bar(sc), scph ^ 1u, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      if (lane < BT) {
+        if (lane < chunk_rows(t))
+          cp_async_4(smem_u32(tscale + sc * SC_PER + lane), p.lhs_scale + (int64_t(t.row0 + lane) * ksteps + ks) * 2);
+        else
+          tscale[sc * SC_PER + lane] = 0.f;
+      }
+      cp_async_mbar_arrive(sfull_bar(sc));
+      uint32_t wbytes = 0;
+      if (p.scale != nullptr) {
+        const int32_t cols = min(BMW, p.n - t.n_tile * BMW);
+        const uint8_t* src = static_cast<const uint8_t*>(p.scale) + wrow;
+        const uint32_t dst = smem_u32(tscale + sc * SC_PER + SC_TOK);
+        if (bulk) {
+          wbytes = uint32_t(cols * esz);  // a multiple of 16: n % 8 == 0 (f32) or n % 16 == 0 (E8M0)
+          if (lane == 0) bulk_load(dst, src, wbytes, sfull_bar(sc));
+        } else {
+          uint8_t* d8 = reinterpret_cast<uint8_t*>(tscale + sc * SC_PER + SC_TOK);
+          for (int c = lane; c < cols * esz; c += 32) d8[c] = __ldg(src + c);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(sfull_bar(sc), wbytes);
+      if (wbytes != 0u) {
+        wpend |= 1u << sc;
+        wpar = (wpar & ~(1u << sc)) | (scph << sc);
+      }
+      step_fwd();
+      if (w < total) step_fwd();
     }
+    cp_async_wait_all();  // this thread's scale copies have landed
     // a wait gave up: the weight-scale copies still in flight land before exit
     if (!ok && lane == 0)
       for (int s2 = 0; s2 < NSC; ++s2)
