@@ -60,6 +60,9 @@ namespace gmmk {
 namespace f16w {
 namespace {
 
+using fp8::cp_async_4;
+using fp8::cp_async_mbar_arrive;
+using fp8::cp_async_wait_all;
 using fp8::Params;
 using fp8::WFmt;
 
@@ -174,17 +177,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
-// A 4-byte asynchronous copy global -> shared, and the arrive on an mbarrier
-// that follows this thread's earlier such copies (the barrier's pending count
-// is raised now and lowered when they land, so the phase waits for them).
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 32 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&v)[32]) {

@@ -220,6 +220,17 @@ struct Params {
   int64_t w_row_bytes;
 };
 
+// A 4-byte asynchronous copy global -> shared, and the arrive on an mbarrier
+// that follows this thread's earlier such copies (the barrier's pending count
+// is raised now and lowered when they land, so the phase waits for them).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // An E8M0 block scale as fp32 (page "gemm_quant.rs", widen_block_scale_f32):
 // byte e is 2^(e - 127), the bits e << 23, except that 0 is 2^-127 and 255 is 0.
 __device__ __forceinline__ float e8m0_value(uint32_t e) {
