@@ -70,6 +70,8 @@ constexpr int BMW = 128;                   // weight rows (n) per item = MMA M
 constexpr int BT = 16;                     // token rows per item at most = MMA N
 constexpr int KS = 128;                    // k per step
 constexpr uint32_t RAW_BYTES = 128 * 128;  // one raw box
+constexpr uint32_t SCALE_BOX = 16 * 128;   // NVFP4: the box's e4m3 block scales, 16 a weight row (256 k)
+constexpr uint32_t RAW_STAGE = RAW_BYTES + SCALE_BOX;
 constexpr int RAWST = 6;
 constexpr int A_COLS = KS / 2;             // TMEM columns of one A tile (two fp16 per column)
 constexpr int CST = 4;
@@ -96,7 +98,7 @@ constexpr int kIssuers = 4;
 constexpr int kThreads = 32 * (kMma3 + 2);
 
 constexpr uint32_t OFF_RAW = 0;
-constexpr uint32_t OFF_B = OFF_RAW + RAWST * RAW_BYTES;
+constexpr uint32_t OFF_B = OFF_RAW + RAWST * RAW_STAGE;
 constexpr uint32_t OFF_SC = OFF_B + BST * B_BYTES;
 constexpr uint32_t OFF_CTRL = OFF_SC + NSC * SC_PER * 4;
 constexpr uint32_t OFF_RAWFULL = OFF_CTRL;
@@ -116,7 +118,7 @@ constexpr uint32_t SMEM_USED = OFF_TILES + 4 * (kMaxGroups + 4);
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_B % 1024 == 0 && B_ATOM % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+static_assert(OFF_B % 1024 == 0 && B_ATOM % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 static_assert(CST <= NDONE && BST <= NDONE && NACC <= NDONE, "step-done ring indexing");
 static_assert(NACC * SLOT_COLS <= int(A_COL0) && A_COL0 + CST * A_COLS <= TMEM_COLS, "TMEM map");
 
@@ -132,6 +134,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -166,6 +174,23 @@ __device__ __forceinline__ void nib8_to_f16(uint32_t w, uint32_t (&o)[4]) {
   o[3] = hfma2((u8 & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, add);
 }
 
+// NVFP4: eight e2m1 codes (k order from the low nibble) times their block's
+// e4m3 scale -> four fp16x2 words holding k (0, 4), (1, 5), (2, 6), (3, 7), as
+// nib8_to_f16 orders them.  A code's sign and three magnitude bits placed at
+// fp16 bits 15 and 11..9 are the fp16 number 2^-14 times its value (magnitude
+// 1 lands on fp16's subnormal 2^-15 = 0.5 * 2^-14), so times 2^14 it is the
+// value; times the scale (`s2`, the scale in both halves) it stays exact: an
+// e2m1 value times an e4m3 one has at most 6 significant bits, lies within
+// 6 * 448 = 2688 and, being a multiple of 2^-10, on fp16's normal grid.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = w >> (4 * i);  // code i in bits 0..3, code i + 4 in bits 16..19
+    const uint32_t bits = ((v & 0x00070007u) << 9) | ((v & 0x00080008u) << 12);
+    o[i] = hmul2(hmul2(bits, 0x74007400u), s2);  // 2^14, then the block scale
+  }
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulator; A (M = 128)
 // one row per TMEM lane, two fp16 per 32-bit column in k order.
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -193,8 +218,10 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&
 template <WFmt F, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16w_kernel(const __grid_constant__ CUtensorMap tm_lhs, const __grid_constant__ CUtensorMap tm_rhs,
+                     const __grid_constant__ CUtensorMap tm_bs,
                      const Params p) {
-  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4;
+  constexpr bool kNv = F == WFmt::kE2M1;  // NVFP4: e2m1 codes with an e4m3 scale per 16 k
+  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || kNv;
   constexpr int STEPS_PER_RAW = k4 ? 2 : 1;  // a raw box holds 256 k of a 4-bit format
   int32_t go;
   if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
@@ -236,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch(&tm_lhs);
     tma_prefetch(&tm_rhs);
+    if constexpr (kNv) tma_prefetch(&tm_bs);
   }
   if (warp == 1) {
     tmem_alloc(sbase + OFF_TMEM, TMEM_COLS);
@@ -281,9 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(rawfull_bar(as), RAW_BYTES);
-          tma_load_3d(sbase + OFF_RAW + as * RAW_BYTES, &tm_rhs, rawfull_bar(as), (ks / STEPS_PER_RAW) * 128,
+          mbar_arrive_expect_tx(rawfull_bar(as), kNv ? RAW_STAGE : RAW_BYTES);
+          tma_load_3d(sbase + OFF_RAW + as * RAW_STAGE, &tm_rhs, rawfull_bar(as), (ks / STEPS_PER_RAW) * 128,
                       t.n_tile * BMW, t.local_group);
+          if constexpr (kNv)  // the box's block scales: 16 bytes of each of its 128 weight rows
+            tma_load_3d(sbase + OFF_RAW + as * RAW_STAGE + RAW_BYTES, &tm_bs, rawfull_bar(as),
+                        (ks / STEPS_PER_RAW) * 16, t.n_tile * BMW, t.local_group);
           apend |= 1u << as;
           apar = (apar & ~(1u << as)) | (aph << as);
         }
@@ -551,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();  // the MMAs that read this A stage are complete
-        const uint32_t src = sbase + OFF_RAW + rs * RAW_BYTES + uint32_t(r) * 128u;
+        const uint32_t src = sbase + OFF_RAW + rs * RAW_STAGE + uint32_t(r) * 128u;
         const uint32_t sw = uint32_t(r & 7);
         uint32_t o[32];
         if constexpr (k4) {
@@ -562,12 +593,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(x[cc][0]), "=r"(x[cc][1]), "=r"(x[cc][2]), "=r"(x[cc][3])
                          : "r"(src + ((uint32_t(4 * h + part * kC + cc) ^ sw) << 4)));
+          // NVFP4: the scales of the thread's four 16-k blocks (bytes 8 h + 4 part .. + 3
+          // of its row in the box's scale rows), each as an fp16 pair
+          uint32_t sp[4] = {0u, 0u, 0u, 0u};
+          if constexpr (kNv) {
+            uint32_t sb, lo, hi;
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=r"(sb)
+                         : "r"(sbase + OFF_RAW + rs * RAW_STAGE + RAW_BYTES + uint32_t(r) * 16u +
+                               uint32_t(8 * h + 4 * part)));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(uint16_t(sb)));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(uint16_t(sb >> 16)));
+            sp[0] = prmt(lo, lo, 0x1010u);
+            sp[1] = prmt(lo, lo, 0x3232u);
+            sp[2] = prmt(hi, hi, 0x1010u);
+            sp[3] = prmt(hi, hi, 0x3232u);
+          }
 #pragma unroll
           for (int cc = 0; cc < kC; ++cc)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               uint32_t q[4];
-              nib8_to_f16<F == WFmt::kInt4>(x[cc][u], q);
+              if constexpr (kNv)
+                e2m1x8_to_f16(x[cc][u], sp[2 * cc + (u >> 1)], q);  // codes 32 cc + 8 u ..: block 2 cc + u / 2
+              else
+                nib8_to_f16<F == WFmt::kInt4>(x[cc][u], q);
 #pragma unroll
               for (int i = 0; i < 4; ++i) o[16 * cc + 4 * u + i] = q[i];
             }
@@ -619,11 +669,12 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
   auto kern = gemm_f16w_kernel<F, kOutF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4;
+  constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
            L.lhs_scale, L.num_lhs_blocks, static_cast<const uint16_t*>(L.lhs_raw),
-           static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k)};
+           static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k),
+           F == WFmt::kE2M1 ? L.mx_scale : nullptr};
   // Launched as the programmatic dependent of the split pass just before it in
   // the stream: the prologue and the weight stream overlap that kernel's end.
   cudaLaunchConfig_t cfg = {};
@@ -636,7 +687,7 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L.tm_lhs, L.tm_rhs, p);
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_lhs, L.tm_rhs, L.tm_bs, p);
 }
 
 template <WFmt F>
@@ -652,6 +703,7 @@ cudaError_t launch_f16w(const ScaledLaunch& p, int weight_format, bool out_f32, 
     case kWeightInt8: return f16w::launch_fmt<fp8::WFmt::kInt8>(p, out_f32, grid, stream);
     case kWeightInt4: return f16w::launch_fmt<fp8::WFmt::kInt4>(p, out_f32, grid, stream);
     case kWeightUint4: return f16w::launch_fmt<fp8::WFmt::kUint4>(p, out_f32, grid, stream);
+    case kWeightE2M1: return f16w::launch_fmt<fp8::WFmt::kE2M1>(p, out_f32, grid, stream);  // NVFP4 (tm_bs)
     default: return cudaErrorInvalidValue;
   }
 }

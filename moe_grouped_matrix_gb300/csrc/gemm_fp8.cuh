@@ -218,6 +218,9 @@ struct Params {
   const uint16_t* x;
   const uint8_t* w;
   int64_t w_row_bytes;
+  // NVFP4 on the fp16-weight kernel: e4m3 block scales [L, n, k / 16] of the e2m1
+  // weights (applied again by the exact recompute); NULL otherwise.
+  const uint8_t* w_block_scale;
 };
 
 // A 4-byte asynchronous copy global -> shared, and the arrive on an mbarrier
@@ -518,7 +521,7 @@ __device__ __forceinline__ void weights8(uint2 raw, float (&v)[8]) {
 template <WFmt F>
 __device__ __forceinline__ float exact_row_sum(const uint16_t* __restrict__ x, const uint8_t* __restrict__ wrow,
                                                const void* scale, bool scale_e8m0, int64_t s0, int64_t sn,
-                                               int32_t k, int32_t nb) {
+                                               int32_t k, int32_t nb, const uint8_t* __restrict__ bs_row = nullptr) {
   constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || F == WFmt::kE2M1;
   const int32_t kb = k / nb;
   float total = 0.f;
@@ -530,6 +533,11 @@ __device__ __forceinline__ float exact_row_sum(const uint16_t* __restrict__ x, c
                            : __ldg(reinterpret_cast<const uint2*>(wrow + k0));
       float wv[8];
       weights8<F>(raw, wv);
+      if (bs_row != nullptr) {  // NVFP4: the 8 codes' e4m3 block scale (per 16 k); w * s is exact
+        const float s16 = e4m3x2_value(__ldg(bs_row + k0 / 16)).x;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wv[i] *= s16;
+      }
       const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -643,7 +651,9 @@ __device__ __noinline__ void fix_marked_rows(const Params& p, int32_t go, const 
       const uint16_t* x = p.x + int64_t(row) * p.k;
       for (int32_t c = threadIdx.x; c < p.n; c += blockDim.x) {
         float v = exact_row_sum<F>(x, p.w + (int64_t(lg) * p.n + c) * p.w_row_bytes, p.scale, p.scale_e8m0 != 0,
-                                   int64_t(lg) * nb * p.n + c, p.n, p.k, nb);
+                                   int64_t(lg) * nb * p.n + c, p.n, p.k, nb,
+                                   p.w_block_scale != nullptr ? p.w_block_scale + (int64_t(lg) * p.n + c) * (p.k / 16)
+                                                              : nullptr);
         if (p.bias != nullptr) {
           const int64_t bi = int64_t(lg) * p.n + c;
           v += p.bias_f32 ? __ldg(static_cast<const float*>(p.bias) + bi)

@@ -410,15 +410,11 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
     const int act_split = opt.act_split == GMM_SPLIT_KERNEL ? 0 : (opt.act_split == GMM_SPLIT_PASS ? 2 : 1);
     // The fp8 kernels; bf16 activations are split once per row into the
     // workspace when it has room (act_split.cu), in the kernel's k steps.
-    auto fp8_kernel = [&](int fmt) -> int {
-      // int8 and int4 with bf16 activations: the fp16 split (2 m k bytes of
-      // fp16 values, then (scale, mark) per 128-wide step) and the fp16-MMA
-      // kernel, when the workspace holds the split; else the e4m3 path below.
-      // uint4 stays on the e4m3 path: its code table makes the e4m3 rewrite
-      // cheap, and there the e4m3 kernel measured faster (120 us against 129 us
-      // on the decode workload; int4 131 against 136, int8 124 against 229).
-      const bool intw = fmt == gmmk::kWeightInt8 || fmt == gmmk::kWeightInt4;
-      if (!lhs8 && act_split != 0 && intw) {
+    // The fp16 split (2 m k bytes of fp16 values, then (scale, mark) per
+    // 128-wide step) and the fp16-MMA kernel (gemm_f16w.cu) on launch `L`; -1
+    // when the workspace cannot hold the split.
+    auto run_f16w = [&](gmmk::ScaledLaunch& L, int fmt) -> int {
+      {
         const int64_t ksteps = k / 128;
         const size_t scales_at = (kActOffset + size_t(2 * m * k) + 255) & ~size_t(255);
         const size_t end = scales_at + size_t(m * ksteps) * 2 * sizeof(float);
@@ -430,12 +426,12 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
           const uint64_t dims[3] = {64u, uint64_t(m), uint64_t(k / 64)};
           const uint64_t strides[2] = {uint64_t(2 * k), 128u};
           const uint32_t box[3] = {64u, 16u, 2u};
-          if (int st = make_map_strided(&S.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, plane, dims, strides, box,
+          if (int st = make_map_strided(&L.tm_lhs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, plane, dims, strides, box,
                                         CU_TENSOR_MAP_SWIZZLE_128B))
             return st;
-          S.lhs_split = 1;
-          S.lhs_scale = scales;
-          S.num_lhs_blocks = int32_t(ksteps);
+          L.lhs_split = 1;
+          L.lhs_scale = scales;
+          L.num_lhs_blocks = int32_t(ksteps);
           if (cudaError_t e1 = gmmk::launch_act_split_f16(lhs, m, k, plane, scales, err + 1,
                                                           fmt != gmmk::kWeightInt8, s))
             return cuda_fail(e1);
@@ -445,9 +441,22 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
                          entry, (long long)m, (long long)k, (long long)n, num_total_groups, num_local_groups,
                          group_offset_dev ? "device" : "host", dtype_name(lhs_dtype), dtype_name(rhs_dtype),
                          dtype_name(out_dtype));
-          if (cudaError_t e2 = gmmk::launch_f16w(S, fmt, f32, dev.sms, s)) return cuda_fail(e2);
+          if (cudaError_t e2 = gmmk::launch_f16w(L, fmt, f32, dev.sms, s)) return cuda_fail(e2);
           return GMM_OK;
         }
+      }
+      return -1;
+    };
+    auto fp8_kernel = [&](int fmt) -> int {
+      // int8 and int4 with bf16 activations: the fp16 split and the fp16-MMA
+      // kernel, when the workspace holds the split; else the e4m3 path below.
+      // uint4 stays on the e4m3 path: its code table makes the e4m3 rewrite
+      // cheap, and there the e4m3 kernel measured faster (120 us against 129 us
+      // on the decode workload; int4 131 against 136, int8 124 against 229).
+      const bool intw = fmt == gmmk::kWeightInt8 || fmt == gmmk::kWeightInt4;
+      if (!lhs8 && act_split != 0 && intw) {
+        const int r = run_f16w(S, fmt);
+        if (r != -1) return r;
         if (act_split == 2) return GMM_ERR_WORKSPACE;
       }
       if (!lhs8 && act_split != 0 && !intw) {
@@ -500,6 +509,27 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       log_decoding();
       e = gmmk::launch_scaled(S, true, f32, dev.sms, s);
     } else if (nvfp4) {
+      // NVFP4 with bf16 activations on the fp16-MMA kernel (each code times its
+      // block scale is exact in fp16) when k % 256 == 0 (the block scales'
+      // rows, k / 16 bytes, are then whole 16-byte units for TMA), the scales
+      // are 16-byte aligned and the workspace holds the split; else the
+      // decoding kernel.
+      if (act_split != 0 && k % 256 == 0 && aligned16(ext.rhs_block_scale)) {
+        gmmk::ScaledLaunch L2 = S;
+        const uint64_t wdims[3] = {uint64_t(k / 2), uint64_t(n), uint64_t(num_local_groups)};
+        const uint32_t wbox[3] = {128u, 128u, 1u};
+        if (int st = make_map(&L2.tm_rhs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, rhs, wdims, wbox,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+          return st;
+        const uint64_t sdims[3] = {uint64_t(k / 16), uint64_t(n), uint64_t(num_local_groups)};
+        const uint32_t sbox[3] = {16u, 128u, 1u};
+        if (int st = make_map(&L2.tm_bs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3, ext.rhs_block_scale, sdims, sbox,
+                              CU_TENSOR_MAP_SWIZZLE_NONE))
+          return st;
+        const int r = run_f16w(L2, gmmk::kWeightE2M1);
+        if (r != -1) return r;
+        if (act_split == 2) return GMM_ERR_WORKSPACE;
+      }
       log_decoding();
       e = gmmk::launch_scaled_nvfp4(S, f32, dev.sms, s);
     } else {

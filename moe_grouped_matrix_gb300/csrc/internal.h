@@ -68,6 +68,7 @@ cudaError_t launch_tgmm_2sm(const TgmmLaunch& p, bool out_f32, int max_ctas, cud
 struct ScaledLaunch {
   CUtensorMap tm_lhs;  // lhs [m, k] bf16, box {64, 16}; e4m3 (lhs_e4m3), box {128, 16}
   CUtensorMap tm_rhs;  // rhs [L, n, k]: e4m3 box {128, 128, 1} / bf16 box {64, 128, 1}
+  CUtensorMap tm_bs;   // fp16-weight kernel, NVFP4: the e4m3 block scales [L, n, k / 16], box {16, 128, 1}
   const int32_t* group_sizes;
   int32_t num_total_groups, group_offset, num_local_groups;
   int32_t m, n, k;

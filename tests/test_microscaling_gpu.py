@@ -156,6 +156,29 @@ def test_nvfp4_every_code_and_group_offset():
     check_close(out, ref, mag, "NVFP4 every code")
 
 
+def test_nvfp4_marked_rows_are_summed_again_with_their_block_scales():
+    # activations whose 128-wide steps the fp16 split cannot hold (values below fp16's grid
+    # under a large one, a NaN-free wide spread): those rows are marked and summed again from
+    # the stored values, block scales included
+    m, k, n, L = 24, 512, 256, 2
+    x = W.normal((m, k), 1.0, 131).float()
+    x[3, ::128] = 1.0
+    x[3, 1::128] = 1.5 * 2.0 ** -40                               # below fp16's grid: marked
+    x[5] = x[5] * torch.pow(2.0, torch.linspace(-40, 10, k))      # many binades per step
+    x[7, ::128] = 3e4
+    x[7, 5::128] = 2.0 ** -30
+    lhs = x.to(torch.bfloat16).to(DEV)
+    rhs = W.weights("e2m1", (L, n, k), 132, DEV)
+    bs = _nvfp4_scales((L, n, k // 16), 133)
+    sizes = np.array([10, 14], np.int32)
+    out = G.gmm(lhs, rhs, torch.tensor(sizes, device=DEV), rhs_block_scale=bs, rhs_format="e2m1",
+                out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = _oracle_fp4(lhs, rhs, sizes, bs)
+    check_close(out, ref, mag, "NVFP4 with marked rows")
+
+
 def test_nvfp4_decode_workload_sampled_rows():
     wl = W.fp8_decode(DEV, fmt="e2m1")
     sizes = wl["group_sizes"]
