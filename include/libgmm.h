@@ -317,10 +317,14 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *                      MXFP8: E4M3 rhs, GMM_DTYPE_E8M0 scales, block_size 32;
  *                      NVFP4: E2M1 rhs, GMM_DTYPE_E4M3 scales, block_size 16 (the second-level
  *                      fp32 scale of NVFP4 is rhs_scale with num_quant_blocks = 1).
- *                    They run on the decoding kernel: the decoders multiply each decoded bf16
- *                    weight by its block scale, exactly (MXFP8 while the product stays in bf16's
- *                    normal range; an e2m1 value times an e4m3 value always fits bf16).  No
- *                    alignment requirement for the scales.
+ *                    MXFP8 runs on the decoding kernel: the decoders multiply each decoded bf16
+ *                    weight by its block scale, exactly while the product stays in bf16's normal
+ *                    range.  NVFP4 runs on the fp16-weight kernel (an fp16 split of the bf16 lhs
+ *                    in the workspace, like int4) when k % 256 == 0, the scales are 16-byte
+ *                    aligned and the workspace holds the split: each e2m1 code times its e4m3
+ *                    scale is an exact fp16 weight; otherwise on the decoding kernel (an e2m1
+ *                    value times an e4m3 value always fits bf16).  No other alignment
+ *                    requirement for the scales.
  *   keep_other_rows  0: rows outside the local groups are set to 0 (gmm); 1: they keep the
  *                    caller's contents (gmm_into).
  *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k
