@@ -631,6 +631,14 @@ def _ncu_decode_int4(torch, G, W, dev):
                          rhs_format="int4")
 
 
+def _ncu_decode_nvfp4(torch, G, W, dev):
+    fd = W.fp8_decode(dev, fmt="e2m1")
+    gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
+    L, n, k = fd["rhs"].shape[0], fd["rhs"].shape[1], fd["lhs"].shape[1]
+    bs = W.uniform((L, n, k // 16), 0.0625, 16.0, 121, dev).to(torch.float8_e4m3fn)
+    return lambda: G.gmm(fd["lhs"], fd["rhs"], gs, rhs_block_scale=bs, rhs_format="e2m1", rhs_bias=fd["rhs_bias"])
+
+
 def _ncu_decode_int8(torch, G, W, dev):
     fd = W.fp8_decode(dev, fmt="int8")
     gs = torch.tensor(fd["group_sizes"], dtype=torch.int32, device=dev)
@@ -653,6 +661,7 @@ def _ncu_moe128_wi(torch, G, W, dev):
 
 NCU_CASES = {"gemm_small": _ncu_gemm_small, "tgmm": _ncu_tgmm, "fp8_decode": _ncu_fp8_decode,
              "moe128_wi": _ncu_moe128_wi, "decode_int4": _ncu_decode_int4, "decode_int8": _ncu_decode_int8,
+             "decode_nvfp4": _ncu_decode_nvfp4,
              "w8a8_decode": _ncu_w8a8_decode}
 
 
