@@ -1,4 +1,4 @@
-// Grouped matmul with int8, int4 or uint4 weights on the fp16 tensor cores:
+// Grouped matmul with int8, int4, uint4 or NVFP4 weights on the fp16 tensor cores:
 //   out[r, c] = sum_b s[g, b, c] * sum_{kk in block b} lhs[r, kk] * W(g, c, kk) + bias[g, c]
 // (page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230", gmm.py:
 // _accum scales each quant block's partial sum by rhs_scale[g, b, 0, n] and adds
@@ -13,6 +13,10 @@
 // codes (gemm_fp8.cuh) needs table lookups and held the integer pipe.  The
 // 4-bit rewrite produces each 8 k in the order 0, 4, 1, 5, 2, 6, 3, 7; the
 // activation rows are stored in the same order, so the products pair up.
+// NVFP4 (e2m1 codes with an e4m3 scale per 16 k; microscaling, the scope's
+// next formats) is a 4-bit format whose rewrite also multiplies each code by
+// its block scale, which fp16 holds exactly (e2m1x8_to_f16); the block scales
+// come with each raw box.
 //
 // Activations: bf16 rows split once per row and 128-wide step by
 // act_split_f16_kernel (act_split.cu) into fp16 values x / sc with sc a power
@@ -26,7 +30,8 @@
 // Pipeline (one CTA per SM, persistent over items of (local group, chunk of
 // up to 16 of its rows, 128-wide n tile)); a step is 128 k:
 //   warp 0      TMA: raw weight boxes {128 bytes, 128 rows} (128 k of int8,
-//               256 k of a 4-bit format: two steps) into a 6-deep ring
+//               256 k of a 4-bit format: two steps; NVFP4 adds the box's
+//               {16 bytes, 128 rows} of block scales) into a 6-deep ring
 //   warp 17     TMA: the chunk's fp16 activation rows, one {64 k, 16 rows,
 //               2 atoms} box a step, into an 8-deep ring
 //   warps 8-15  rewrite a step's raw codes as an fp16 A tile in tensor memory
