@@ -17,6 +17,13 @@
 // next formats) is a 4-bit format whose rewrite also multiplies each code by
 // its block scale, which fp16 holds exactly (e2m1x8_to_f16); the block scales
 // come with each raw box.
+// MXFP8 (e4m3 codes with an E8M0 scale per 32 k): every e4m3 value is an fp16
+// value (one cvt per two codes), but a power of two from 2^-127 to 2^127 is
+// not always one, so the block scales are not folded into the weights: each
+// 32-k block of a step accumulates into its own 16 columns (a step's slot is
+// 64 columns, 4 slots), and the epilogue scales the four partial sums by their
+// blocks' powers of two.  The E8M0 bytes come with the step's scales (4 bytes
+// of each weight row a step).
 //
 // Activations: bf16 rows split once per row and 128-wide step by
 // act_split_f16_kernel (act_split.cu) into fp16 values x / sc with sc a power
@@ -90,7 +97,10 @@ constexpr uint32_t A_COL0 = NACC * SLOT_COLS;  // the A tiles follow the accumul
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NSC = 8;
 constexpr int SC_TOK = BT;                 // the chunk rows' split scales
-constexpr int SC_PER = SC_TOK + BMW;       // then one 512-byte weight-scale row
+constexpr int SC_MX = SC_TOK + BMW;        // MXFP8: the step's 4 E8M0 bytes of each weight row
+constexpr int SC_PER = SC_MX + BMW;        // after one 512-byte weight-scale row
+constexpr int MX_SLOT_COLS = 4 * BT;       // MXFP8: a step's four 32-k blocks, 16 columns each
+constexpr int MX_NACC = A_COL0 / MX_SLOT_COLS;
 constexpr int kMaxGroups = 1024;
 constexpr int kConvWarps = 8;             // the weight rewrite: two threads per weight row
 constexpr int kParts = kConvWarps / 4;
@@ -126,6 +136,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_B % 1024 == 0 && B_ATOM % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 static_assert(CST <= NDONE && BST <= NDONE && NACC <= NDONE, "step-done ring indexing");
 static_assert(NACC * SLOT_COLS <= int(A_COL0) && A_COL0 + CST * A_COLS <= TMEM_COLS, "TMEM map");
+static_assert(MX_NACC * MX_SLOT_COLS <= int(A_COL0) && MX_NACC <= NACC, "TMEM map (MXFP8)");
 
 // kind::f16 with fp16 A and B (type code 0), both K-major, f32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) { return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24); }
@@ -161,6 +172,14 @@ __device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
   const uint32_t u = w ^ 0x80808080u;
   lo = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
   hi = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+// Four e4m3 codes (k order, lowest in the low byte) -> two fp16x2 words, the
+// lower byte of each pair in the lower half: exact, every e4m3fn value being an
+// fp16 value (the NaN codes become NaN).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(uint16_t(w)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(uint16_t(w >> 16)));
 }
 
 // Eight 4-bit codes (k order from the low nibble) -> four fp16x2 words holding
@@ -228,6 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kNv = F == WFmt::kE2M1;  // NVFP4: e2m1 codes with an e4m3 scale per 16 k
   constexpr bool k4 = F == WFmt::kInt4 || F == WFmt::kUint4 || kNv;
   constexpr int STEPS_PER_RAW = k4 ? 2 : 1;  // a raw box holds 256 k of a 4-bit format
+  constexpr bool kMx = F == WFmt::kE4M3;     // MXFP8: e4m3 codes with an E8M0 scale per 32 k
+  constexpr int kSlotCols = kMx ? MX_SLOT_COLS : SLOT_COLS;
+  constexpr int kNacc = kMx ? MX_NACC : NACC;
   int32_t go;
   if (!resolve_group_offset(p.group_offset_dev, p.group_offset, p.num_total_groups, p.num_local_groups, p.err, go))
     return;
@@ -370,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int32_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
       for (int32_t ks = 0; ks < ksteps; ++ks, ++j) {
         if ((j & uint32_t(kIssuers - 1)) != mine) continue;
-        const uint32_t cs = j % CST, bs = j % BST, slot = j % NACC;
-        if (!wait_bar(acce_bar(slot), ((j / NACC) & 1u) ^ 1u, abort_flag, p.err) ||
+        const uint32_t cs = j % CST, bs = j % BST, slot = j % kNacc;
+        if (!wait_bar(acce_bar(slot), ((j / kNacc) & 1u) ^ 1u, abort_flag, p.err) ||
             !wait_bar(convfull_bar(cs), (j / CST) & 1u, abort_flag, p.err) ||
             !wait_bar(bfull_bar(bs), (j / BST) & 1u, abort_flag, p.err)) {
           ok = false;
@@ -381,11 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t a0 = tmem_base + A_COL0 + cs * A_COLS;
           const uint32_t b0 = sbase + OFF_B + bs * B_BYTES;
-          const uint32_t d = tmem_base + slot * SLOT_COLS;
+          const uint32_t d = tmem_base + slot * kSlotCols;
 #pragma unroll
           for (int kk = 0; kk < KS / 16; ++kk) {
             const uint32_t atom = uint32_t(kk >> 2), off = uint32_t(kk & 3) * 32u;
-            mma_f16_ts(d, a0 + 8u * kk, sw128_desc(b0 + atom * B_ATOM + off, 16, 1024), kIdesc, kk != 0 ? 1u : 0u);
+            const uint64_t bd = sw128_desc(b0 + atom * B_ATOM + off, 16, 1024);
+            if constexpr (kMx)  // 32-k block kk / 2 into its own 16 columns
+              mma_f16_ts(d + uint32_t(BT) * uint32_t(kk >> 1), a0 + 8u * kk, bd, kIdesc, uint32_t(kk & 1));
+            else
+              mma_f16_ts(d, a0 + 8u * kk, bd, kIdesc, kk != 0 ? 1u : 0u);
           }
           mma_commit(stepdone_bar(j % NDONE));
         }
@@ -430,17 +456,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float sw = p.scale == nullptr ? 1.f
                            : p.scale_e8m0   ? fp8::e8m0_value(wsc[wrow])
                                             : reinterpret_cast<const float*>(wsc)[wrow];
-          float d[T8];
-          fp8::tmem_ld_cols<T8>(tmem_base + lane_base + slot * SLOT_COLS, d);
+          if constexpr (kMx) {
+            // the four 32-k blocks' sums, two per load: D_q * sc_i is the block's partial
+            // sum, times its power of two (and the quant block's weight scale)
+            const uint32_t e4 = reinterpret_cast<const uint32_t*>(ts + SC_MX)[wrow];
+            const uint32_t col0 = tmem_base + lane_base + slot * kSlotCols;
 #pragma unroll
-          for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
+            for (int h = 0; h < 2; ++h) {
+              const float u0 = sw * fp8::e8m0_value((e4 >> (16 * h)) & 255u);
+              const float u1 = sw * fp8::e8m0_value((e4 >> (16 * h + 8)) & 255u);
+              float d[2 * BT];
+              fp8::tmem_ld_cols<2 * BT>(col0 + uint32_t(2 * BT * h), d);
+#pragma unroll
+              for (int i = 0; i < T8; ++i) acc[i] = fmaf(u1, ts[i] * d[BT + i], fmaf(u0, ts[i] * d[i], acc[i]));
+            }
+          } else {
+            float d[T8];
+            fp8::tmem_ld_cols<T8>(tmem_base + lane_base + slot * SLOT_COLS, d);
+#pragma unroll
+            for (int i = 0; i < T8; ++i) acc[i] = fmaf(sw * ts[i], d[i], acc[i]);
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(acce_bar(slot));
             mbar_arrive(sempty_bar(sc));
           }
-          if (++slot == NACC) slot = 0;
+          if (++slot == uint32_t(kNacc)) slot = 0;
           if (++ds == NDONE) {
             ds = 0;
             dph ^= 1u;
@@ -536,6 +578,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           tscale[sc * SC_PER + lane] = 0.f;
       }
+      if constexpr (kMx) {
+        // the step's 4 E8M0 bytes of each of the item's weight rows (rows of k / 32
+        // bytes; k % 128 == 0, so each copy is 4-byte aligned)
+        const int32_t cols = min(BMW, p.n - t.n_tile * BMW);
+        const int64_t pitch = p.k / 32;
+        const uint8_t* src = p.w_block_scale + (int64_t(t.local_group) * p.n + int64_t(t.n_tile) * BMW) * pitch + 4 * ks;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(tscale + sc * SC_PER + SC_MX);
+#pragma unroll
+        for (int q = 0; q < BMW / 32; ++q) {
+          const int c = lane + 32 * q;
+          if (c < cols)
+            cp_async_4(smem_u32(dst + c), src + c * pitch);
+          else
+            dst[c] = 0u;
+        }
+      }
       cp_async_mbar_arrive(sfull_bar(sc));
       uint32_t wbytes = 0;
       if (p.scale != nullptr) {
@@ -571,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sub-partition has two rewrite warps to interleave).  Raw rows are 128
     // bytes, 128-byte swizzled (16-byte chunk j of row r at position j ^ (r % 8));
     // A column 4 q + i holds word i of the row's 16-byte fp16 chunk q (8 k).
-    // int8: raw chunk c (16 codes) becomes A chunks 2c and 2c + 1.
+    // int8 and e4m3: raw chunk c (16 codes) becomes A chunks 2c and 2c + 1.
     // 4-bit: raw chunk 4 h + c of the box (step h of its two) becomes A chunks
     // 4c .. 4c + 3.  Either way part p writes columns 32 p .. 32 p + 31.
     const int r = (warp & 3) * 32 + lane, part = (warp - kConvWarp0) >> 2;
@@ -637,7 +695,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < kC; ++cc)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) int8x4_to_f16(x[cc][u], o[8 * cc + 2 * u], o[8 * cc + 2 * u + 1]);
+            for (int u = 0; u < 4; ++u) {
+              if constexpr (kMx)
+                e4m3x4_to_f16(x[cc][u], o[8 * cc + 2 * u], o[8 * cc + 2 * u + 1]);
+              else
+                int8x4_to_f16(x[cc][u], o[8 * cc + 2 * u], o[8 * cc + 2 * u + 1]);
+            }
         }
         tmem_st_32cols(tmem_base + lane_base + A_COL0 + cs * A_COLS + 32u * part, o);
         tmem_st_wait();
@@ -679,7 +742,7 @@ cudaError_t launch_impl(const ScaledLaunch& L, int grid, cudaStream_t stream) {
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
            L.lhs_scale, L.num_lhs_blocks, static_cast<const uint16_t*>(L.lhs_raw),
            static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k),
-           F == WFmt::kE2M1 ? L.mx_scale : nullptr};
+           F == WFmt::kE2M1 || F == WFmt::kE4M3 ? L.mx_scale : nullptr};
   // Launched as the programmatic dependent of the split pass just before it in
   // the stream: the prologue and the weight stream overlap that kernel's end.
   cudaLaunchConfig_t cfg = {};
@@ -709,6 +772,10 @@ cudaError_t launch_f16w(const ScaledLaunch& p, int weight_format, bool out_f32, 
     case kWeightInt4: return f16w::launch_fmt<fp8::WFmt::kInt4>(p, out_f32, grid, stream);
     case kWeightUint4: return f16w::launch_fmt<fp8::WFmt::kUint4>(p, out_f32, grid, stream);
     case kWeightE2M1: return f16w::launch_fmt<fp8::WFmt::kE2M1>(p, out_f32, grid, stream);  // NVFP4 (tm_bs)
+    case kWeightE4M3:  // MXFP8 only: the E8M0 block scales are required
+      if (p.mx_scale == nullptr || reinterpret_cast<uintptr_t>(p.mx_scale) % 4 != 0 || p.k % 128 != 0)
+        return cudaErrorInvalidValue;
+      return f16w::launch_fmt<fp8::WFmt::kE4M3>(p, out_f32, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

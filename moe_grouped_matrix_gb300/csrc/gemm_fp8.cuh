@@ -533,10 +533,16 @@ __device__ __forceinline__ float exact_row_sum(const uint16_t* __restrict__ x, c
                            : __ldg(reinterpret_cast<const uint2*>(wrow + k0));
       float wv[8];
       weights8<F>(raw, wv);
-      if (bs_row != nullptr) {  // NVFP4: the 8 codes' e4m3 block scale (per 16 k); w * s is exact
-        const float s16 = e4m3x2_value(__ldg(bs_row + k0 / 16)).x;
+      if (bs_row != nullptr) {
+        // NVFP4: the 8 codes' e4m3 block scale (per 16 k); MXFP8: their E8M0 one (per
+        // 32 k).  w * s is exact (in fp32's range, for MXFP8)
+        float sb;
+        if constexpr (F == WFmt::kE2M1)
+          sb = e4m3x2_value(__ldg(bs_row + k0 / 16)).x;
+        else
+          sb = e8m0_value(__ldg(bs_row + k0 / 32));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wv[i] *= s16;
+        for (int i = 0; i < 8; ++i) wv[i] *= sb;
       }
       const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
@@ -652,8 +658,9 @@ __device__ __noinline__ void fix_marked_rows(const Params& p, int32_t go, const 
       for (int32_t c = threadIdx.x; c < p.n; c += blockDim.x) {
         float v = exact_row_sum<F>(x, p.w + (int64_t(lg) * p.n + c) * p.w_row_bytes, p.scale, p.scale_e8m0 != 0,
                                    int64_t(lg) * nb * p.n + c, p.n, p.k, nb,
-                                   p.w_block_scale != nullptr ? p.w_block_scale + (int64_t(lg) * p.n + c) * (p.k / 16)
-                                                              : nullptr);
+                                   p.w_block_scale != nullptr
+                                       ? p.w_block_scale + (int64_t(lg) * p.n + c) * (p.k / (F == WFmt::kE2M1 ? 16 : 32))
+                                       : nullptr);
         if (p.bias != nullptr) {
           const int64_t bi = int64_t(lg) * p.n + c;
           v += p.bias_f32 ? __ldg(static_cast<const float*>(p.bias) + bi)

@@ -432,8 +432,10 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
           L.lhs_split = 1;
           L.lhs_scale = scales;
           L.num_lhs_blocks = int32_t(ksteps);
-          if (cudaError_t e1 = gmmk::launch_act_split_f16(lhs, m, k, plane, scales, err + 1,
-                                                          fmt != gmmk::kWeightInt8, s))
+          // 4-bit codes come out of their rewrite as k (0, 4), (1, 5), ..: the split
+          // stores those rows in the same order
+          const bool perm = fmt == gmmk::kWeightInt4 || fmt == gmmk::kWeightUint4 || fmt == gmmk::kWeightE2M1;
+          if (cudaError_t e1 = gmmk::launch_act_split_f16(lhs, m, k, plane, scales, err + 1, perm, s))
             return cuda_fail(e1);
           if (log_enabled())
             std::fprintf(stderr, "libgmm: %s m=%lld k=%lld n=%lld groups=%d local=%d offset=%s lhs=%s rhs=%s out=%s "
@@ -503,9 +505,18 @@ int gmm_impl(const void* lhs, int lhs_dtype, int64_t m, int64_t k, const void* r
       log_decoding();
       e = gmmk::launch_scaled(S, false, f32, dev.sms, s);
     } else if (rhs_dtype == GMM_DTYPE_E4M3) {
-      int decode = opt.e4m3_kernel == GMM_E4M3_DECODE ? 1 : 0;
-      if (mx) decode = 1;  // per-32 scales are applied as the weights are decoded
-      if (!decode) return fp8_kernel(gmmk::kWeightE4M3);
+      const bool decode = opt.e4m3_kernel == GMM_E4M3_DECODE;
+      if (!decode && !mx) return fp8_kernel(gmmk::kWeightE4M3);
+      // MXFP8 with bf16 activations on the fp16-MMA kernel (e4m3 codes are fp16
+      // values; each 32-k block sums into its own accumulator and is scaled by its
+      // power of two after) when the scales are 4-byte aligned and the workspace
+      // holds the split; else (or with GMM_E4M3_DECODE) the decoding kernel, which
+      // applies the per-32 scales as it decodes.
+      if (mx && !decode && act_split != 0 && reinterpret_cast<uintptr_t>(ext.rhs_block_scale) % 4 == 0) {
+        const int r = run_f16w(S, gmmk::kWeightE4M3);
+        if (r != -1) return r;
+        if (act_split == 2) return GMM_ERR_WORKSPACE;
+      }
       log_decoding();
       e = gmmk::launch_scaled(S, true, f32, dev.sms, s);
     } else if (nvfp4) {

@@ -84,8 +84,8 @@ struct ScaledLaunch {
   int32_t lhs_e4m3;                 // lhs holds e4m3 codes (fp8 kernels only)
   const float* lhs_scale;           // lhs_e4m3: NULL or f32 [m, num_lhs_blocks]
   int32_t num_lhs_blocks;
-  const uint8_t* mx_scale;          // decoding kernel: NULL, E8M0 [L, n, k / 32] (e4m3 weights) or
-                                    // e4m3 [L, n, k / 16] (e2m1 weights)
+  const uint8_t* mx_scale;          // decoding and fp16-weight kernels: NULL, E8M0 [L, n, k / 32]
+                                    // (e4m3 weights) or e4m3 [L, n, k / 16] (e2m1 weights)
   int32_t lhs_split;                // fp8 kernels: tm_lhs spans act_split's h / l / h2 / l2 planes
                                     // [4, m, k] (box {128, 8, 4}); lhs_scale its (s1, s2) step
                                     // scales [m, k steps, 2]

@@ -1,6 +1,8 @@
 """Microscaling weight block scales on the GPU: MXFP8 (float8_e4m3fn weights with one E8M0
 scale per 32 consecutive k of a weight row) against the oracle evaluated on the same stored
-bytes, with the per-block fp32 scale, bias, ragged groups, group_offset and both output dtypes."""
+bytes, with the per-block fp32 scale, bias, ragged groups, group_offset and both output dtypes,
+on the fp16-weight kernel (the default) and on the decoding kernel (e4m3_kernel="decode", and
+scales that are not 4-byte aligned); then NVFP4."""
 
 import numpy as np
 import pytest
@@ -42,9 +44,12 @@ def _oracle(lhs, rhs, sizes, mx, go=0, rhs_scale=None, bias=None, rows=None):
 SIZES = np.array([0, 37, 1, 64, 50, 9], np.int32)
 
 
+@pytest.mark.parametrize("kernel", ["auto", "decode"])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("with_scale", [False, True])
-def test_mxfp8_matches_oracle(with_scale, out_dtype):
+def test_mxfp8_matches_oracle(with_scale, out_dtype, kernel, monkeypatch):
+    if kernel == "decode":
+        use_options(monkeypatch, e4m3_kernel="decode")
     m, k, n, L = 200, 512, 384, 6
     lhs = W.normal((m, k), 1.0, 61, DEV)
     rhs = W.weights("e4m3", (L, n, k), 62, DEV)
@@ -56,7 +61,7 @@ def test_mxfp8_matches_oracle(with_scale, out_dtype):
     torch.cuda.synchronize()
     assert G.read_device_errors() == 0
     ref, mag = _oracle(lhs, rhs, SIZES, mx, rhs_scale=scale, bias=bias)
-    check_close(out, ref, mag, f"MXFP8 (scale {with_scale})")
+    check_close(out, ref, mag, f"MXFP8 (scale {with_scale}, {kernel})")
 
 
 @pytest.mark.parametrize("device_offset", [False, True])
@@ -82,17 +87,54 @@ def test_mxfp8_group_offset_and_kept_rows(device_offset):
 
 
 def test_unit_block_scales_equal_the_plain_decoding_kernel(monkeypatch):
-    # E8M0 127 is 1: the result is the decoding kernel's without block scales, bit for bit
+    # E8M0 127 is 1: on the decoding kernel the result is the one without block scales, bit for bit
     m, k, n, L = 120, 384, 256, 4
     lhs = W.normal((m, k), 1.0, 81, DEV)
     rhs = W.weights("e4m3", (L, n, k), 82, DEV)
     sizes = torch.tensor([30, 0, 50, 40], dtype=torch.int32, device=DEV)
     ones = torch.full((L, n, k // 32), 127, dtype=torch.uint8, device=DEV)
-    with_mx = G.gmm(lhs, rhs, sizes, rhs_block_scale=ones, out_dtype=torch.float32)
     use_options(monkeypatch, e4m3_kernel="decode")
+    with_mx = G.gmm(lhs, rhs, sizes, rhs_block_scale=ones, out_dtype=torch.float32)
     plain = G.gmm(lhs, rhs, sizes, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(with_mx, plain)
+
+
+def test_mxfp8_marked_rows_are_summed_again_with_their_block_scales():
+    # activation steps the fp16 split cannot hold mark their rows, which are summed again from
+    # the stored values with the E8M0 scales; a zero block (E8M0 255) and 2^-127 included
+    m, k, n, L = 24, 512, 256, 2
+    x = W.normal((m, k), 1.0, 141).float()
+    x[3, ::128] = 1.0
+    x[3, 1::128] = 1.5 * 2.0 ** -40
+    x[5] = x[5] * torch.pow(2.0, torch.linspace(-40, 10, k))
+    x[7, ::128] = 3e4
+    x[7, 5::128] = 2.0 ** -30
+    lhs = x.to(torch.bfloat16).to(DEV)
+    rhs = W.weights("e4m3", (L, n, k), 142, DEV)
+    mx = _mx_scales((L, n, k // 32), 143).to(DEV)
+    sizes = np.array([10, 14], np.int32)
+    out = G.gmm(lhs, rhs, torch.tensor(sizes, device=DEV), rhs_block_scale=mx, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = _oracle(lhs, rhs, sizes, mx)
+    check_close(out, ref, mag, "MXFP8 with marked rows")
+
+
+def test_mxfp8_scales_off_four_byte_alignment_take_the_decoding_kernel():
+    m, k, n, L = 64, 256, 128, 2
+    lhs = W.normal((m, k), 1.0, 151, DEV)
+    rhs = W.weights("e4m3", (L, n, k), 152, DEV)
+    mx = _mx_scales((L, n, k // 32), 153)
+    store = torch.empty(mx.numel() + 1, dtype=torch.uint8, device=DEV)
+    store[1:] = mx.reshape(-1).to(DEV)
+    shifted = store[1:].view(L, n, k // 32)  # one byte past an aligned allocation
+    sizes = np.array([40, 24], np.int32)
+    out = G.gmm(lhs, rhs, torch.tensor(sizes, device=DEV), rhs_block_scale=shifted, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert G.read_device_errors() == 0
+    ref, mag = _oracle(lhs, rhs, sizes, mx)
+    check_close(out, ref, mag, "MXFP8, scales at an odd address")
 
 
 def test_mxfp8_decode_workload_sampled_rows():
