@@ -574,7 +574,7 @@ def run_suite(dev, peaks):
     del fd, o, q, a_scale, e8
     torch.cuda.empty_cache()
 
-    # Microscaling weights on the decode workload (bf16 activations, the decoding kernel):
+    # Microscaling weights on the decode workload (bf16 activations, the fp16-weight kernel):
     # MXFP8 (e4m3, an E8M0 scale per 32 k of a weight row) and NVFP4 (e2m1, an e4m3 scale per 16 k).
     for name, fmt, per in (("decode_mxfp8_weights", "e4m3", 32), ("decode_nvfp4_weights", "e2m1", 16)):
         fd = W.fp8_decode(dev, fmt=fmt)

@@ -96,11 +96,13 @@ enum {
  *    terms rounded up to 256, then 8 m ceil(k / 256) bytes of step scales; the
  *    fp8 kernel reads the terms instead of splitting every row again for each
  *    128-wide weight tile, and the result is the same, bit for bit;
- *  - int8 and int4 weights: 256 bytes of flags, then 2 m k bytes of fp16
- *    values rounded up to 256, then 8 m k / 128 bytes of (scale, mark) pairs;
- *    the weights are then rewritten as fp16 and multiplied on the fp16 tensor
- *    cores.  Both ways give exact products and fp32 sums, but the sums may
- *    round differently from the in-kernel split's.
+ *  - int8 and int4 weights, and MXFP8 and NVFP4 block-scaled weights
+ *    (gmm_ex): 256 bytes of flags, then 2 m k bytes of fp16 values rounded up
+ *    to 256, then 8 m k / 128 bytes of (scale, mark) pairs; the weights are
+ *    then rewritten as fp16 and multiplied on the fp16 tensor cores.  Both
+ *    ways give exact products and fp32 sums, but the sums may round
+ *    differently from the in-kernel split's.  (The e4m3 and e2m1 sizes below
+ *    cover this layout too.)
  * With a smaller workspace (at least GMM_WORKSPACE_MIN_BYTES) the fp8 kernel
  * splits inside (e4m3 terms, for every format).
  */
@@ -317,14 +319,19 @@ int gmm_device_offset(const void* lhs, int lhs_dtype, int64_t m, int64_t k, cons
  *                      MXFP8: E4M3 rhs, GMM_DTYPE_E8M0 scales, block_size 32;
  *                      NVFP4: E2M1 rhs, GMM_DTYPE_E4M3 scales, block_size 16 (the second-level
  *                      fp32 scale of NVFP4 is rhs_scale with num_quant_blocks = 1).
- *                    MXFP8 runs on the decoding kernel: the decoders multiply each decoded bf16
- *                    weight by its block scale, exactly while the product stays in bf16's normal
- *                    range.  NVFP4 runs on the fp16-weight kernel (an fp16 split of the bf16 lhs
- *                    in the workspace, like int4) when k % 256 == 0, the scales are 16-byte
- *                    aligned and the workspace holds the split: each e2m1 code times its e4m3
- *                    scale is an exact fp16 weight; otherwise on the decoding kernel (an e2m1
- *                    value times an e4m3 value always fits bf16).  No other alignment
- *                    requirement for the scales.
+ *                    MXFP8 runs on the fp16-weight kernel (an fp16 split of the bf16 lhs in the
+ *                    workspace, like int8) when the scales are 4-byte aligned, the workspace
+ *                    holds the split and options->e4m3_kernel is not GMM_E4M3_DECODE: the e4m3
+ *                    codes are exact fp16 weights, each 32-k block sums into its own fp32
+ *                    accumulator, and the block's sum is multiplied by its power of two (exact
+ *                    while it stays in fp32's range).  Otherwise it runs on the decoding kernel:
+ *                    the decoders multiply each decoded bf16 weight by its block scale, exactly
+ *                    while the product stays in bf16's normal range.  NVFP4 runs on the
+ *                    fp16-weight kernel (an fp16 split of the bf16 lhs in the workspace, like
+ *                    int4) when k % 256 == 0, the scales are 16-byte aligned and the workspace
+ *                    holds the split: each e2m1 code times its e4m3 scale is an exact fp16
+ *                    weight; otherwise on the decoding kernel (an e2m1 value times an e4m3 value
+ *                    always fits bf16).  No other alignment requirement for the scales.
  *   keep_other_rows  0: rows outside the local groups are set to 0 (gmm); 1: they keep the
  *                    caller's contents (gmm_into).
  *   Everything else as gmm().  e4m3 activations are taken as they are: each 128-wide k

@@ -1,4 +1,4 @@
-// Grouped matmul with int8, int4, uint4 or NVFP4 weights on the fp16 tensor cores:
+// Grouped matmul with int8, int4, uint4, NVFP4 or MXFP8 weights on the fp16 tensor cores:
 //   out[r, c] = sum_b s[g, b, c] * sum_{kk in block b} lhs[r, kk] * W(g, c, kk) + bias[g, c]
 // (page "tpu-inference 0.12.0.dev20251213 -> 0.13.2.dev20251230", gmm.py:
 // _accum scales each quant block's partial sum by rhs_scale[g, b, 0, n] and adds
