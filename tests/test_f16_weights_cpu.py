@@ -11,6 +11,10 @@ float16 and checked, for every code, against the oracle's format decoders:
   value; times 2^14 and then times its block's e4m3 scale, both fp16 multiplications are exact
   for every code and every finite scale (the products have at most 6 significant bits, lie
   within 6 * 448 and on fp16's grid).
+- MXFP8: every e4m3fn code is an fp16 value (the two NaN codes are NaN), and the kernel's fold of
+  one 16-column accumulator per 32-k block, each scaled by its E8M0 byte of the step's 4-byte
+  word (byte q for block q), reproduces the definition: a host statement of that fold against
+  the oracle.
 """
 
 import numpy as np
@@ -123,3 +127,65 @@ def test_nvfp4_code_times_scale_is_exact_in_fp16():
     want = w[:, None] * scales[None, :]
     np.testing.assert_array_equal(got, want)
     assert np.abs(want).max() <= 6 * 448
+
+
+def test_e4m3_codes_to_fp16_exact():
+    codes = np.arange(256, dtype=np.uint8).reshape(1, -1)
+    v = oracle.decode(codes, oracle.E4M3).ravel()
+    nan = np.isnan(v)
+    assert sorted(np.flatnonzero(nan).tolist()) == [0x7F, 0xFF]
+    np.testing.assert_array_equal(v[~nan].astype(np.float16).astype(np.float64), v[~nan])
+
+
+def _e8m0(b):
+    return 0.0 if b == 255 else 2.0 ** (int(b) - 127)
+
+
+def test_mxfp8_block_fold_matches_oracle():
+    """The kernel's arithmetic for one (row, weight row), restated: per 128-wide step the row is
+    stored as fp16 x / sc (sc = 2^(E - 141), E the exponent field of the step's largest |x|, at
+    least 15); each 32-k block q sums the exact products (x / sc) w into fp32 (D_q); the epilogue
+    reads the step's E8M0 word e4 and adds u_q * (sc * D_q), u_q = s_w * 2^(e_q - 127) with e_q
+    = byte q of e4, the two halves of the word in order."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.Generator(np.random.PCG64(11))
+    m, k, n = 3, 256, 5
+    x = torch.from_numpy(rng.standard_normal((m, k)).astype(np.float32)).to(torch.bfloat16)
+    x[1] = x[1] * 2.0 ** 20
+    xb = x.view(torch.uint16).numpy()
+    xv = x.float().numpy().astype(np.float64)
+    codes = rng.integers(0, 256, size=(1, n, k), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN weights
+    w = oracle.decode(codes.reshape(n, k), oracle.E4M3).reshape(n, k)
+    e = rng.integers(118, 137, size=(1, n, k // 32), dtype=np.uint8)
+    e[0, 1, 0], e[0, 2, 5] = 255, 0
+    ref, mag = oracle.gmm(xb, codes, np.array([m], np.int32), rhs_dtype=oracle.E4M3, rhs_block_scale=e,
+                          rhs_block_scale_dtype=oracle.E8M0)
+    got = np.zeros((m, n))
+    for r in range(m):
+        for c in range(n):
+            acc = np.float32(0.0)
+            for ks in range(k // 128):
+                seg = slice(128 * ks, 128 * ks + 128)
+                big = int(np.abs(xb[r, seg].astype(np.int64) & 0x7FFF).max()) >> 7
+                sc = 2.0 ** (max(big, 15) - 141)
+                h = (xv[r, seg] / sc).astype(np.float16).astype(np.float64)
+                assert np.array_equal(h * sc, xv[r, seg])  # the split holds these rows exactly
+                d = [np.float32(np.sum(h[32 * q:32 * q + 32] * w[c, 128 * ks + 32 * q:128 * ks + 32 * q + 32]))
+                     for q in range(4)]
+                e4 = int.from_bytes(bytes(e[0, c, 4 * ks:4 * ks + 4]), "little")
+                for half in range(2):
+                    u0 = np.float32(_e8m0((e4 >> (16 * half)) & 255))
+                    u1 = np.float32(_e8m0((e4 >> (16 * half + 8)) & 255))
+                    s = np.float32(sc)
+                    acc = np.float32(acc + u0 * (s * d[2 * half]))
+                    acc = np.float32(acc + u1 * (s * d[2 * half + 1]))
+            got[r, c] = acc
+    bound = 4 * 2.0 ** -24 * (k // 32 + 8) * mag
+    assert np.all(np.abs(got - ref) <= bound + 1e-300), np.max(np.abs(got - ref) / np.maximum(mag, 1e-300))
+    # a wrong byte-to-block mapping (the halves swapped) does not pass
+    swapped = e.copy()
+    swapped[0, :, 0::4], swapped[0, :, 2::4] = e[0, :, 2::4], e[0, :, 0::4]
+    ref_sw, _ = oracle.gmm(xb, codes, np.array([m], np.int32), rhs_dtype=oracle.E4M3, rhs_block_scale=swapped,
+                           rhs_block_scale_dtype=oracle.E8M0)
+    assert not np.all(np.abs(got - ref_sw) <= bound)
