@@ -191,10 +191,10 @@ struct Cfg {
   static_assert((kSplit ? 4 * BT : BT) <= SUB_COLS, "sub-tile accumulator width");
   static_assert(kConv || RAWST == NDONE, "raw stages are freed through the step-done ring");
   static_assert(BST <= NDONE && CST <= NDONE, "step-done ring indexing");
-  // Issuer i takes the steps j with j % kIssuers == i: a ring the issuers wait on must be a
-  // multiple of kIssuers deep, so that step j + depth has the same waiter as step j (another
-  // warp could begin its parity wait a phase early and pass it at once).
-  static_assert(NACC % kIssuers == 0 && BST % kIssuers == 0 && (kConv ? CST : RAWST) % kIssuers == 0,
+  // Issuer i takes the steps j with j % kIssuers == i: a ring the issuers wait on must be at
+  // least kIssuers deep, or the issuer of step j + depth (another warp) could begin its parity
+  // wait a phase early and pass it at once.
+  static_assert(NACC >= kIssuers && BST >= kIssuers && (kConv ? CST : RAWST) >= kIssuers,
                 "rings the MMA issuers wait on");
   static_assert(OFF_ABORT + 4 <= OFF_OFFS, "control block overlaps the tables");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");

@@ -1,0 +1,201 @@
+"""The fp16-weight kernel's pipeline protocol (gemm_f16w.cu), modelled on the CPU: its roles and
+mbarrier rings as the kernel runs them, under many random schedules.
+
+Each role is a generator of the kernel's waits and arrivals. A parity wait passes as the hardware
+lets it, when the barrier's phase count has the other parity, and the test checks two things:
+- each wait passes on the phase it means, not one a full parity cycle earlier (phase aliasing:
+  a waiter that begins a phase early and passes at once);
+- each arrival lands in the phase it is meant for.
+Every schedule must also run to its end (no deadlock). The ring depths are read from the kernel
+source. The rule the model bears out: a ring the MMA issuers wait on must be at least as deep as
+there are issuers. Negative controls show that the check catches shallower rings, among them the
+layout that returned wrong sums (3 A stages and 5 accumulator slots for MXFP8 with 4 MMA
+issuers)."""
+
+import os
+import random
+import re
+
+import pytest
+
+SRC = os.path.join(os.path.dirname(__file__), "..", "moe_grouped_matrix_gb300", "csrc", "gemm_f16w.cu")
+
+
+def constants():
+    text = open(SRC).read()
+    out = {}
+    for name in ("RAWST", "CST", "BST", "NACC", "NDONE", "NSC", "kIssuers", "kConvWarps", "BT"):
+        m = re.search(rf"constexpr (?:int|uint32_t) {name} = (\d+);", text)
+        assert m, name
+        out[name] = int(m.group(1))
+    # MX_NACC = A_COL0 / MX_SLOT_COLS with A_COL0 = NACC * SLOT_COLS and MX_SLOT_COLS = 4 * BT
+    slot_cols = int(re.search(r"constexpr int SLOT_COLS = (\d+);", text).group(1))
+    assert re.search(r"constexpr int MX_NACC = A_COL0 / MX_SLOT_COLS;", text)
+    out["MX_NACC"] = out["NACC"] * slot_cols // (4 * out["BT"])
+    return out
+
+
+class Barrier:
+    def __init__(self, name, count):
+        self.name, self.count, self.arrived, self.done = name, count, 0, 0
+
+    def arrive(self, phase, errors):
+        if phase != self.done:
+            errors.append(f"{self.name}: arrival meant for phase {phase} landed in phase {self.done}")
+        self.arrived += 1
+        if self.arrived == self.count:
+            self.arrived = 0
+            self.done += 1
+
+
+def wait_full(bar, q):
+    """Wait for phase q of `bar` to complete (parity q & 1)."""
+    return ("wait", bar, q & 1, q + 1)
+
+
+def roles(c, steps, spr, nacc, cst):
+    """The kernel's roles over `steps` steps of one CTA (spr steps per raw box)."""
+    RAWST, BST, NDONE, NSC = c["RAWST"], c["BST"], c["NDONE"], c["NSC"]
+    ISS, CONV = c["kIssuers"], c["kConvWarps"]
+    rawfull = [Barrier(f"rawfull{s}", 1) for s in range(RAWST)]
+    rawempty = [Barrier(f"rawempty{s}", CONV) for s in range(RAWST)]
+    convfull = [Barrier(f"convfull{s}", CONV) for s in range(cst)]
+    stepdone = [Barrier(f"stepdone{s}", 1) for s in range(NDONE)]
+    acce = [Barrier(f"acce{s}", 4) for s in range(nacc)]
+    bfull = [Barrier(f"bfull{s}", 1) for s in range(BST)]
+    sfull = [Barrier(f"sfull{s}", 1) for s in range(NSC)]
+    sempty = [Barrier(f"sempty{s}", 4) for s in range(NSC)]
+    boxes = (steps + spr - 1) // spr
+
+    def step_done(j, depth):  # wait_step_done(j, depth): the MMAs of step j - depth are complete
+        if j >= depth:
+            yield wait_full(stepdone[(j - depth) % NDONE], (j - depth) // NDONE)
+
+    def raw_producer():
+        for b in range(boxes):
+            # the empty wait: phase b / RAWST - 1 complete (b < RAWST: passes at once)
+            yield wait_full(rawempty[b % RAWST], b // RAWST - 1)
+            yield ("async", None, rawfull[b % RAWST], b // RAWST)
+
+    def b_producer():
+        for j in range(steps):
+            yield from step_done(j, BST)
+            yield ("async", None, bfull[j % BST], j // BST)
+
+    def issuer(mine):
+        for j in range(steps):
+            if j % ISS != mine:
+                continue
+            yield wait_full(acce[j % nacc], j // nacc - 1)
+            yield wait_full(convfull[j % cst], j // cst)
+            yield wait_full(bfull[j % BST], j // BST)
+            # the commit arrives once the step's MMAs complete, in issue order per thread
+            yield ("async", f"issuer{mine}", stepdone[j % NDONE], j // NDONE)
+
+    def converter():
+        for j in range(steps):
+            h, box = j % spr, j // spr
+            if h == 0:
+                yield wait_full(rawfull[box % RAWST], box // RAWST)
+            yield from step_done(j, cst)
+            if h == spr - 1 or j + 1 == steps:
+                yield ("arrive", rawempty[box % RAWST], box // RAWST)
+            yield ("arrive", convfull[j % cst], j // cst)
+
+    def epilogue():
+        for j in range(steps):
+            yield wait_full(stepdone[j % NDONE], j // NDONE)
+            yield wait_full(sfull[j % NSC], j // NSC)
+            yield ("arrive", acce[j % nacc], j // nacc)
+            yield ("arrive", sempty[j % NSC], j // NSC)
+
+    def scale(mine):
+        for j in range(steps):
+            if j % 2 != mine:
+                continue
+            yield wait_full(sempty[j % NSC], j // NSC - 1)
+            yield ("async", None, sfull[j % NSC], j // NSC)
+
+    gens = [raw_producer(), b_producer()] + [issuer(i) for i in range(ISS)]
+    gens += [converter() for _ in range(CONV)] + [epilogue() for _ in range(4)] + [scale(i) for i in range(2)]
+    return gens
+
+
+def run(c, steps, spr, nacc, cst, seed):
+    rng = random.Random(seed)
+    gens = roles(c, steps, spr, nacc, cst)
+    speed = [rng.choice((0.05, 0.3, 1.0, 3.0)) for _ in gens]  # some roles run far ahead
+    ops = [next(g, None) for g in gens]
+    fifo = {}      # in-order completions (one issuing thread's commits)
+    loose = []     # completions in any order (copies)
+    errors = []
+    while True:
+        cand = []
+        for i, op in enumerate(ops):
+            if op is None:
+                continue
+            if op[0] == "wait":
+                _, bar, parity, _ = op
+                if (bar.done & 1) != parity:
+                    cand.append(("role", i))
+            else:
+                cand.append(("role", i))
+        cand += [("fifo", k) for k, v in fifo.items() if v]
+        cand += [("loose", k) for k in range(len(loose))]
+        if not cand:
+            if any(op is not None for op in ops) or loose or any(fifo.values()):
+                errors.append("deadlock")
+            return errors
+        weights = [speed[x[1]] if x[0] == "role" else 0.5 for x in cand]
+        kind, i = rng.choices(cand, weights)[0]
+        if kind == "fifo":
+            bar, phase = fifo[i].pop(0)
+            bar.arrive(phase, errors)
+            continue
+        if kind == "loose":
+            bar, phase = loose.pop(i)
+            bar.arrive(phase, errors)
+            continue
+        op = ops[i]
+        if op[0] == "wait":
+            _, bar, _, target = op
+            if bar.done != target:
+                errors.append(f"{bar.name}: a wait for completion {target} passed at {bar.done}")
+        elif op[0] == "arrive":
+            op[1].arrive(op[2], errors)
+        else:
+            _, key, bar, phase = op
+            if key is None:
+                loose.append((bar, phase))
+            else:
+                fifo.setdefault(key, []).append((bar, phase))
+        ops[i] = next(gens[i], None)
+
+
+C = constants()
+
+
+@pytest.mark.parametrize("fmt,spr,nacc", [("int8", 1, C["NACC"]), ("4-bit", 2, C["NACC"]),
+                                           ("MXFP8", 1, C["MX_NACC"])])
+def test_shipped_rings_never_alias(fmt, spr, nacc):
+    for seed in range(40):
+        errors = run(C, 37, spr, nacc, C["CST"], seed)
+        assert not errors, (fmt, seed, errors[:3])
+
+
+def test_a_ring_shallower_than_the_issuer_count_is_caught():
+    # 3 A stages and 5 accumulator slots with 4 issuers: the issuer of step j + 3 is another
+    # warp than step j's, and begins its wait on the shared A-stage barrier a phase early
+    found = [e for seed in range(40) for e in run(C, 37, 1, 5, 3, seed)]
+    assert any("convfull" in e and "passed at" in e for e in found), found[:3]
+    shallow_b = dict(C, BST=C["kIssuers"] - 1)
+    found = [e for seed in range(40) for e in run(shallow_b, 37, 1, C["NACC"], C["CST"], seed)]
+    assert any("bfull" in e and "passed at" in e for e in found), found[:3]
+    found = [e for seed in range(40) for e in run(C, 37, 1, C["kIssuers"] - 1, C["CST"], seed)]
+    assert any("acce" in e for e in found), found[:3]
+
+
+@pytest.mark.parametrize("nacc,cst", [(5, 4), (4, 5), (6, 6)])
+def test_depths_at_least_the_issuer_count_need_not_be_multiples(nacc, cst):
+    for seed in range(25):
+        assert not run(C, 37, 1, nacc, cst, seed)
