@@ -199,3 +199,15 @@ def test_a_ring_shallower_than_the_issuer_count_is_caught():
 def test_depths_at_least_the_issuer_count_need_not_be_multiples(nacc, cst):
     for seed in range(25):
         assert not run(C, 37, 1, nacc, cst, seed)
+
+
+def test_the_256k_step_layout_needs_fewer_issuers():
+    # The 256-k step layout (4 raw stages, 6 activation stages, 3 A stages of 128 columns and 4
+    # accumulator slots: all of TMEM) with 4 issuers: its A-stage ring is shallower than the
+    # issuer count, and schedules alias and deadlock, as that build's wait timeouts did on the
+    # GPU.  With 3 issuers every schedule runs clean.
+    layout = dict(C, RAWST=4, BST=6, NDONE=8, NSC=8)
+    found = [e for seed in range(40) for e in run(dict(layout, kIssuers=4), 37, 1, 4, 3, seed)]
+    assert "deadlock" in found and any("convfull" in e and "passed at" in e for e in found)
+    for seed in range(40):
+        assert not run(dict(layout, kIssuers=3), 37, 1, 4, 3, seed)
