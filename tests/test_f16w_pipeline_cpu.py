@@ -1,22 +1,18 @@
 """The fp16-weight kernel's pipeline protocol (gemm_f16w.cu), modelled on the CPU: its roles and
-mbarrier rings as the kernel runs them, under many random schedules.
-
-Each role is a generator of the kernel's waits and arrivals. A parity wait passes as the hardware
-lets it, when the barrier's phase count has the other parity, and the test checks two things:
-- each wait passes on the phase it means, not one a full parity cycle earlier (phase aliasing:
-  a waiter that begins a phase early and passes at once);
-- each arrival lands in the phase it is meant for.
-Every schedule must also run to its end (no deadlock). The ring depths are read from the kernel
-source. The rule the model bears out: a ring the MMA issuers wait on must be at least as deep as
+mbarrier rings as the kernel runs them, under many random schedules (pipeline_model.py). Every
+wait must pass on the phase it means, every arrival land in its phase, and every schedule run to
+its end. The ring depths are read from the kernel source. The rule the model bears out: a ring the MMA issuers wait on must be at least as deep as
 there are issuers. Negative controls show that the check catches shallower rings, among them the
 layout that returned wrong sums (3 A stages and 5 accumulator slots for MXFP8 with 4 MMA
 issuers)."""
 
 import os
-import random
 import re
 
 import pytest
+
+import pipeline_model as model
+from pipeline_model import ring, wait_full
 
 SRC = os.path.join(os.path.dirname(__file__), "..", "moe_grouped_matrix_gb300", "csrc", "gemm_f16w.cu")
 
@@ -35,36 +31,14 @@ def constants():
     return out
 
 
-class Barrier:
-    def __init__(self, name, count):
-        self.name, self.count, self.arrived, self.done = name, count, 0, 0
-
-    def arrive(self, phase, errors):
-        if phase != self.done:
-            errors.append(f"{self.name}: arrival meant for phase {phase} landed in phase {self.done}")
-        self.arrived += 1
-        if self.arrived == self.count:
-            self.arrived = 0
-            self.done += 1
-
-
-def wait_full(bar, q):
-    """Wait for phase q of `bar` to complete (parity q & 1)."""
-    return ("wait", bar, q & 1, q + 1)
-
-
 def roles(c, steps, spr, nacc, cst):
     """The kernel's roles over `steps` steps of one CTA (spr steps per raw box)."""
     RAWST, BST, NDONE, NSC = c["RAWST"], c["BST"], c["NDONE"], c["NSC"]
     ISS, CONV = c["kIssuers"], c["kConvWarps"]
-    rawfull = [Barrier(f"rawfull{s}", 1) for s in range(RAWST)]
-    rawempty = [Barrier(f"rawempty{s}", CONV) for s in range(RAWST)]
-    convfull = [Barrier(f"convfull{s}", CONV) for s in range(cst)]
-    stepdone = [Barrier(f"stepdone{s}", 1) for s in range(NDONE)]
-    acce = [Barrier(f"acce{s}", 4) for s in range(nacc)]
-    bfull = [Barrier(f"bfull{s}", 1) for s in range(BST)]
-    sfull = [Barrier(f"sfull{s}", 1) for s in range(NSC)]
-    sempty = [Barrier(f"sempty{s}", 4) for s in range(NSC)]
+    rawfull, rawempty = ring("rawfull", RAWST, 1), ring("rawempty", RAWST, CONV)
+    convfull, stepdone = ring("convfull", cst, CONV), ring("stepdone", NDONE, 1)
+    acce, bfull = ring("acce", nacc, 4), ring("bfull", BST, 1)
+    sfull, sempty = ring("sfull", NSC, 1), ring("sempty", NSC, 4)
     boxes = (steps + spr - 1) // spr
 
     def step_done(j, depth):  # wait_step_done(j, depth): the MMAs of step j - depth are complete
@@ -122,54 +96,7 @@ def roles(c, steps, spr, nacc, cst):
 
 
 def run(c, steps, spr, nacc, cst, seed):
-    rng = random.Random(seed)
-    gens = roles(c, steps, spr, nacc, cst)
-    speed = [rng.choice((0.05, 0.3, 1.0, 3.0)) for _ in gens]  # some roles run far ahead
-    ops = [next(g, None) for g in gens]
-    fifo = {}      # in-order completions (one issuing thread's commits)
-    loose = []     # completions in any order (copies)
-    errors = []
-    while True:
-        cand = []
-        for i, op in enumerate(ops):
-            if op is None:
-                continue
-            if op[0] == "wait":
-                _, bar, parity, _ = op
-                if (bar.done & 1) != parity:
-                    cand.append(("role", i))
-            else:
-                cand.append(("role", i))
-        cand += [("fifo", k) for k, v in fifo.items() if v]
-        cand += [("loose", k) for k in range(len(loose))]
-        if not cand:
-            if any(op is not None for op in ops) or loose or any(fifo.values()):
-                errors.append("deadlock")
-            return errors
-        weights = [speed[x[1]] if x[0] == "role" else 0.5 for x in cand]
-        kind, i = rng.choices(cand, weights)[0]
-        if kind == "fifo":
-            bar, phase = fifo[i].pop(0)
-            bar.arrive(phase, errors)
-            continue
-        if kind == "loose":
-            bar, phase = loose.pop(i)
-            bar.arrive(phase, errors)
-            continue
-        op = ops[i]
-        if op[0] == "wait":
-            _, bar, _, target = op
-            if bar.done != target:
-                errors.append(f"{bar.name}: a wait for completion {target} passed at {bar.done}")
-        elif op[0] == "arrive":
-            op[1].arrive(op[2], errors)
-        else:
-            _, key, bar, phase = op
-            if key is None:
-                loose.append((bar, phase))
-            else:
-                fifo.setdefault(key, []).append((bar, phase))
-        ops[i] = next(gens[i], None)
+    return model.run(roles(c, steps, spr, nacc, cst), seed)
 
 
 C = constants()
