@@ -11,7 +11,6 @@ run to its end. The ring depths are those of the kernel's configuration, whose f
 checks in the source first."""
 
 import os
-import re
 
 import pytest
 
@@ -21,7 +20,7 @@ from pipeline_model import ring, wait_full
 SRC = os.path.join(os.path.dirname(__file__), "..", "moe_grouped_matrix_gb300", "csrc", "gemm_fp8.cuh")
 
 
-def test_the_modelled_configuration_is_the_source_s():
+def test_the_modelled_depths_are_the_kernel_s_own():
     text = open(SRC).read()
     for line in ("static constexpr int QPS = F == WFmt::kInt8 ? 1 : 2;",
                  "static constexpr int RAWST = 4;",

@@ -10,7 +10,7 @@ import oracle
 import moe_grouped_matrix_gb300 as G
 from moe_grouped_matrix_gb300 import build as B
 from moe_grouped_matrix_gb300 import workloads as W
-from parity import bits, check_close, oracle_gmm, use_options
+from parity import check_close, oracle_gmm, use_options
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
