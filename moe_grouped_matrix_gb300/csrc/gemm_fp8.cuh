@@ -1378,7 +1378,8 @@ cudaError_t launch_format(const ScaledLaunch& L, int grid, cudaStream_t stream) 
   Params p{L.group_sizes, L.num_total_groups, L.group_offset, L.num_local_groups, L.m, L.n, L.k, L.scale,
            L.num_blocks, L.bias, L.bias_f32, L.out, L.err, L.zero_rest, L.group_offset_dev, L.scale_e8m0,
            L.lhs_scale, L.num_lhs_blocks, static_cast<const uint16_t*>(L.lhs_raw),
-           static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k)};
+           static_cast<const uint8_t*>(L.rhs_raw), k4 ? int64_t(L.k) / 2 : int64_t(L.k),
+           /*w_block_scale=*/nullptr};  // block-scaled weights run on the other kernels
   if constexpr (kPS) {
     // Launched as the programmatic dependent of the split-rows kernel just
     // before it in the stream: the prologue and the weight stream overlap that
