@@ -120,7 +120,7 @@ def test_pair_kernels(src):
         assert not errors, (src, seed, errors[:3])
 
 
-def test_a_follower_that_waited_on_the_leader_s_ring_only_is_caught():
+def test_a_follower_producer_without_its_empty_wait_is_caught():
     # a control: a pair whose follower producer skipped its own empty wait would copy into a
     # stage the MMAs may still read, and its bytes would land in the wrong phase
     n = stages("gemm_bf16_2sm.cu")
